@@ -1,0 +1,362 @@
+"""Benchmark: exact attention forward + backward on GB300, one JSON line.
+
+A step is one pass of the whole path on one batch: fa_fwd, fa_bwd_preprocess
+and fa_bwd (dK/dV kernel then dQ kernel) on the long causal training shape
+B=1, H=32, N=16384, D=128, bf16.  `value` is forward+backward TFLOP/s over all
+ranks (forward 4*B*H*N^2*D flops halved for causal, backward credited at 2.5x
+the forward), timed with CUDA events on the launching stream, inputs resident
+in HBM.  The inputs (4 x 128 MiB) are larger than the 129 MB L2, so L2 is not
+flushed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+Under torchrun each rank runs its own copy of the workload (independent heads,
+no collective on the data path; weak scaling) and rank 0 prints the line.
+`--impl reference` times the fp64 CPU oracle on a bounded sample (one head) of
+the same workload on the host cores (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from exact_attention_83_gb300.inputs import (LONG_CAUSAL, Workload, bf16_n1024,  # noqa: E402
+                                             make_inputs, sweep)
+
+METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 peak"
+
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
+# the dominant kernel, keyed by the sha256 of the source file it was measured
+# on; a changed source gives null.  Figures come from the summaries under
+# profiles/.
+MEASURED_TRAFFIC = {}
+
+
+def workloads():
+    ws = {LONG_CAUSAL.name: LONG_CAUSAL}
+    for c in (False, True):
+        w = bf16_n1024(c)
+        ws[w.name] = w
+        for N in (1024, 4096, 16384):
+            for dt in ("bf16", "fp16"):
+                s = sweep(N, dt, c)
+                ws[s.name] = s
+    return ws
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_sha(name: str) -> str:
+    path = os.path.join(ROOT, "exact_attention_83_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def run_reference(args, w: Workload):
+    """The fp64 oracle on the host cores, one head of the workload per step."""
+    import oracle
+    sample = Workload(w.name + "-one-head", w.B, 1, w.N, w.D, w.dtype, w.causal, w.layout,
+                      w.qkv_scale, w.seed)
+    q, k, v, do = make_inputs(sample)
+    qn, kn, vn, dn = (t.float().double().numpy() for t in (q, k, v, do))
+    for _ in range(args.warmup):
+        oracle.fwd_bwd(qn, kn, vn, dn, w.causal, w.scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fwd_bwd(qn, kn, vn, dn, w.causal, w.scale)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    tflops = sample.fwd_bwd_flops() / dt / 1e12
+    cores = oracle.num_threads()
+    line = {
+        "metric": METRIC, "impl": "reference", "value": tflops, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": "one head (B=1, H=1) per step",
+                   "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"fp64 oracle fwd+bwd on 1 of {w.B * w.H} heads per step"},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w: Workload):
+    """The oracle as it stands, on one head of the workload (bounded sample)."""
+    import oracle
+    sample = Workload(w.name + "-one-head", w.B, 1, w.N, w.D, w.dtype, w.causal, w.layout,
+                      w.qkv_scale, w.seed)
+    q, k, v, do = make_inputs(sample)
+    qn, kn, vn, dn = (t.float().double().numpy() for t in (q, k, v, do))
+    t0 = time.perf_counter()
+    oracle.fwd_bwd(qn, kn, vn, dn, w.causal, w.scale)
+    dt = time.perf_counter() - t0
+    return {"value": sample.fwd_bwd_flops() / dt / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd on 1 of {w.B * w.H} heads ({dt:.1f} s)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=LONG_CAUSAL.name)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = workloads()[args.workload]
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+
+    from exact_attention_83_gb300 import fa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    fa.load_library()
+
+    q, k, v, do = (t.to(dev) for t in make_inputs(w))
+    B, H, N, D = w.B, w.H, w.N, w.D
+    o = torch.empty((B, H, N, D), dtype=q.dtype, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    delta = torch.empty_like(lse)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fwd(q, k, v, o, lse, w.causal, w.scale)
+        fa.bwd_preprocess(o, do, delta)
+        fa.bwd(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    if fa.device_status() != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    # ---- forward + backward step, with per-kernel events on the stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            e = ev[i]
+            e[0].record(stream)
+            fa.fwd(q, k, v, o, lse, w.causal, w.scale)
+            e[1].record(stream)
+            fa.bwd_preprocess(o, do, delta)
+            fa.set_profile_events(e[2:5])
+            fa.bwd(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale)
+        end.record(stream)
+        barrier()
+    fa.set_profile_events(None)
+    total_ms = max_over_ranks(start.elapsed_time(end))
+    ms_step = total_ms / args.steps
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    pre_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    dq_ms = statistics.median(e[3].elapsed_time(e[4]) for e in ev)
+    if fa.device_status() != 0:
+        raise RuntimeError("device status not OK after the timed region")
+
+    # ---- forward alone
+    barrier()
+    fs, fe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fs.record(stream)
+    for _ in range(args.steps):
+        fa.fwd(q, k, v, o, lse, w.causal, w.scale)
+    fe.record(stream)
+    barrier()
+    fwd_only_ms = max_over_ranks(fs.elapsed_time(fe)) / args.steps
+
+    flops_fwd = w.fwd_flops()
+    flops_step = w.fwd_bwd_flops()
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+    peak_dense = pk["bf16_tflops_sustained"]
+
+    # dominant kernel: the dK/dV kernel (4 of the 7 N x N x D products of the
+    # split backward); its algorithmic flops are 4 products of 2*N^2*D per
+    # head, halved when causal.
+    dkdv_flops = 4 * 2.0 * B * H * N * N * D * (0.5 if w.causal else 1.0)
+    achieved = dkdv_flops / (dkdv_ms * 1e-3) / 1e12
+    sha = kernel_source_sha("fa_bwd_tc.cu")
+    traffic = MEASURED_TRAFFIC.get(("dkdv", sha, w.name))
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, w, dev, fa)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D,
+                       "causal": w.causal, "parallelism": f"replicas{world}",
+                       "l2": "inputs 4 x %d MiB > L2, no flush" % (B * H * N * D * 2 >> 20)},
+            "fwd_tflops": world * flops_fwd / (fwd_only_ms * 1e-3) / 1e12,
+            "fwd_ms": fwd_only_ms,
+            "fwd_frac_of_peak": flops_fwd / (fwd_only_ms * 1e-3) / 1e12 / peak_dense,
+            "fwd_bwd_frac_of_peak": value / world / peak_dense,
+            "peak_tflops": peak_dense, "peak_source": pk["source"] + " sustained bf16",
+            "kernel_ms": {"fwd": fwd_ms, "preprocess": pre_ms, "bwd_dkdv": dkdv_ms,
+                          "bwd_dq": dq_ms},
+            "roofline": {"kernel": "bwd_dkdv", "bound": "tensor", "achieved": achieved,
+                         "peak": peak_dense, "unit": "TFLOP/s", "frac": achieved / peak_dense,
+                         "traffic": traffic},
+            "clocks": clocks.summary(),
+            "gpu_launches": 4 * args.steps,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def measure_e2e(args, w, dev, fa):
+    """Same metric through the public API with host buffers: every step copies
+    Q, K, V, dO from pinned host memory, runs forward and backward, and copies
+    O, dQ, dK, dV back to pinned host memory."""
+    hq, hk, hv, hdo = (t.contiguous().pin_memory() for t in make_inputs(w))
+    outs = [torch.empty(hq.shape, dtype=hq.dtype).pin_memory() for _ in range(4)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        q, k, v, do = (t.to(dev, non_blocking=True) for t in (hq, hk, hv, hdo))
+        o, lse = fa.attention_fwd(q, k, v, w.causal, w.scale)
+        dq, dk, dv = fa.attention_bwd(q, k, v, o, lse, do, w.causal, w.scale)
+        for h, d in zip(outs, (o, dq, dk, dv)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(args.steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = s.elapsed_time(e) / args.steps
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    nbytes = hq.numel() * hq.element_size()
+    return {"value": world * w.fwd_bwd_flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": ms, "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,259 @@
+// The C ABI of libfa: argument validation, per-device set-up and dispatch.
+//
+// Nothing here computes attention; every step of the path runs in the kernels
+// of the other translation units.  Validation happens before any launch, so an
+// invalid call returns its fa_status without touching the device.
+
+#include "fa_internal.h"
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+// Device status word of the current context.  A kernel whose bounded wait
+// runs out stores FA_ERR_TIMEOUT here (first writer wins);
+// fa_get_device_status reads and clears it.  A file-scope device variable, so
+// the library allocates no device memory.
+__device__ unsigned int fa_device_status_word;
+
+namespace fa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+std::atomic<int> g_path{FA_PATH_AUTO};
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+std::mutex g_mu;
+cudaEvent_t g_prof_events[3];
+std::atomic<bool> g_prof_on{false};
+struct DeviceInfo {
+  int state = 0;              // 0: not set up, 1: ready, -1: not sm_103
+  int sm_count = 0;
+  unsigned int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Once per device, with that device current: check the architecture, cache
+// the SM count and the device address of the status word.
+fa_status device_setup(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.state == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+    if (major != 10 || minor != 3) {
+      d.state = -1;
+    } else {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, fa_device_status_word) != cudaSuccess) return FA_ERR_LAUNCH;
+      d.status = static_cast<unsigned int*>(p);
+      d.sm_count = sms;
+      d.state = 1;
+    }
+  }
+  if (d.state < 0) return FA_ERR_ARCH;
+  *out = &d;
+  return FA_OK;
+}
+
+int64_t elem_size(fa_dtype dt) { return dt == FA_F32 ? 4 : 2; }
+
+bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+fa_status check_shape(int64_t B, int64_t H, int64_t N, int64_t D, fa_dtype dt) {
+  if (dt != FA_F32 && dt != FA_F16 && dt != FA_BF16) return FA_ERR_DTYPE;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return FA_ERR_HEADDIM;
+  int64_t bh, bhn, bhnd;
+  if (!mul_ok(B, H, &bh) || !mul_ok(bh, N, &bhn) || !mul_ok(bhn, D * 8, &bhnd)) return FA_ERR_SHAPE;
+  if (bh > (int64_t)INT32_MAX || N > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
+  return FA_OK;
+}
+
+// Checks one [B,H,N,D] tensor and copies its strides into dst.  The stride of
+// a dimension of extent 1 is never used; it is replaced by 0.
+fa_status check_tensor(const void* p, const int64_t* s, int64_t B, int64_t H, int64_t N,
+                       fa_dtype dt, int64_t* dst) {
+  if (!p || !s) return FA_ERR_NULL;
+  if (s[3] != 1) return FA_ERR_STRIDE;
+  const int64_t ext[3] = {B, H, N};
+  const int64_t es = elem_size(dt);
+  if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return FA_ERR_ALIGN;
+  for (int i = 0; i < 3; ++i) {
+    if (ext[i] == 1) { dst[i] = 0; continue; }
+    if (s[i] < 0) return FA_ERR_STRIDE;
+    int64_t bytes;
+    if (!mul_ok(s[i], es, &bytes)) return FA_ERR_SHAPE;
+    if (bytes % 16 != 0) return FA_ERR_ALIGN;
+    dst[i] = s[i];
+  }
+  dst[3] = 1;
+  return FA_OK;
+}
+
+fa_status check_f32_vec(const void* p) {
+  if (!p) return FA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
+fa_status check_scale(float scale) {
+  return (std::isfinite(scale) && scale > 0.f) ? FA_OK : FA_ERR_SCALE;
+}
+
+#define FA_TRY(expr)                   \
+  do {                                 \
+    const fa_status st_ = (expr);      \
+    if (st_ != FA_OK) return st_;      \
+  } while (0)
+
+bool use_tc(fa_dtype dt) { return g_path.load() == FA_PATH_AUTO && dt != FA_F32; }
+
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kMaxDevices && g_dev[dev].state == 1) return g_dev[dev].sm_count;
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 1;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int64_t B, int64_t H, int64_t N, int64_t D,
+                 const int64_t* sq, const int64_t* sk, const int64_t* sv,
+                 const int64_t* so, int causal, float scale, fa_dtype dtype,
+                 cudaStream_t stream) {
+  FwdParams p{};
+  FA_TRY(check_shape(B, H, N, D, dtype));
+  FA_TRY(check_tensor(q, sq, B, H, N, dtype, p.sq));
+  FA_TRY(check_tensor(k, sk, B, H, N, dtype, p.sk));
+  FA_TRY(check_tensor(v, sv, B, H, N, dtype, p.sv));
+  FA_TRY(check_tensor(o, so, B, H, N, dtype, p.so));
+  FA_TRY(check_f32_vec(lse));
+  FA_TRY(check_scale(scale));
+  DeviceInfo* dev = nullptr;
+  FA_TRY(device_setup(&dev));
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+  p.B = B; p.H = H; p.N = N; p.D = D;
+  p.causal = causal ? 1 : 0; p.scale = scale; p.dtype = dtype;
+  p.status = dev->status; p.timeout_ns = g_timeout_ns.load();
+  if (use_tc(dtype) && have_fwd_tc(D, dtype)) return launch_fwd_tc(p, stream);
+  return launch_fwd_ffma(p, stream);
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dout, float* delta,
+                            int64_t B, int64_t H, int64_t N, int64_t D,
+                            const int64_t* so, const int64_t* sdo, fa_dtype dtype,
+                            cudaStream_t stream) {
+  PreParams p{};
+  FA_TRY(check_shape(B, H, N, D, dtype));
+  FA_TRY(check_tensor(o, so, B, H, N, dtype, p.so));
+  FA_TRY(check_tensor(dout, sdo, B, H, N, dtype, p.sdo));
+  FA_TRY(check_f32_vec(delta));
+  DeviceInfo* dev = nullptr;
+  FA_TRY(device_setup(&dev));
+  p.o = o; p.dout = dout; p.delta = delta;
+  p.B = B; p.H = H; p.N = N; p.D = D; p.dtype = dtype;
+  return launch_preprocess(p, stream);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout,
+                 const float* lse, const float* delta, void* dq, void* dk, void* dv,
+                 int64_t B, int64_t H, int64_t N, int64_t D,
+                 const int64_t* sq, const int64_t* sk, const int64_t* sv,
+                 const int64_t* sdo, const int64_t* sdq, const int64_t* sdk,
+                 const int64_t* sdv, int causal, float scale, fa_dtype dtype,
+                 cudaStream_t stream) {
+  BwdParams p{};
+  FA_TRY(check_shape(B, H, N, D, dtype));
+  FA_TRY(check_tensor(q, sq, B, H, N, dtype, p.sq));
+  FA_TRY(check_tensor(k, sk, B, H, N, dtype, p.sk));
+  FA_TRY(check_tensor(v, sv, B, H, N, dtype, p.sv));
+  FA_TRY(check_tensor(dout, sdo, B, H, N, dtype, p.sdo));
+  FA_TRY(check_tensor(dq, sdq, B, H, N, dtype, p.sdq));
+  FA_TRY(check_tensor(dk, sdk, B, H, N, dtype, p.sdk));
+  FA_TRY(check_tensor(dv, sdv, B, H, N, dtype, p.sdv));
+  FA_TRY(check_f32_vec(lse));
+  FA_TRY(check_f32_vec(delta));
+  FA_TRY(check_scale(scale));
+  DeviceInfo* dev = nullptr;
+  FA_TRY(device_setup(&dev));
+  p.q = q; p.k = k; p.v = v; p.dout = dout; p.lse = lse; p.delta = delta;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.B = B; p.H = H; p.N = N; p.D = D;
+  p.causal = causal ? 1 : 0; p.scale = scale; p.dtype = dtype;
+  p.status = dev->status; p.timeout_ns = g_timeout_ns.load();
+  p.prof = g_prof_on.load() ? g_prof_events : nullptr;
+  if (use_tc(dtype) && have_bwd_tc(D, dtype)) return launch_bwd_tc(p, stream);
+  return launch_bwd_ffma(p, stream);
+}
+
+fa_status fa_get_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  DeviceInfo* dev = nullptr;
+  FA_TRY(device_setup(&dev));
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, fa_device_status_word, sizeof(word)) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(fa_device_status_word, &zero, sizeof(zero)) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+  }
+  return static_cast<fa_status>(word);
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_NULL: return "FA_ERR_NULL: a required pointer is NULL";
+    case FA_ERR_SHAPE: return "FA_ERR_SHAPE: B, H or N < 1, or sizes overflow";
+    case FA_ERR_HEADDIM: return "FA_ERR_HEADDIM: D must be 16, 32, 64 or 128";
+    case FA_ERR_DTYPE: return "FA_ERR_DTYPE: unknown dtype";
+    case FA_ERR_STRIDE: return "FA_ERR_STRIDE: d-stride must be 1 and strides non-negative";
+    case FA_ERR_ALIGN: return "FA_ERR_ALIGN: bases and strides must be 16-byte multiples";
+    case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: CUDA error configuring or launching a kernel";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side bounded wait ran out";
+    case FA_ERR_ARCH: return "FA_ERR_ARCH: the current device is not sm_103";
+    case FA_ERR_SCALE: return "FA_ERR_SCALE: scale must be finite and > 0";
+    case FA_ERR_ARG: return "FA_ERR_ARG: invalid argument";
+  }
+  return "unknown fa_status";
+}
+
+fa_status fa_set_path(fa_path path) {
+  if (path != FA_PATH_AUTO && path != FA_PATH_FFMA) return FA_ERR_ARG;
+  g_path.store(path);
+  return FA_OK;
+}
+
+void fa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
+
+void fa_set_profile_events(const cudaEvent_t* events) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (events) {
+    for (int i = 0; i < 3; ++i) g_prof_events[i] = events[i];
+    g_prof_on.store(true);
+  } else {
+    g_prof_on.store(false);
+  }
+}
+
+int fa_version(void) { return 0x000100; }
+
+}  // extern "C"

@@ -1,0 +1,7 @@
+// Tensor-core forward (tcgen05 + TMA) -- not compiled for any shape yet.
+#include "fa_internal.h"
+
+namespace fa {
+bool have_fwd_tc(int64_t, fa_dtype) { return false; }
+fa_status launch_fwd_tc(const FwdParams&, cudaStream_t) { return FA_ERR_ARG; }
+}  // namespace fa

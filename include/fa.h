@@ -1,0 +1,169 @@
+/*
+ * fa.h -- C ABI of libfa: exact scaled-dot-product attention, forward and
+ * backward, in FlashAttention-2 form, for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (sources named by page title and section):
+ *
+ *   S = scale * Q K^T                      per (b, h); Q, K, V are N x D
+ *   causal: key j is kept for query i iff j <= i (top-left aligned)
+ *       ("FlashAttention-2 from PyTorch to Triton", the kernel's causal
+ *        predicate and its test harness)
+ *   L_i = log sum_j exp(S_ij)  (natural log)        P = exp(S - L)
+ *   O   = P V
+ *       ("FlashAttention-2 from PyTorch to Triton", section on the three
+ *        running quantities: L_i = m_i + log(l_i), and the backward's
+ *        recovery of P as exp(S - L))
+ *   Delta_i = sum_d dO_id O_id
+ *       ("Triton FlashAttention", project summary: rowsum(dO.O) is computed
+ *        by its own small kernel; "FlashAttention-2 from PyTorch to Triton",
+ *        defect 5: the precomputed D = rowsum(dO o O))
+ *   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - Delta),
+ *   dQ = scale dS K,  dK = scale dS^T Q
+ *       (the standard softmax-attention gradient; "Triton FlashAttention":
+ *        a dK/dV kernel and a dQ kernel, no atomics, P rebuilt from L)
+ *
+ * Tensors.  Q, K, V, O, dO, dQ, dK, dV are logical [B, H, N, D] arrays of one
+ * element type (fa_dtype) addressed through int64 ELEMENT strides given in the
+ * order (b, h, n, d).  The d-stride must be 1; the others are free (permuted
+ * views such as [B, N, H, D] storage need no copy).  lse and delta are
+ * contiguous fp32 [B, H, N] arrays with 16-byte aligned bases.  All pointers
+ * are device pointers.
+ *
+ * Alignment.  Every tensor base must be 16-byte aligned and every b/h/n stride
+ * times the element size must be a multiple of 16 bytes (tiles move by TMA).
+ *
+ * Shapes.  B, H, N >= 1; D in {16, 32, 64, 128}; Q, K and V share N.
+ * scale must be finite and > 0 (use 1/sqrt(D) for standard attention).
+ *
+ * Ownership.  The caller allocates every buffer.  The library allocates no
+ * device memory per call and keeps no pointer after a call returns.  Inputs are
+ * never written.  Outputs are fully overwritten (no accumulate-into
+ * semantics; dQ, dK, dV need no zeroing).  Output buffers must not overlap
+ * inputs or each other.
+ *
+ * Ordering.  Calls are asynchronous on `stream`.  fa_fwd -> fa_bwd_preprocess
+ * -> fa_bwd must run in that order on one stream (or be ordered by the caller
+ * with events).  The return code reports argument and launch errors only;
+ * a device-side wait that runs out is reported by fa_get_device_status.
+ *
+ * Precision.  fp16/bf16: products on tensor cores with fp32 accumulation; the
+ * probabilities are rounded to the input type before P.V, dS and P^T before
+ * the gradient products; O, dQ, dK, dV are rounded to the input type (RNE).
+ * fp32: IEEE fp32 FFMA throughout (no TF32).
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL = 1,     /* a required pointer is NULL                          */
+  FA_ERR_SHAPE = 2,    /* B, H or N < 1, or the sizes overflow int64          */
+  FA_ERR_HEADDIM = 3,  /* D not in {16, 32, 64, 128}                           */
+  FA_ERR_DTYPE = 4,    /* unknown fa_dtype                                     */
+  FA_ERR_STRIDE = 5,   /* d-stride != 1, or a negative stride                  */
+  FA_ERR_ALIGN = 6,    /* base not 16-byte aligned, or stride*size % 16 != 0   */
+  FA_ERR_LAUNCH = 7,   /* CUDA reported an error configuring or launching      */
+  FA_ERR_TIMEOUT = 8,  /* a device-side bounded wait ran out (see below)       */
+  FA_ERR_ARCH = 9,     /* the current device is not sm_103                      */
+  FA_ERR_SCALE = 10,   /* scale is not finite and > 0                          */
+  FA_ERR_ARG = 11      /* another invalid argument (e.g. an unknown option)    */
+} fa_status;
+
+/*
+ * Forward.  Writes O (caller strides so) and lse = L [B, H, N] fp32, natural
+ * log units: L_i = log sum_j exp(S_ij) over the kept keys.
+ * sq, sk, sv, so: 4 int64 element strides each, order (b, h, n, d).
+ */
+FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int64_t B, int64_t H, int64_t N, int64_t D,
+                 const int64_t* sq, const int64_t* sk, const int64_t* sv,
+                 const int64_t* so, int causal, float scale, fa_dtype dtype,
+                 cudaStream_t stream);
+
+/*
+ * Backward preprocess.  delta[b,h,i] = sum_d dO[b,h,i,d] * O[b,h,i,d], with
+ * the products and the sum in fp32, O being the stored forward output.
+ */
+FA_API fa_status fa_bwd_preprocess(const void* o, const void* dout, float* delta,
+                            int64_t B, int64_t H, int64_t N, int64_t D,
+                            const int64_t* so, const int64_t* sdo, fa_dtype dtype,
+                            cudaStream_t stream);
+
+/*
+ * Backward.  From Q, K, V, dO, the forward's lse and the preprocess's delta,
+ * writes dQ, dK, dV (strides sdq, sdk, sdv).  P is rebuilt tile by tile as
+ * exp(S - L); no N x N matrix is stored.  Runs a dK/dV kernel and then a dQ
+ * kernel on `stream`; neither uses atomics.
+ */
+FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout,
+                 const float* lse, const float* delta, void* dq, void* dk, void* dv,
+                 int64_t B, int64_t H, int64_t N, int64_t D,
+                 const int64_t* sq, const int64_t* sk, const int64_t* sv,
+                 const int64_t* sdo, const int64_t* sdq, const int64_t* sdk,
+                 const int64_t* sdv, int causal, float scale, fa_dtype dtype,
+                 cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns FA_OK, FA_ERR_TIMEOUT if a kernel's bounded wait on
+ * an mbarrier ran out since the last call (that kernel's outputs are then
+ * undefined; the CUDA context stays usable), or FA_ERR_LAUNCH if the stream
+ * reported a CUDA error.
+ */
+FA_API fa_status fa_get_device_status(cudaStream_t stream);
+
+/* Static, NUL-terminated name of a status code. */
+FA_API const char* fa_status_string(fa_status status);
+
+/*
+ * Kernel family selection for later calls in this process (for tests and
+ * benchmarks; the default is FA_PATH_AUTO).
+ *   FA_PATH_AUTO: tensor-core kernels for fp16/bf16 where compiled, FFMA
+ *                 kernels otherwise (always for fp32).
+ *   FA_PATH_FFMA: the FFMA kernels for every dtype.
+ * Returns FA_ERR_ARG for an unknown value.
+ */
+typedef enum { FA_PATH_AUTO = 0, FA_PATH_FFMA = 1 } fa_path;
+FA_API fa_status fa_set_path(fa_path path);
+
+/*
+ * Upper bound, in nanoseconds, on any single device-side wait of the
+ * tensor-core kernels (default 2e9 = 2 s).  When a wait runs out the kernel
+ * records FA_ERR_TIMEOUT, drains its own copies in flight, releases its tensor
+ * memory and returns.  0 restores the default.
+ */
+FA_API void fa_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Profiling hook for benchmarks.  When `events` is non-NULL its three handles
+ * are copied, and every later fa_bwd call records events[0] before its dK/dV
+ * kernel, events[1] between the dK/dV and the dQ kernel, and events[2] after
+ * the dQ kernel, on the call's stream.  NULL turns the hook off.  The caller
+ * creates and destroys the events and must not destroy them while the hook is
+ * on.
+ */
+FA_API void fa_set_profile_events(const cudaEvent_t* events);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+FA_API int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

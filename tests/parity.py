@@ -1,0 +1,145 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI on
+seeded inputs and compare with the fp64 oracle.
+
+Tolerances (stated in the attention spec this library follows): max-abs error
+1e-4 for fp32 and 2e-2 for fp16/bf16, for O, L, dQ, dK and dV at unit-normal
+inputs.  For inputs scaled by 4 the outputs scale too (O by 4, L and the
+gradients of Q and K by ~16), so those cases use tol * max(1, RMS(reference))
+per tensor.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from exact_attention_83_gb300 import fa
+from exact_attention_83_gb300.inputs import Workload, make_inputs
+
+TOL = {"fp32": 1e-4, "fp16": 2e-2, "bf16": 2e-2}
+KEYS = ("o", "lse", "dq", "dk", "dv")
+
+
+def tolerance(w: Workload, key: str, ref: np.ndarray) -> float:
+    t = TOL[w.dtype]
+    if w.qkv_scale != 1.0:
+        rms = float(np.sqrt(np.mean(np.square(ref)))) if ref.size else 0.0
+        t *= max(1.0, rms)
+    return t
+
+
+def run_gpu(w: Workload, inputs=None, backward: bool = True):
+    """Runs fa_fwd (+ fa_bwd_preprocess + fa_bwd) on cuda:0 with NaN-filled
+    outputs; returns (inputs on CPU, dict of CPU float64 numpy outputs)."""
+    if inputs is None:
+        inputs = make_inputs(w, "cpu", with_grad_out=backward)
+    q, k, v, do = inputs
+    dev = torch.device("cuda", 0)
+
+    def to_dev(x):
+        # keep the generated storage order: permute back to storage, copy, re-permute
+        if w.layout == "bnhd":
+            return x.permute(0, 2, 1, 3).contiguous().to(dev).permute(0, 2, 1, 3)
+        return x.contiguous().to(dev)
+
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    B, H, N, D = w.B, w.H, w.N, w.D
+    dt = qd.dtype
+    o = torch.full((B, H, N, D), float("nan"), dtype=dt, device=dev)
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=dev)
+    fa.fwd(qd, kd, vd, o, lse, w.causal, w.scale)
+    out = {"o": o, "lse": lse}
+    if backward:
+        dod = to_dev(do)
+        delta = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=dev)
+        fa.bwd_preprocess(o, dod, delta)
+        dq = torch.full((B, H, N, D), float("nan"), dtype=dt, device=dev)
+        dk = torch.full_like(dq, float("nan"))
+        dv = torch.full_like(dq, float("nan"))
+        fa.bwd(qd, kd, vd, dod, lse, delta, dq, dk, dv, w.causal, w.scale)
+        out.update(delta=delta, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    status = fa.device_status()
+    assert status == 0, f"device status {fa.STATUS_NAMES.get(status, status)}"
+    return inputs, {k_: t.float().cpu().double().numpy() for k_, t in out.items()}
+
+
+def check(name: str, got: np.ndarray, ref: np.ndarray, tol: float):
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{name}: non-finite values (unwritten output?)"
+    err = float(np.abs(got - ref).max()) if ref.size else 0.0
+    assert err <= tol, f"{name}: max abs error {err:.3e} > {tol:.3e}"
+    return err
+
+
+def compare_full(w: Workload, inputs, got, heads=None):
+    """Compare every element of the selected heads (list of (b, h); all heads
+    when None) with the oracle run on those heads alone."""
+    q, k, v, do = inputs
+    if heads is None:
+        sel = (slice(None), slice(None))
+        ref = oracle.fwd_bwd(q, k, v, do, w.causal, w.scale) if do is not None else None
+        if ref is None:
+            o, L = oracle.fwd(q, k, v, w.causal, w.scale)
+            ref = {"o": o, "lse": L}
+        pairs = [(ref, sel)]
+    else:
+        pairs = []
+        for b, h in heads:
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            qs, ks, vs = q[sl], k[sl], v[sl]
+            if do is not None:
+                r = oracle.fwd_bwd(qs, ks, vs, do[sl], w.causal, w.scale)
+            else:
+                o, L = oracle.fwd(qs, ks, vs, w.causal, w.scale)
+                r = {"o": o, "lse": L}
+            pairs.append((r, sl))
+    errs = {}
+    for ref, sl in pairs:
+        for key in KEYS + ("delta",):
+            if key not in ref or key not in got:
+                continue
+            g = got[key][sl]
+            tol = tolerance(w, key, ref[key])
+            if key == "delta":
+                tol = tolerance(w, "o", ref["o"]) * max(1.0, float(np.abs(ref[key]).max()))
+            errs[key] = max(errs.get(key, 0.0), check(f"{w.name}:{key}", g, ref[key], tol))
+    return errs
+
+
+def sample_rows(w: Workload, heads, n_random: int = 8, seed: int = 1):
+    """(b*H+h, i) pairs: tile edges, the ends of the sequence and random rows."""
+    N = w.N
+    fixed = {0, 1, 63, 64, 65, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128,
+             N - 65, N - 2, N - 1}
+    fixed = sorted(i for i in fixed if 0 <= i < N)
+    rng = np.random.default_rng(seed)
+    rows = []
+    for b, h in heads:
+        bh = b * w.H + h
+        idx = fixed + list(rng.integers(0, N, size=n_random))
+        rows += [(bh, int(i)) for i in idx]
+    return np.array(rows, dtype=np.int64)
+
+
+def compare_sampled(w: Workload, inputs, got, q_heads, k_heads):
+    """Sampled query rows (O, L, Delta, dQ) over q_heads and sampled key rows
+    (dK, dV) over k_heads, against the oracle's row entry points."""
+    q, k, v, do = inputs
+    errs = {}
+    qrows = sample_rows(w, q_heads)
+    ref = oracle.query_rows(q, k, v, do, w.causal, qrows, w.scale)
+    bh, i = qrows[:, 0], qrows[:, 1]
+    b, h = bh // w.H, bh % w.H
+    for key in ("o", "lse", "dq"):
+        g = got[key][b, h, i]
+        errs[key] = check(f"{w.name}:{key}", g, ref[key], tolerance(w, key, ref[key]))
+    krows = sample_rows(w, k_heads, seed=2)
+    ref = oracle.key_rows(q, k, v, do, w.causal, krows, w.scale)
+    bh, j = krows[:, 0], krows[:, 1]
+    b, h = bh // w.H, bh % w.H
+    for key in ("dk", "dv"):
+        g = got[key][b, h, j]
+        errs[key] = check(f"{w.name}:{key}", g, ref[key], tolerance(w, key, ref[key]))
+    return errs

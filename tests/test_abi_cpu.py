@@ -1,0 +1,100 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+function include/fa.h declares, and rejects invalid arguments with the
+documented status codes before touching any device (no compute call is made;
+the pointers below are never dereferenced)."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_83_gb300 import build as fabuild
+from exact_attention_83_gb300 import fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+FAKE = 0x100000          # 16-byte aligned, never dereferenced
+S = (ctypes.c_int64 * 4)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fabuild.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "fa_fwd" in names and "fa_bwd" in names and "fa_bwd_preprocess" in names
+    for n in names:
+        assert hasattr(lib, n), f"libfa.so does not export {n}"
+    assert set(fa.EXPORTED) <= set(names)
+
+
+def test_status_strings(lib):
+    for code, name in fa.STATUS_NAMES.items():
+        assert lib.fa_status_string(code).decode().startswith(name)
+    assert lib.fa_version() >= 0x000100
+
+
+def _fwd(lib, q=FAKE, lse=FAKE, B=1, H=2, N=64, D=64, strides=None, scale=0.125, dtype=2):
+    st = strides or (2 * 64 * 64, 64 * 64, 64, 1)
+    return lib.fa_fwd(q, FAKE, FAKE, FAKE, lse, B, H, N, D, S(*st), S(*st), S(*st), S(*st),
+                      0, scale, dtype, None)
+
+
+def test_validation_codes(lib):
+    assert _fwd(lib, q=None) == 1                       # FA_ERR_NULL
+    assert _fwd(lib, lse=None) == 1
+    assert _fwd(lib, N=0) == 2                          # FA_ERR_SHAPE
+    assert _fwd(lib, B=-1) == 2
+    assert _fwd(lib, B=1 << 40, H=1 << 40) == 2         # overflow
+    assert _fwd(lib, D=48) == 3                         # FA_ERR_HEADDIM
+    assert _fwd(lib, D=256) == 3
+    assert _fwd(lib, dtype=7) == 4                      # FA_ERR_DTYPE
+    assert _fwd(lib, strides=(8192, 4096, 64, 2)) == 5  # FA_ERR_STRIDE
+    assert _fwd(lib, strides=(8192, -4096, 64, 1)) == 5
+    assert _fwd(lib, q=FAKE + 2) == 6                   # FA_ERR_ALIGN
+    assert _fwd(lib, strides=(8192, 4096, 68, 1), dtype=2) == 6
+    assert _fwd(lib, scale=0.0) == 10                   # FA_ERR_SCALE
+    assert _fwd(lib, scale=float("nan")) == 10
+    assert lib.fa_set_path(5) == 11                     # FA_ERR_ARG
+
+
+def test_extent_one_dims_ignore_their_stride(lib):
+    # B == 1: the b-stride is never used, so an unaligned value is accepted by
+    # validation (the call then fails later only for lack of a device here).
+    code = _fwd(lib, B=1, strides=(3, 4096, 64, 1))
+    assert code in (0, 7, 9)
+
+
+def test_valid_call_without_device_reports_launch_or_arch(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert _fwd(lib) in (7, 9)
+
+
+def test_preprocess_and_bwd_validation(lib):
+    st = S(64 * 64 * 2, 64 * 64, 64, 1)
+    assert lib.fa_bwd_preprocess(FAKE, None, FAKE, 1, 2, 64, 64, st, st, 2, None) == 1
+    assert lib.fa_bwd_preprocess(FAKE, FAKE, FAKE, 1, 2, 64, 24, st, st, 2, None) == 3
+    bad = S(64 * 64 * 2, 64 * 64, 64, 3)
+    assert lib.fa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 64, 64,
+                      st, st, st, st, st, st, bad, 1, 0.125, 2, None) == 5
+    assert lib.fa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 1, 2, 64, 64,
+                      st, st, st, st, st, st, st, 1, 0.125, 2, None) == 1

@@ -247,3 +247,21 @@ def test_strided_input_is_read_as_logical_bhnd():
                    view.contiguous().numpy(), True)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_rows_match_full(causal):
+    """The sampled-row entry points give exactly the rows of the full result."""
+    q, k, v, do = (rnd((2, 3, 90, 16), s) for s in (80, 81, 82, 83))
+    full = oracle.fwd_bwd(q, k, v, do, causal)
+    rows = np.array([[0, 0], [5, 89], [3, 17], [1, 40], [5, 0], [2, 64]])
+    qr = oracle.query_rows(q, k, v, do, causal, rows)
+    kr = oracle.key_rows(q, k, v, do, causal, rows)
+    for t, (bh, i) in enumerate(rows):
+        b, h = divmod(bh, 3)
+        np.testing.assert_allclose(qr["o"][t], full["o"][b, h, i], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(qr["lse"][t], full["lse"][b, h, i], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(qr["delta"][t], full["delta"][b, h, i], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(qr["dq"][t], full["dq"][b, h, i], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(kr["dk"][t], full["dk"][b, h, i], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(kr["dv"][t], full["dv"][b, h, i], rtol=0, atol=1e-13)
