@@ -70,6 +70,14 @@ def _load():
                                          _i64, _i64, _i64, ctypes.c_int,
                                          ctypes.c_double, _i64, _i64, _dp, _dp,
                                          _dp]
+        lib.oracle_query_rows.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64,
+                                          _i64, ctypes.c_int, ctypes.c_double,
+                                          _i64, ctypes.POINTER(ctypes.c_int64),
+                                          _dp, _dp, _dp, _dp]
+        lib.oracle_key_rows.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64,
+                                        _i64, ctypes.c_int, ctypes.c_double,
+                                        _i64, ctypes.POINTER(ctypes.c_int64),
+                                        _dp, _dp]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -142,6 +150,40 @@ def fwd_bwd(q, k, v, do, causal: bool, scale: float | None = None):
                            int(bool(causal)), scale, _ptr(o), _ptr(L),
                            _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv))
     return dict(o=o, lse=L, delta=delta, dq=dq, dk=dk, dv=dv)
+
+
+def _rows(rows):
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 2))
+    return rows, rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+def query_rows(q, k, v, do, causal: bool, rows, scale: float | None = None):
+    """Row-local outputs for sampled query rows (rows: [n, 2] of (b*H+h, i)).
+    Returns dict o [n,D], lse [n], delta [n], dq [n,D]."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, H, N, D = _shape(q)
+    scale = default_scale(D) if scale is None else float(scale)
+    rows, rp = _rows(rows)
+    n = rows.shape[0]
+    o = np.empty((n, D)); L = np.empty((n,)); delta = np.empty((n,)); dq = np.empty((n, D))
+    _load().oracle_query_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, N, D,
+                              int(bool(causal)), scale, n, rp, _ptr(o), _ptr(L),
+                              _ptr(delta), _ptr(dq))
+    return dict(o=o, lse=L, delta=delta, dq=dq)
+
+
+def key_rows(q, k, v, do, causal: bool, rows, scale: float | None = None):
+    """dK, dV for sampled key rows (rows: [n, 2] of (b*H+h, j)).
+    Returns dict dk [n,D], dv [n,D]."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, H, N, D = _shape(q)
+    scale = default_scale(D) if scale is None else float(scale)
+    rows, rp = _rows(rows)
+    n = rows.shape[0]
+    dk = np.empty((n, D)); dv = np.empty((n, D))
+    _load().oracle_key_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, N, D,
+                            int(bool(causal)), scale, n, rp, _ptr(dk), _ptr(dv))
+    return dict(dk=dk, dv=dv)
 
 
 def dense(q, k, v, do, causal: bool, scale: float | None = None,

@@ -222,6 +222,93 @@ void oracle_fwd_bwd(const double* Q, const double* K, const double* V,
   }
 }
 
+// Sampled query rows: O_i, L_i, Delta_i and dQ_i are row-local (they need
+// only query row i and every key), so they are computed one row at a time
+// with the same formulas as pass 1 of oracle_fwd_bwd.
+// rows[2*t] = flat head index b*H+h, rows[2*t+1] = query index i.
+void oracle_query_rows(const double* Q, const double* K, const double* V,
+                       const double* dO, int64_t B, int64_t H, int64_t N,
+                       int64_t D, int causal, double scale, int64_t n_rows,
+                       const int64_t* rows, double* O_rows, double* L_rows,
+                       double* Delta_rows, double* dQ_rows) {
+  (void)B; (void)H;
+#pragma omp parallel
+  {
+    std::vector<double> p(static_cast<size_t>(N));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t t = 0; t < n_rows; ++t) {
+      const int64_t bh = rows[2 * t], i = rows[2 * t + 1];
+      const int64_t base = bh * N * D;
+      const int64_t nk = keys_allowed(i, N, causal);
+      const double* doi = dO + base + i * D;
+      double* oi = O_rows + t * D;
+      row_forward(Q + base + i * D, K + base, V + base, nk, D, scale, p.data(),
+                  oi, L_rows + t);
+      const double delta = dot(doi, oi, D);
+      Delta_rows[t] = delta;
+      double* dqi = dQ_rows + t * D;
+      for (int64_t d = 0; d < D; ++d) dqi[d] = 0.0;
+      for (int64_t j = 0; j < nk; ++j) {
+        const double ds = p[j] * (dot(doi, V + base + j * D, D) - delta);
+        const double* kj = K + base + j * D;
+        for (int64_t d = 0; d < D; ++d) dqi[d] += ds * kj[d];
+      }
+      for (int64_t d = 0; d < D; ++d) dqi[d] *= scale;
+    }
+  }
+}
+
+// Sampled key rows: dK_j and dV_j need L_i and Delta_i of every query of the
+// head, so those are computed first for each head that holds a sampled key
+// (pass 1 of oracle_fwd_bwd without dQ), then pass 2 runs for the sampled
+// keys only.  rows as in oracle_query_rows, with j in place of i.
+void oracle_key_rows(const double* Q, const double* K, const double* V,
+                     const double* dO, int64_t B, int64_t H, int64_t N,
+                     int64_t D, int causal, double scale, int64_t n_rows,
+                     const int64_t* rows, double* dK_rows, double* dV_rows) {
+  (void)B; (void)H;
+  std::vector<int64_t> heads;
+  for (int64_t t = 0; t < n_rows; ++t) heads.push_back(rows[2 * t]);
+  std::sort(heads.begin(), heads.end());
+  heads.erase(std::unique(heads.begin(), heads.end()), heads.end());
+  std::vector<double> L(N), Delta(N);
+  for (const int64_t bh : heads) {
+    const int64_t base = bh * N * D;
+#pragma omp parallel
+    {
+      std::vector<double> p(static_cast<size_t>(N)), oi(static_cast<size_t>(D));
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t i = 0; i < N; ++i) {
+        row_forward(Q + base + i * D, K + base, V + base,
+                    keys_allowed(i, N, causal), D, scale, p.data(), oi.data(),
+                    &L[i]);
+        Delta[i] = dot(dO + base + i * D, oi.data(), D);
+      }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < n_rows; ++t) {
+      if (rows[2 * t] != bh) continue;
+      const int64_t j = rows[2 * t + 1];
+      const double* kj = K + base + j * D;
+      const double* vj = V + base + j * D;
+      double* dkj = dK_rows + t * D;
+      double* dvj = dV_rows + t * D;
+      for (int64_t d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
+      for (int64_t i = causal ? j : 0; i < N; ++i) {
+        const double* qi = Q + base + i * D;
+        const double* doi = dO + base + i * D;
+        const double pij = std::exp(scale * dot(qi, kj, D) - L[i]);
+        const double ds = pij * (dot(doi, vj, D) - Delta[i]);
+        for (int64_t d = 0; d < D; ++d) {
+          dvj[d] += pij * doi[d];
+          dkj[d] += ds * qi[d];
+        }
+      }
+      for (int64_t d = 0; d < D; ++d) dkj[d] *= scale;
+    }
+  }
+}
+
 // Dense materialisation, for small N: the full N x N score and probability
 // matrices are built per head, then every product is an explicit matrix loop.
 // P is written to P_out [B,H,N,N] (masked entries exactly 0) when non-null.
