@@ -242,6 +242,9 @@ def main():
 
     # ---- forward + backward step, with per-kernel events on the stream
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for e in ev:        # create the events (torch creates them lazily on first record)
+        for x in e:
+            x.record(stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier()
