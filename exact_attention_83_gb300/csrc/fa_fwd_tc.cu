@@ -1,7 +1,418 @@
-// Tensor-core forward (tcgen05 + TMA) -- not compiled for any shape yet.
-#include "fa_internal.h"
+// Tensor-core forward: TMA + tcgen05 + TMEM, warp-specialised, for fp16/bf16
+// with D in {64, 128}.
+//
+// Algorithm ("FlashAttention-2 from PyTorch to Triton", the running quantities
+// m, l, O and the store of L = m + log l; "Triton FlashAttention", the online
+// softmax in fp32 with exp2 on scores pre-scaled by log2(e), the accumulator
+// rescaled when the max moves, and causal key tiles above the diagonal never
+// visited): for each 128-row query tile, loop over 128-key tiles,
+//   S = Q K_j^T (tensor cores, fp32 in TMEM),
+//   mask keys past N (last tile) and keys after the query (diagonal tile only),
+//   m_new = max(m, c * rowmax S) with c = scale * log2(e),
+//   P = exp2(c * S - m) rounded to the input type (FIX 1 of the Triton page),
+//   l += rowsum P,  O += P V_j (tensor cores, fp32 in TMEM),
+// then O / l and L = (m + log2 l) * ln 2.
+//
+// Lazy rescale: the running max used in the exponent is only moved when the
+// row max grows by more than 8 (a factor 2^8 in P); then O (in TMEM) and l
+// are multiplied by exp2(m_old - m_new).  Otherwise P is computed against the
+// stale max and stays <= 2^8.  The result is the same: numerator and
+// denominator share the one max used for that row, and the final division
+// cancels it.
+//
+// CTA = two query tiles (256 rows) of one head sharing every K/V tile load.
+// Warps 0-3: softmax + epilogue of query tile 0 (one TMEM lane = one row per
+// thread); warps 4-7: the same for query tile 1; warp 8: TMA producer (lane 0)
+// and TMEM allocation; warp 9: MMA issuer (lane 0).  TMEM columns: S0 [0,128),
+// S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D); P (input type, packed two
+// per column) overwrites the first 64 columns of its S after S is read.
+// The MMA issue order S0_0, S1_0, {PV0_j, S0_j+1, PV1_j, S1_j+1} lets one
+// tile's softmax overlap the other tile's two MMAs.  A tcgen05.commit tracks
+// every earlier MMA of the issuing thread, so when the softmax warps see S_j
+// complete, PV_{j-1} of the same tile is complete too and O may be rescaled.
+//
+// Every mbarrier wait is bounded (see tc_common.cuh); a wait that runs out
+// records FA_ERR_TIMEOUT, the CTA drains its copies and MMAs in flight,
+// releases its tensor memory and exits.
+
+#include "tc_common.cuh"
 
 namespace fa {
-bool have_fwd_tc(int64_t, fa_dtype) { return false; }
-fa_status launch_fwd_tc(const FwdParams&, cudaStream_t) { return FA_ERR_ARG; }
+namespace {
+
+using namespace tc;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;                  // query rows per tile
+  static constexpr int BN = 128;                  // keys per tile
+  static constexpr int DC = D / 64;               // 128-byte column chunks per row
+  static constexpr int CHUNK = BM * 128;          // bytes of one 128-row chunk
+  static constexpr int TILE = DC * CHUNK;         // bytes of one 128 x D tile
+  static constexpr int NS = D == 128 ? 4 : 8;     // K/V ring slots
+  static constexpr int OFF_RING = 2 * TILE;
+  static constexpr int OFF_BAR = OFF_RING + NS * TILE;
+  static constexpr int SMEM = OFF_BAR + 1024 + 1024;   // + barriers, + alignment slack
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_S0 = 0, COL_O0 = 256;
+};
+
+struct FwdTcArgs {
+  void* o;
+  float* lse;
+  int64_t H, N, BH, npairs;
+  int64_t so[4];
+  int causal;
+  float c;                 // scale * log2(e)
+  unsigned int* status;
+  uint64_t timeout_ns;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(320, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, const FwdTcArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + C::OFF_RING;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  Ctl* ctl = reinterpret_cast<Ctl*>(bars + 40);
+  // barrier map
+  const uint32_t b_q = smem_u32(&bars[0]);
+  const uint32_t b_full0 = smem_u32(&bars[1]);            // + 8 * slot
+  const uint32_t b_empty0 = smem_u32(&bars[1 + C::NS]);   // + 8 * slot
+  const uint32_t b_sfull0 = smem_u32(&bars[1 + 2 * C::NS]);      // + 8 * g
+  const uint32_t b_pready0 = smem_u32(&bars[3 + 2 * C::NS]);     // + 8 * g
+  const uint32_t b_ofinal0 = smem_u32(&bars[5 + 2 * C::NS]);     // + 8 * g
+  const uint32_t b_mmadone = smem_u32(&bars[7 + 2 * C::NS]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t id = blockIdx.x;
+  const int64_t bh = id % a.BH;
+  const int64_t pr = a.causal ? (a.npairs - 1 - id / a.BH) : (id / a.BH);
+  const int32_t hh = static_cast<int32_t>(bh % a.H), bb = static_cast<int32_t>(bh / a.H);
+  const int64_t N = a.N;
+  const int nk = static_cast<int>((N + C::BN - 1) / C::BN);
+  int ntile[2];
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int64_t qt = 2 * pr + g;
+    const int64_t diag = qt + 1;   // key tiles up to and including the diagonal
+    ntile[g] = (qt * C::BM >= N) ? 0 : (a.causal ? static_cast<int>(diag < nk ? diag : nk) : nk);
+  }
+  const int nmax = max(ntile[0], ntile[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(b_full0 + 8 * s, 1);
+      mbar_init(b_empty0 + 8 * s, 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(b_sfull0 + 8 * g, 1);
+      mbar_init(b_pready0 + 8 * g, 128);
+      mbar_init(b_ofinal0 + 8 * g, 1);
+    }
+    mbar_init(b_mmadone, 1);
+    ctl->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      uint32_t issued[C::NS];
+#pragma unroll
+      for (int s = 0; s < C::NS; ++s) issued[s] = 0;
+      const uint32_t qbytes = (ntile[0] > 0 ? C::TILE : 0) + (ntile[1] > 0 ? C::TILE : 0);
+      mbar_arrive_expect_tx(b_q, qbytes);
+      for (int g = 0; g < 2; ++g) {
+        if (ntile[g] == 0) continue;
+        for (int c = 0; c < C::DC; ++c)
+          tma_load_4d(smem_u32(sQ + g * C::TILE + c * C::CHUNK), &tmq, b_q, c * 64,
+                      static_cast<int32_t>((2 * pr + g) * C::BM), hh, bb);
+      }
+      bool ok = true;
+      for (int j = 0; ok && j < nmax; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int u = 2 * j + kv, s = u % C::NS;
+          const uint32_t r = static_cast<uint32_t>(u / C::NS);
+          if (r > 0 && !(ok = wait_bounded(b_empty0 + 8 * s, (r - 1) & 1, ctl, a.status,
+                                           a.timeout_ns)))
+            break;
+          mbar_arrive_expect_tx(b_full0 + 8 * s, C::TILE);
+          for (int c = 0; c < C::DC; ++c)
+            tma_load_4d(smem_u32(sRing + s * C::TILE + c * C::CHUNK), kv ? &tmv : &tmk,
+                        b_full0 + 8 * s, c * 64, j * C::BN, hh, bb);
+          issued[s] = r + 1;
+        }
+      }
+      // Drain: every copy issued has landed before the CTA may exit.
+      wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns, false);
+      for (int s = 0; s < C::NS; ++s)
+        if (issued[s]) wait_bounded(b_full0 + 8 * s, (issued[s] - 1) & 1, ctl, a.status,
+                                    a.timeout_ns, false);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_f16<T>(128, C::BN, false, false);
+      const uint32_t idO = idesc_f16<T>(128, D, false, true);
+      // Descriptors are built once and advanced by adding (byte offset >> 4)
+      // to the start-address field (addresses stay below 256 KiB, so the
+      // 14-bit field never carries).
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sRing), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sRing), C::CHUNK, 1024);
+      auto issue_S = [&](int g, int slot) {
+        const uint64_t qa = dQ0 + static_cast<uint64_t>((g * C::TILE) >> 4);
+        const uint64_t kb = dK0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
+        const uint32_t d = tmem + C::COL_S0 + 128 * g;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+          mma_ss(d, qa + off, kb + off, idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_PV = [&](int g, int slot, bool acc) {
+        const uint64_t vb = dV0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
+        const uint32_t d = tmem + C::COL_O0 + D * g, p = tmem + C::COL_S0 + 128 * g;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ts(d, p + kk * 8, vb + static_cast<uint64_t>((kk * 2048) >> 4), idO,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns) &&
+                wait_bounded(b_full0, 0, ctl, a.status, a.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        for (int g = 0; g < 2; ++g)
+          if (ntile[g] > 0) {
+            issue_S(g, 0);
+            mma_commit(b_sfull0 + 8 * g);
+          }
+        mma_commit(b_empty0);
+      }
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int uV = 2 * j + 1, sV = uV % C::NS;
+        const int uK = 2 * j + 2, sK = uK % C::NS;
+        const bool next = j + 1 < nmax;
+        ok = wait_bounded(b_full0 + 8 * sV, (uV / C::NS) & 1, ctl, a.status, a.timeout_ns);
+        if (ok && next)
+          ok = wait_bounded(b_full0 + 8 * sK, (uK / C::NS) & 1, ctl, a.status, a.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+        for (int g = 0; g < 2; ++g) {
+          if (j >= ntile[g]) continue;
+          if (!(ok = wait_bounded(b_pready0 + 8 * g, j & 1, ctl, a.status, a.timeout_ns))) break;
+          tc_fence_after();
+          issue_PV(g, sV, j > 0);
+          if (j + 1 < ntile[g]) {
+            issue_S(g, sK);
+            mma_commit(b_sfull0 + 8 * g);
+          } else {
+            mma_commit(b_ofinal0 + 8 * g);
+          }
+        }
+        if (!ok) break;
+        mma_commit(b_empty0 + 8 * sV);
+        if (next) mma_commit(b_empty0 + 8 * sK);
+      }
+      // Drain: every MMA (and every commit arrival) of this thread is complete.
+      mma_commit(b_mmadone);
+      wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int g = warp >> 2, quarter = warp & 3;
+    const int r = quarter * 32 + lane;                       // row in the query tile
+    const int64_t qt = 2 * pr + g;
+    const int64_t qrow = qt * C::BM + r;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tS = lane_base + C::COL_S0 + 128 * g;
+    const uint32_t tO = lane_base + C::COL_O0 + D * g;
+    const float c = a.c;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    const int n = ntile[g];
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = wait_warp(b_sfull0 + 8 * g, j & 1, ctl, a.status, a.timeout_ns))) break;
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tS + 0, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tmem_wait_ld();
+        reg_fence32(r0); reg_fence32(r1); reg_fence32(r2); reg_fence32(r3);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(r0[i]);
+          s[32 + i] = __uint_as_float(r1[i]);
+          s[64 + i] = __uint_as_float(r2[i]);
+          s[96 + i] = __uint_as_float(r3[i]);
+        }
+      }
+      // Exclude keys past N (last key tile) and keys after the query (the
+      // diagonal tile, the only one a causal row can straddle).
+      int lim = C::BN - 1;
+      if (a.causal && j == qt) lim = r;
+      if (j == nk - 1) lim = min(lim, static_cast<int>(N - 1 - static_cast<int64_t>(j) * C::BN));
+      if (lim < C::BN - 1) {
+#pragma unroll
+        for (int kk = 0; kk < C::BN; ++kk)
+          if (kk > lim) s[kk] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int kk = 4; kk < C::BN; kk += 4) {
+        mx0 = fmaxf(mx0, s[kk]);
+        mx1 = fmaxf(mx1, s[kk + 1]);
+        mx2 = fmaxf(mx2, s[kk + 2]);
+        mx3 = fmaxf(mx3, s[kk + 3]);
+      }
+      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
+      // Lazy rescale decision (warp-uniform for the TMEM access below).
+      bool rescale = false;
+      float alpha = 1.f;
+      if (j == 0) {
+        m = m_new;
+      } else {
+        const bool need = m_new > m + 8.f;
+        rescale = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ex2(m - m_new);
+          l *= alpha;
+          m = m_new;
+        }
+      }
+      const float negm = -m;
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(s[64 * half + 2 * i], c, negm));
+          const float p1 = ex2(fmaf(s[64 * half + 2 * i + 1], c, negm));
+          sum0 += p0;
+          sum1 += p1;
+          pk[i] = pack2<T>(p0, p1);
+        }
+        tmem_st32(tS + 32 * half, pk);
+      }
+      // O *= alpha once the scores are dead (PV_j is not issued before the
+      // arrival below, and PV_{j-1} completed before S_j did).
+      if (rescale) {
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t t[32];
+          tmem_ld32(tO + 32 * cc, t);
+          tmem_wait_ld();
+          reg_fence32(t);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+          tmem_st32(tO + 32 * cc, t);
+        }
+      }
+      tmem_wait_st();
+      l += sum0 + sum1;
+      tc_fence_before();
+      mbar_arrive(b_pready0 + 8 * g);
+    }
+    if (ok && n > 0) ok = wait_warp(b_ofinal0 + 8 * g, 0, ctl, a.status, a.timeout_ns);
+    if (ok && n > 0) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool store = qrow < N;
+      T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hh * a.so[1] + qrow * a.so[2];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t t[32];
+        tmem_ld32(tO + 32 * cc, t);
+        tmem_wait_ld();
+        reg_fence32(t);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack2<T>(__uint_as_float(t[2 * i]) * inv, __uint_as_float(t[2 * i + 1]) * inv);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+        }
+      }
+      if (store) a.lse[bh * N + qrow] = (m + log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <typename T, int D>
+fa_status run_fwd_tc(const FwdParams& p, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  CUtensorMap mq, mk, mv;
+  if (!encode_tile_map(&mq, p.q, p.dtype, p.B, p.H, p.N, D, p.sq, 128, 64) ||
+      !encode_tile_map(&mk, p.k, p.dtype, p.B, p.H, p.N, D, p.sk, 128, 64) ||
+      !encode_tile_map(&mv, p.v, p.dtype, p.B, p.H, p.N, D, p.sv, 128, 64))
+    return FA_ERR_LAUNCH;
+  FwdTcArgs a{};
+  a.o = p.o; a.lse = p.lse;
+  a.H = p.H; a.N = p.N; a.BH = p.B * p.H; a.npairs = (p.N + 255) / 256;
+  for (int i = 0; i < 4; ++i) a.so[i] = p.so[i];
+  a.causal = p.causal;
+  a.c = p.scale * kLog2e;
+  a.status = p.status;
+  a.timeout_ns = p.timeout_ns;
+  const int64_t blocks = a.BH * a.npairs;
+  if (blocks > 0x7fffffffLL) return FA_ERR_SHAPE;
+  auto kern = fwd_tc_kernel<T, D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+      cudaSuccess)
+    return FA_ERR_LAUNCH;
+  kern<<<dim3(static_cast<unsigned>(blocks)), dim3(C::THREADS), C::SMEM, stream>>>(mq, mk, mv, a);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+bool have_fwd_tc(int64_t D, fa_dtype dt) { return (D == 64 || D == 128) && dt != FA_F32; }
+
+fa_status launch_fwd_tc(const FwdParams& p, cudaStream_t s) {
+  if (p.dtype == FA_BF16) {
+    if (p.D == 128) return run_fwd_tc<__nv_bfloat16, 128>(p, s);
+    if (p.D == 64) return run_fwd_tc<__nv_bfloat16, 64>(p, s);
+  } else if (p.dtype == FA_F16) {
+    if (p.D == 128) return run_fwd_tc<__half, 128>(p, s);
+    if (p.D == 64) return run_fwd_tc<__half, 64>(p, s);
+  }
+  return FA_ERR_ARG;
+}
+
 }  // namespace fa

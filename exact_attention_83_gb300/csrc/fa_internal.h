@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libfa.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -58,6 +59,12 @@ fa_status launch_fwd_tc(const FwdParams& p, cudaStream_t s);
 fa_status launch_bwd_tc(const BwdParams& p, cudaStream_t s);
 bool have_fwd_tc(int64_t D, fa_dtype dt);
 bool have_bwd_tc(int64_t D, fa_dtype dt);
+
+// Encodes a 4-D tiled TMA map (d, n, h, b) over a strided [B,H,N,D] fp16/bf16
+// tensor with 128-byte swizzle and a box of box_cols x box_rows elements.
+bool encode_tile_map(CUtensorMap* map, const void* base, fa_dtype dt, int64_t B, int64_t H,
+                     int64_t N, int64_t D, const int64_t* strides, uint32_t box_rows,
+                     uint32_t box_cols);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

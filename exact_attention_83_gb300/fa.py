@@ -89,6 +89,8 @@ def load_library(path: str = LIB_PATH):
         lib.fa_set_profile_events.argtypes = [ctypes.c_void_p]
         lib.fa_set_profile_events.restype = None
         lib.fa_version.restype = ctypes.c_int
+        if os.environ.get("FA_WAIT_TIMEOUT_NS"):
+            lib.fa_set_wait_timeout_ns(int(os.environ["FA_WAIT_TIMEOUT_NS"]))
         _lib = lib
         return lib
 
