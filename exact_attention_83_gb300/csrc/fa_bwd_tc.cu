@@ -1,7 +1,663 @@
-// Tensor-core backward (tcgen05 + TMA) -- not compiled for any shape yet.
-#include "fa_internal.h"
+// Tensor-core backward: TMA + tcgen05 + TMEM, warp-specialised, for fp16/bf16
+// with D in {64, 128}.
+//
+// The FlashAttention-2 split of "Triton FlashAttention" (project summary): a
+// dK/dV kernel that, for each 128-key tile, loops over the query tiles that
+// attend to it, and a dQ kernel that, for each 128-query tile, loops over the
+// key tiles it attends to.  Neither uses atomics.  Both rebuild the
+// probabilities from the saved log-sum-exp, P = exp(S - L)
+// ("FlashAttention-2 from PyTorch to Triton", section on the running
+// quantities), evaluated as exp2(c * S - L * log2(e)) with c = scale * log2(e),
+// and use Delta = rowsum(dO o O) from the preprocess kernel (same page,
+// defect 5).  With dS = P o (dP - Delta):
+//   dK/dV kernel (key tile j):  S^T = K_j Q_i^T,  dP^T = V_j dO_i^T,
+//                               dV_j += P^T dO_i,  dK_j += dS^T Q_i,
+//                               dK_j *= scale at the end;
+//   dQ kernel (query tile i):   S = Q_i K_j^T,  dP = dO_i V_j^T,
+//                               dQ_i += dS K_j,  dQ_i *= scale at the end.
+// P^T and dS are rounded to the input type before they enter a product.
+//
+// Warp roles (320 threads): warps 0-3 and 4-7 are two elementwise warpgroups
+// that split the 128 columns of each score tile (64 each; one TMEM lane = one
+// row per thread); warp 8 is the TMA producer and owns the TMEM allocation;
+// warp 9 issues the MMAs from one thread.  Each elementwise warpgroup writes
+// its rounded P^T / dS into the TMEM columns it alone reads, so the two never
+// race, and the MMAs that consume them are issued per half as soon as that
+// half is ready.
+//
+// Every mbarrier wait is bounded (tc_common.cuh); on a timeout the CTA drains
+// its copies and MMAs in flight, frees its tensor memory and exits.
+
+#include "tc_common.cuh"
 
 namespace fa {
-bool have_bwd_tc(int64_t, fa_dtype) { return false; }
-fa_status launch_bwd_tc(const BwdParams&, cudaStream_t) { return FA_ERR_ARG; }
+namespace {
+
+using namespace tc;
+
+template <int D>
+struct BwdShape {
+  static constexpr int BT = 128;                 // rows per tile (keys and queries)
+  static constexpr int DC = D / 64;              // 128-byte column chunks per row
+  static constexpr int CHUNK = BT * 128;         // bytes of one 128-row chunk
+  static constexpr int TILE = DC * CHUNK;        // bytes of one 128 x D tile
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+
+struct BwdTcArgs {
+  const float* lse;
+  const float* delta;
+  void* out0;              // dK/dV kernel: dV;  dQ kernel: dQ
+  void* out1;              // dK/dV kernel: dK
+  int64_t H, N, BH, ntiles;
+  int64_t s0[4], s1[4];    // strides of out0, out1
+  int causal;
+  float c;                 // scale * log2(e)
+  float scale;
+  unsigned int* status;
+  uint64_t timeout_ns;
+};
+
+// Loads 64 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
+  uint32_t a[32], b[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_wait_ld();
+  reg_fence32(a);
+  reg_fence32(b);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    x[i] = __uint_as_float(a[i]);
+    x[32 + i] = __uint_as_float(b[i]);
+  }
+}
+
+// Rounds 64 floats to T, packs two per column and stores 32 TMEM columns.
+template <typename T>
+__device__ __forceinline__ void tmem_st_packed64(uint32_t taddr, const float (&x)[64]) {
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = pack2<T>(x[2 * i], x[2 * i + 1]);
+  tmem_st32(taddr, w);
+}
+
+// Epilogue: NCOL fp32 columns of this thread's lane (starting at taddr), times
+// `mul`, rounded to T, stored to a row of global memory (when `store`).
+template <typename T, int NCOL>
+__device__ __forceinline__ void store_row(uint32_t taddr, float mul, T* row, bool store) {
+#pragma unroll
+  for (int cc = 0; cc < NCOL / 32; ++cc) {
+    uint32_t t[32];
+    tmem_ld32(taddr + 32 * cc, t);
+    tmem_wait_ld();
+    reg_fence32(t);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      w[i] = pack2<T>(__uint_as_float(t[2 * i]) * mul, __uint_as_float(t[2 * i + 1]) * mul);
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(row + 32 * cc);
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4)
+        dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+    }
+  }
+}
+
+// ============================================================================
+// dK / dV
+// ============================================================================
+template <int D>
+struct DkdvCfg : BwdShape<D> {
+  using S = BwdShape<D>;
+  static constexpr int NST = D == 128 ? 2 : 4;               // query-tile stages
+  static constexpr int STAGE = 2 * S::TILE + 1024;           // Q, dO, L*log2e, Delta
+  static constexpr int OFF_V = S::TILE;
+  static constexpr int OFF_STAGES = 2 * S::TILE;
+  static constexpr int OFF_BAR = OFF_STAGES + NST * STAGE;
+  static constexpr int SMEM = OFF_BAR + 1024 + 1024;
+  static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + D;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                       const BwdTcArgs a) {
+  using C = DkdvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sStage = smem + C::OFF_STAGES;   // stage st: Q | dO | L2 (128 f32) | Delta (128 f32)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  Ctl* ctl = reinterpret_cast<Ctl*>(bars + 48);
+  const uint32_t b_kv = smem_u32(&bars[0]);
+  const uint32_t b_qfull0 = smem_u32(&bars[1]);                  // + 8 * stage
+  const uint32_t b_qempty0 = smem_u32(&bars[1 + C::NST]);        // + 8 * stage
+  const uint32_t b_sfull = smem_u32(&bars[1 + 2 * C::NST]);
+  const uint32_t b_dpfull = smem_u32(&bars[2 + 2 * C::NST]);
+  const uint32_t b_pready0 = smem_u32(&bars[3 + 2 * C::NST]);    // + 8 * half
+  const uint32_t b_dsready0 = smem_u32(&bars[5 + 2 * C::NST]);   // + 8 * half
+  const uint32_t b_accdone = smem_u32(&bars[7 + 2 * C::NST]);
+  const uint32_t b_mmadone = smem_u32(&bars[8 + 2 * C::NST]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t id = blockIdx.x;
+  const int64_t bh = id % a.BH;
+  const int64_t kt = id / a.BH;                 // key tile; low tiles (most work) first
+  const int32_t hh = static_cast<int32_t>(bh % a.H), bb = static_cast<int32_t>(bh / a.H);
+  const int64_t N = a.N;
+  const int nq = static_cast<int>(a.ntiles);
+  const int i0 = a.causal ? static_cast<int>(kt) : 0;   // first query tile
+  const int n = nq - i0;                                 // query tiles to visit (>= 1)
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_kv, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(b_qfull0 + 8 * s, 32);
+      mbar_init(b_qempty0 + 8 * s, 1);
+    }
+    mbar_init(b_sfull, 1);
+    mbar_init(b_dpfull, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(b_pready0 + 8 * h, 128);
+      mbar_init(b_dsready0 + 8 * h, 128);
+    }
+    mbar_init(b_accdone, 1);
+    mbar_init(b_mmadone, 1);
+    ctl->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    // Lane 0 issues the TMA copies; all 32 lanes stage L * log2(e) and Delta
+    // of the query tile (4 rows per lane).  Rows past N get L = +inf, so their
+    // probabilities are exactly 0, and Delta = 0.
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
+      mbar_arrive_expect_tx(b_kv, 2 * C::TILE);
+      for (int c = 0; c < C::DC; ++c) {
+        tma_load_4d(smem_u32(sK + c * C::CHUNK), &tmk, b_kv, c * 64, static_cast<int32_t>(kt * C::BT), hh, bb);
+        tma_load_4d(smem_u32(sV + c * C::CHUNK), &tmv, b_kv, c * 64, static_cast<int32_t>(kt * C::BT), hh, bb);
+      }
+    }
+    uint32_t last_round[C::NST];
+#pragma unroll
+    for (int s = 0; s < C::NST; ++s) last_round[s] = 0;
+    bool ok = true;
+    for (int it = 0; it < n; ++it) {
+      const int st = it % C::NST;
+      const uint32_t r = static_cast<uint32_t>(it / C::NST);
+      if (r > 0 && !(ok = wait_warp(b_qempty0 + 8 * st, (r - 1) & 1, ctl, a.status, a.timeout_ns)))
+        break;
+      uint8_t* stage = sStage + st * C::STAGE;
+      float* L2s = reinterpret_cast<float*>(stage + 2 * C::TILE);
+      float* Ds = L2s + 128;
+      const int64_t q0 = static_cast<int64_t>(i0 + it) * C::BT;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int64_t q = q0 + lane * 4 + t;
+        L2s[lane * 4 + t] = q < N ? a.lse[bh * N + q] * kLog2e : INFINITY;
+        Ds[lane * 4 + t] = q < N ? a.delta[bh * N + q] : 0.f;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(b_qfull0 + 8 * st, 2 * C::TILE);
+        for (int c = 0; c < C::DC; ++c) {
+          tma_load_4d(smem_u32(stage + c * C::CHUNK), &tmq, b_qfull0 + 8 * st, c * 64,
+                      static_cast<int32_t>(q0), hh, bb);
+          tma_load_4d(smem_u32(stage + C::TILE + c * C::CHUNK), &tmdo, b_qfull0 + 8 * st, c * 64,
+                      static_cast<int32_t>(q0), hh, bb);
+        }
+      } else {
+        mbar_arrive(b_qfull0 + 8 * st);
+      }
+      last_round[st] = r + 1;
+    }
+    // Drain: every copy issued has landed.
+    if (lane == 0) {
+      wait_bounded(b_kv, 0, ctl, a.status, a.timeout_ns, false);
+      for (int s = 0; s < C::NST; ++s)
+        if (last_round[s]) wait_bounded(b_qfull0 + 8 * s, (last_round[s] - 1) & 1, ctl, a.status,
+                                        a.timeout_ns, false);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_f16<T>(128, C::BT, false, false);
+      const uint32_t idG = idesc_f16<T>(128, D, false, true);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t dSt0 = sdesc_sw128(smem_u32(sStage), 16, 1024);          // K-major view
+      const uint64_t dSt0mn = sdesc_sw128(smem_u32(sStage), C::CHUNK, 1024);  // MN-major view
+      bool ok = wait_bounded(b_kv, 0, ctl, a.status, a.timeout_ns);
+      for (int it = 0; ok && it < n; ++it) {
+        const int st = it % C::NST;
+        if (!(ok = wait_bounded(b_qfull0 + 8 * st, (it / C::NST) & 1, ctl, a.status, a.timeout_ns)))
+          break;
+        tc_fence_after();
+        const uint64_t stq = dSt0 + static_cast<uint64_t>((st * C::STAGE) >> 4);
+        const uint64_t stdo = stq + static_cast<uint64_t>(C::TILE >> 4);
+        // S^T = K Q^T, then dP^T = V dO^T  (both K-major operands)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::COL_ST, dK0 + off, stq + off, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(b_sfull);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::COL_DPT, dV0 + off, stdo + off, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(b_dpfull);
+        // dV += P^T dO and dK += dS^T Q, per 64-query half as each is ready.
+        // B operands are the same tiles read MN-major (N = d).
+        const uint64_t mq = dSt0mn + static_cast<uint64_t>((st * C::STAGE) >> 4);
+        const uint64_t mdo = mq + static_cast<uint64_t>(C::TILE >> 4);
+        for (int h = 0; ok && h < 2; ++h) {
+          if (!(ok = wait_bounded(b_pready0 + 8 * h, it & 1, ctl, a.status, a.timeout_ns))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + C::COL_DV, tmem + C::COL_ST + 64 * h + 8 * kk,
+                   mdo + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
+                   (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
+        }
+        for (int h = 0; ok && h < 2; ++h) {
+          if (!(ok = wait_bounded(b_dsready0 + 8 * h, it & 1, ctl, a.status, a.timeout_ns))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + C::COL_DK, tmem + C::COL_DPT + 64 * h + 8 * kk,
+                   mq + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
+                   (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        mma_commit(b_qempty0 + 8 * st);
+      }
+      if (ok) mma_commit(b_accdone);
+      mma_commit(b_mmadone);
+      wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise + epilogue
+    const int hf = warp >> 2, quarter = warp & 3;
+    const int row = quarter * 32 + lane;                 // key within the tile
+    const int64_t key = kt * C::BT + row;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c = a.c;
+    bool ok = true;
+    for (int it = 0; it < n; ++it) {
+      const int i = i0 + it, st = it % C::NST;
+      if (!(ok = wait_warp(b_sfull, it & 1, ctl, a.status, a.timeout_ns))) break;
+      if (!(ok = wait_warp(b_qfull0 + 8 * st, (it / C::NST) & 1, ctl, a.status, a.timeout_ns))) break;
+      tc_fence_after();
+      const float* L2s = reinterpret_cast<const float*>(sStage + st * C::STAGE + 2 * C::TILE) + 64 * hf;
+      const float* Ds = L2s + 128;
+      float p[64];
+      tmem_ld64(lane_base + C::COL_ST + 64 * hf, p);
+#pragma unroll
+      for (int q = 0; q < 64; q += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(L2s + q);
+        p[q] = ex2(fmaf(p[q], c, -l4.x));
+        p[q + 1] = ex2(fmaf(p[q + 1], c, -l4.y));
+        p[q + 2] = ex2(fmaf(p[q + 2], c, -l4.z));
+        p[q + 3] = ex2(fmaf(p[q + 3], c, -l4.w));
+      }
+      if (a.causal && i == kt) {
+        // diagonal tile: query (64*hf + q) attends to this key only if it is not earlier
+#pragma unroll
+        for (int q = 0; q < 64; ++q)
+          if (64 * hf + q < row) p[q] = 0.f;
+      }
+      tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, p);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(b_pready0 + 8 * hf);
+
+      if (!(ok = wait_warp(b_dpfull, it & 1, ctl, a.status, a.timeout_ns))) break;
+      tc_fence_after();
+      float dp[64];
+      tmem_ld64(lane_base + C::COL_DPT + 64 * hf, dp);
+#pragma unroll
+      for (int q = 0; q < 64; q += 4) {
+        const float4 d4 = *reinterpret_cast<const float4*>(Ds + q);
+        dp[q] = p[q] * (dp[q] - d4.x);
+        dp[q + 1] = p[q + 1] * (dp[q + 1] - d4.y);
+        dp[q + 2] = p[q + 2] * (dp[q + 2] - d4.z);
+        dp[q + 3] = p[q + 3] * (dp[q + 3] - d4.w);
+      }
+      tmem_st_packed64<T>(lane_base + C::COL_DPT + 64 * hf, dp);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(b_dsready0 + 8 * hf);
+    }
+    if (ok) ok = wait_warp(b_accdone, 0, ctl, a.status, a.timeout_ns);
+    if (ok) {
+      tc_fence_after();
+      const bool store = key < N;
+      if (hf == 0) {
+        T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hh * a.s0[1] + key * a.s0[2];
+        store_row<T, D>(lane_base + C::COL_DV, 1.f, out, store);
+      } else {
+        T* out = static_cast<T*>(a.out1) + bb * a.s1[0] + hh * a.s1[1] + key * a.s1[2];
+        store_row<T, D>(lane_base + C::COL_DK, a.scale, out, store);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ============================================================================
+// dQ
+// ============================================================================
+template <int D>
+struct DqCfg : BwdShape<D> {
+  using S = BwdShape<D>;
+  static constexpr int NST = D == 128 ? 2 : 4;               // key-tile stages (K | V)
+  static constexpr int STAGE = 2 * S::TILE;
+  static constexpr int OFF_DO = S::TILE;
+  static constexpr int OFF_STAGES = 2 * S::TILE;
+  static constexpr int OFF_BAR = OFF_STAGES + NST * STAGE;
+  static constexpr int SMEM = OFF_BAR + 1024 + 1024;
+  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                     const BwdTcArgs a) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + C::OFF_DO;
+  uint8_t* sStage = smem + C::OFF_STAGES;   // stage st: K | V
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  Ctl* ctl = reinterpret_cast<Ctl*>(bars + 48);
+  const uint32_t b_q = smem_u32(&bars[0]);
+  const uint32_t b_kvfull0 = smem_u32(&bars[1]);                 // + 8 * stage
+  const uint32_t b_kvempty0 = smem_u32(&bars[1 + C::NST]);       // + 8 * stage
+  const uint32_t b_sfull = smem_u32(&bars[1 + 2 * C::NST]);
+  const uint32_t b_sfree = smem_u32(&bars[2 + 2 * C::NST]);
+  const uint32_t b_dpfull = smem_u32(&bars[3 + 2 * C::NST]);
+  const uint32_t b_dsready0 = smem_u32(&bars[4 + 2 * C::NST]);   // + 8 * half
+  const uint32_t b_accdone = smem_u32(&bars[6 + 2 * C::NST]);
+  const uint32_t b_mmadone = smem_u32(&bars[7 + 2 * C::NST]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t id = blockIdx.x;
+  const int64_t bh = id % a.BH;
+  const int64_t qt = a.causal ? (a.ntiles - 1 - id / a.BH) : (id / a.BH);   // longest first
+  const int32_t hh = static_cast<int32_t>(bh % a.H), bb = static_cast<int32_t>(bh / a.H);
+  const int64_t N = a.N;
+  const int nk = static_cast<int>(a.ntiles);
+  const int n = a.causal ? static_cast<int>(qt) + 1 : nk;   // key tiles to visit
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(b_kvfull0 + 8 * s, 1);
+      mbar_init(b_kvempty0 + 8 * s, 1);
+    }
+    mbar_init(b_sfull, 1);
+    mbar_init(b_sfree, 256);
+    mbar_init(b_dpfull, 1);
+    for (int h = 0; h < 2; ++h) mbar_init(b_dsready0 + 8 * h, 128);
+    mbar_init(b_accdone, 1);
+    mbar_init(b_mmadone, 1);
+    ctl->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
+      mbar_arrive_expect_tx(b_q, 2 * C::TILE);
+      for (int c = 0; c < C::DC; ++c) {
+        tma_load_4d(smem_u32(sQ + c * C::CHUNK), &tmq, b_q, c * 64, static_cast<int32_t>(qt * C::BT), hh, bb);
+        tma_load_4d(smem_u32(sDO + c * C::CHUNK), &tmdo, b_q, c * 64, static_cast<int32_t>(qt * C::BT), hh, bb);
+      }
+      uint32_t last_round[C::NST];
+#pragma unroll
+      for (int s = 0; s < C::NST; ++s) last_round[s] = 0;
+      for (int jt = 0; jt < n; ++jt) {
+        const int st = jt % C::NST;
+        const uint32_t r = static_cast<uint32_t>(jt / C::NST);
+        if (r > 0 && !wait_bounded(b_kvempty0 + 8 * st, (r - 1) & 1, ctl, a.status, a.timeout_ns))
+          break;
+        uint8_t* stage = sStage + st * C::STAGE;
+        mbar_arrive_expect_tx(b_kvfull0 + 8 * st, 2 * C::TILE);
+        for (int c = 0; c < C::DC; ++c) {
+          tma_load_4d(smem_u32(stage + c * C::CHUNK), &tmk, b_kvfull0 + 8 * st, c * 64, jt * C::BT, hh, bb);
+          tma_load_4d(smem_u32(stage + C::TILE + c * C::CHUNK), &tmv, b_kvfull0 + 8 * st, c * 64,
+                      jt * C::BT, hh, bb);
+        }
+        last_round[st] = r + 1;
+      }
+      wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns, false);
+      for (int s = 0; s < C::NST; ++s)
+        if (last_round[s]) wait_bounded(b_kvfull0 + 8 * s, (last_round[s] - 1) & 1, ctl, a.status,
+                                        a.timeout_ns, false);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    // Order: S_0, dP_0, then per key tile jt: S_jt+1 (once S_jt has been read
+    // out of TMEM), dQ += dS_jt K_jt (per half as ready), dP_jt+1.
+    if (lane == 0) {
+      const uint32_t idS = idesc_f16<T>(128, C::BT, false, false);
+      const uint32_t idG = idesc_f16<T>(128, D, false, true);
+      const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dDOd = sdesc_sw128(smem_u32(sDO), 16, 1024);
+      const uint64_t dSt0 = sdesc_sw128(smem_u32(sStage), 16, 1024);
+      const uint64_t dSt0mn = sdesc_sw128(smem_u32(sStage), C::CHUNK, 1024);
+      auto issue_S = [&](int st) {
+        const uint64_t kb = dSt0 + static_cast<uint64_t>((st * C::STAGE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::COL_S, dQd + off, kb + off, idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_dP = [&](int st) {
+        const uint64_t vb = dSt0 + static_cast<uint64_t>((st * C::STAGE + C::TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::COL_DP, dDOd + off, vb + off, idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns) &&
+                wait_bounded(b_kvfull0, 0, ctl, a.status, a.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0);
+        mma_commit(b_sfull);
+        issue_dP(0);
+        mma_commit(b_dpfull);
+      }
+      for (int jt = 0; ok && jt < n; ++jt) {
+        const int st = jt % C::NST;
+        const bool next = jt + 1 < n;
+        const int stn = (jt + 1) % C::NST;
+        if (next) {
+          if (!(ok = wait_bounded(b_kvfull0 + 8 * stn, ((jt + 1) / C::NST) & 1, ctl, a.status,
+                                  a.timeout_ns)))
+            break;
+          if (!(ok = wait_bounded(b_sfree, jt & 1, ctl, a.status, a.timeout_ns))) break;
+          tc_fence_after();
+          issue_S(stn);
+          mma_commit(b_sfull);
+        }
+        const uint64_t kmn = dSt0mn + static_cast<uint64_t>((st * C::STAGE) >> 4);
+        for (int h = 0; ok && h < 2; ++h) {
+          if (!(ok = wait_bounded(b_dsready0 + 8 * h, jt & 1, ctl, a.status, a.timeout_ns))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + C::COL_DQ, tmem + C::COL_DP + 64 * h + 8 * kk,
+                   kmn + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
+                   (jt > 0 || h > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        mma_commit(b_kvempty0 + 8 * st);
+        if (next) {
+          issue_dP(stn);
+          mma_commit(b_dpfull);
+        }
+      }
+      if (ok) mma_commit(b_accdone);
+      mma_commit(b_mmadone);
+      wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise + epilogue
+    const int hf = warp >> 2, quarter = warp & 3;
+    const int row = quarter * 32 + lane;                  // query within the tile
+    const int64_t qrow = qt * C::BT + row;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c = a.c;
+    const float l2 = qrow < N ? a.lse[bh * N + qrow] * kLog2e : INFINITY;
+    const float dl = qrow < N ? a.delta[bh * N + qrow] : 0.f;
+    bool ok = true;
+    for (int jt = 0; jt < n; ++jt) {
+      if (!(ok = wait_warp(b_sfull, jt & 1, ctl, a.status, a.timeout_ns))) break;
+      tc_fence_after();
+      float p[64];
+      tmem_ld64(lane_base + C::COL_S + 64 * hf, p);
+      tc_fence_before();
+      mbar_arrive(b_sfree);                  // S may be overwritten by the next tile
+      // keys past N (last tile) and keys after the query (diagonal tile)
+      int lim = 63;
+      if (a.causal && jt == qt) lim = row - 64 * hf;
+      if (jt == nk - 1) lim = min(lim, static_cast<int>(N - 1 - static_cast<int64_t>(jt) * C::BT) - 64 * hf);
+#pragma unroll
+      for (int q = 0; q < 64; ++q) p[q] = ex2(fmaf(p[q], c, -l2));
+      if (lim < 63) {
+#pragma unroll
+        for (int q = 0; q < 64; ++q)
+          if (q > lim) p[q] = 0.f;
+      }
+      if (!(ok = wait_warp(b_dpfull, jt & 1, ctl, a.status, a.timeout_ns))) break;
+      tc_fence_after();
+      float dp[64];
+      tmem_ld64(lane_base + C::COL_DP + 64 * hf, dp);
+#pragma unroll
+      for (int q = 0; q < 64; ++q) dp[q] = p[q] * (dp[q] - dl);
+      tmem_st_packed64<T>(lane_base + C::COL_DP + 64 * hf, dp);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(b_dsready0 + 8 * hf);
+    }
+    if (ok) ok = wait_warp(b_accdone, 0, ctl, a.status, a.timeout_ns);
+    if (ok) {
+      tc_fence_after();
+      T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hh * a.s0[1] + qrow * a.s0[2] + (D / 2) * hf;
+      store_row<T, D / 2>(lane_base + C::COL_DQ + (D / 2) * hf, a.scale, out, qrow < N);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <typename T, int D>
+fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_tile_map(&mq, p.q, p.dtype, p.B, p.H, p.N, D, p.sq, 128, 64) ||
+      !encode_tile_map(&mk, p.k, p.dtype, p.B, p.H, p.N, D, p.sk, 128, 64) ||
+      !encode_tile_map(&mv, p.v, p.dtype, p.B, p.H, p.N, D, p.sv, 128, 64) ||
+      !encode_tile_map(&mdo, p.dout, p.dtype, p.B, p.H, p.N, D, p.sdo, 128, 64))
+    return FA_ERR_LAUNCH;
+  BwdTcArgs a{};
+  a.lse = p.lse; a.delta = p.delta;
+  a.H = p.H; a.N = p.N; a.BH = p.B * p.H; a.ntiles = (p.N + 127) / 128;
+  a.causal = p.causal;
+  a.c = p.scale * kLog2e;
+  a.scale = p.scale;
+  a.status = p.status;
+  a.timeout_ns = p.timeout_ns;
+  const int64_t blocks = a.BH * a.ntiles;
+  if (blocks > 0x7fffffffLL) return FA_ERR_SHAPE;
+
+  // dK / dV
+  a.out0 = p.dv; a.out1 = p.dk;
+  for (int i = 0; i < 4; ++i) { a.s0[i] = p.sdv[i]; a.s1[i] = p.sdk[i]; }
+  auto k1 = bwd_dkdv_tc_kernel<T, D>;
+  if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  prof_record(p, 0, stream);
+  k1<<<dim3(static_cast<unsigned>(blocks)), dim3(DkdvCfg<D>::THREADS), DkdvCfg<D>::SMEM, stream>>>(
+      mq, mk, mv, mdo, a);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  prof_record(p, 1, stream);
+
+  // dQ
+  a.out0 = p.dq; a.out1 = nullptr;
+  for (int i = 0; i < 4; ++i) { a.s0[i] = p.sdq[i]; a.s1[i] = 0; }
+  auto k2 = bwd_dq_tc_kernel<T, D>;
+  if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  k2<<<dim3(static_cast<unsigned>(blocks)), dim3(DqCfg<D>::THREADS), DqCfg<D>::SMEM, stream>>>(
+      mq, mk, mv, mdo, a);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  prof_record(p, 2, stream);
+  return FA_OK;
+}
+
+}  // namespace
+
+bool have_bwd_tc(int64_t D, fa_dtype dt) { return (D == 64 || D == 128) && dt != FA_F32; }
+
+fa_status launch_bwd_tc(const BwdParams& p, cudaStream_t s) {
+  if (p.dtype == FA_BF16) {
+    if (p.D == 128) return run_bwd_tc<__nv_bfloat16, 128>(p, s);
+    if (p.D == 64) return run_bwd_tc<__nv_bfloat16, 64>(p, s);
+  } else if (p.dtype == FA_F16) {
+    if (p.D == 128) return run_bwd_tc<__half, 128>(p, s);
+    if (p.D == 64) return run_bwd_tc<__half, 64>(p, s);
+  }
+  return FA_ERR_ARG;
+}
+
 }  // namespace fa
