@@ -232,6 +232,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_ARCH: return "FA_ERR_ARCH: the current device is not sm_103";
     case FA_ERR_SCALE: return "FA_ERR_SCALE: scale must be finite and > 0";
     case FA_ERR_ARG: return "FA_ERR_ARG: invalid argument";
+    case FA_ERR_SCRATCH: return "FA_ERR_SCRATCH: B*H*N exceeds FA_NOALLOC_MAX_ROWS";
   }
   return "unknown fa_status";
 }

@@ -37,11 +37,12 @@ STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_HEADDIM",
     4: "FA_ERR_DTYPE", 5: "FA_ERR_STRIDE", 6: "FA_ERR_ALIGN", 7: "FA_ERR_LAUNCH",
     8: "FA_ERR_TIMEOUT", 9: "FA_ERR_ARCH", 10: "FA_ERR_SCALE", 11: "FA_ERR_ARG",
+    12: "FA_ERR_SCRATCH",
 }
 
 EXPORTED = ("fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_get_device_status",
             "fa_status_string", "fa_set_path", "fa_set_wait_timeout_ns",
-            "fa_set_profile_events", "fa_version")
+            "fa_set_profile_events", "fa_version", "fa_bwd_noalloc")
 
 
 class FAError(RuntimeError):
@@ -78,6 +79,11 @@ def load_library(path: str = LIB_PATH):
                                _s4, _s4, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                _vp]
         lib.fa_bwd.restype = ctypes.c_int
+        lib.fa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                       _i64, _i64, _i64, _i64, _s4, _s4, _s4, _s4, _s4,
+                                       _s4, _s4, _s4, ctypes.c_int, ctypes.c_float,
+                                       ctypes.c_int, _vp]
+        lib.fa_bwd_noalloc.restype = ctypes.c_int
         lib.fa_get_device_status.argtypes = [_vp]
         lib.fa_get_device_status.restype = ctypes.c_int
         lib.fa_status_string.argtypes = [ctypes.c_int]
@@ -163,6 +169,23 @@ def bwd(q, k, v, do, lse, delta, dq, dk, dv, causal: bool, scale=None):
                           _strides(dk), _strides(dv), int(bool(causal)),
                           _scale(D, scale), _DTYPE_CODE[q.dtype], _stream(q))
     _check(code, "fa_bwd")
+
+
+def bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale=None):
+    """fa_bwd_noalloc: the backward for callers that cannot allocate device
+    memory; Delta lives in a fixed buffer inside libfa (B*H*N must not exceed
+    its FA_NOALLOC_MAX_ROWS rows).  Calls must not overlap on the GPU."""
+    B, H, N, D = _dims(q)
+    _same(q, k, v, o, do, dq, dk, dv)
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        code = lib.fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                  dv.data_ptr(), B, H, N, D, _strides(q), _strides(k),
+                                  _strides(v), _strides(o), _strides(do), _strides(dq),
+                                  _strides(dk), _strides(dv), int(bool(causal)),
+                                  _scale(D, scale), _DTYPE_CODE[q.dtype], _stream(q))
+    _check(code, "fa_bwd_noalloc")
 
 
 def device_status(device=None) -> int:

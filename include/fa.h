@@ -81,7 +81,8 @@ typedef enum {
   FA_ERR_TIMEOUT = 8,  /* a device-side bounded wait ran out (see below)       */
   FA_ERR_ARCH = 9,     /* the current device is not sm_103                      */
   FA_ERR_SCALE = 10,   /* scale is not finite and > 0                          */
-  FA_ERR_ARG = 11      /* another invalid argument (e.g. an unknown option)    */
+  FA_ERR_ARG = 11,     /* another invalid argument (e.g. an unknown option)    */
+  FA_ERR_SCRATCH = 12  /* fa_bwd_noalloc: B*H*N exceeds FA_NOALLOC_MAX_ROWS    */
 } fa_status;
 
 /*
@@ -117,6 +118,42 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
                  const int64_t* sdo, const int64_t* sdq, const int64_t* sdk,
                  const int64_t* sdv, int causal, float scale, fa_dtype dtype,
                  cudaStream_t stream);
+
+/*
+ * Backward that needs no device buffer beyond inputs and outputs.  The pages
+ * that define the method have no counterpart for this entry point; it serves
+ * callers that cannot allocate device memory at the point where they run the
+ * backward -- for example code executing while a CUDA graph is being
+ * captured (cudaMalloc is not allowed then), code inside a framework or
+ * plugin that is handed fixed buffers and no allocator, or latency-critical
+ * paths that must not take cudaMalloc's implicit synchronisation.
+ *
+ * Computes exactly what fa_bwd_preprocess followed by fa_bwd computes, with
+ * the same argument meanings, layouts and validation, except that the per-row
+ * Delta = rowsum(dO o O) is kept in a buffer inside libfa instead of one the
+ * caller passes: a fixed device array of FA_NOALLOC_MAX_ROWS floats (16 MiB)
+ * that every GPU which loads this part of the library holds until the
+ * process exits.  O is the forward output (strides so).  The call allocates
+ * nothing (no cudaMalloc, no cudaFree).
+ *
+ * Limit: B * H * N <= FA_NOALLOC_MAX_ROWS, else FA_ERR_SCRATCH and nothing is
+ * launched.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * buffer's device address once; make that first call before any stream
+ * capture begins.
+ * Sharing: every call uses the same buffer and leaves its Delta rows in it.
+ * Each call writes all the rows it reads before reading them, so nothing
+ * needs to start at zero, but calls whose work overlaps on the GPU (for
+ * example on two streams at once) race on the buffer: order them.
+ */
+#define FA_NOALLOC_MAX_ROWS (1 << 22)
+FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                                const void* dout, const float* lse, void* dq, void* dk,
+                                void* dv, int64_t B, int64_t H, int64_t N, int64_t D,
+                                const int64_t* sq, const int64_t* sk, const int64_t* sv,
+                                const int64_t* so, const int64_t* sdo, const int64_t* sdq,
+                                const int64_t* sdk, const int64_t* sdv, int causal,
+                                float scale, fa_dtype dtype, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the

@@ -76,10 +76,11 @@ def test_validation_codes(lib):
 
 
 def test_extent_one_dims_ignore_their_stride(lib):
-    # B == 1: the b-stride is never used, so an unaligned value is accepted by
-    # validation (the call then fails later only for lack of a device here).
-    code = _fwd(lib, B=1, strides=(3, 4096, 64, 1))
-    assert code in (0, 7, 9)
+    # B == 1: the b-stride is never used, so an unaligned value passes the
+    # alignment check; the invalid scale then stops the call before any device
+    # work (a launch with these fake pointers must never happen).
+    code = _fwd(lib, B=1, strides=(3, 4096, 64, 1), scale=0.0)
+    assert code == 10
 
 
 def test_valid_call_without_device_reports_launch_or_arch(lib):
