@@ -42,11 +42,21 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # the dominant kernel, keyed by the sha256 of the source file it was measured
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    # bwd_dkdv_tc_kernel<bf16,128>: 1040.7 MB per launch measured on 16 heads,
+    # scaled by heads to the 32-head launch
+    ("dkdv", "63a060bd06fb4364b587c9ec8216570b4ac8e28f8a1eeb49acfd0653e401d3f7",
+     "long-bf16-B1-H32-N16384-D128-causal"): 2081.4e6,
+}
+
+
+# The long causal shape with half the heads: inputs (4 x 64 MiB) still exceed
+# L2, device footprint ~0.5 GB; used for counter captures.
+PROFILE_CASE = Workload("long-bf16-B1-H16-N16384-D128-causal", 1, 16, 16384, 128, "bf16", True)
 
 
 def workloads():
-    ws = {LONG_CAUSAL.name: LONG_CAUSAL}
+    ws = {LONG_CAUSAL.name: LONG_CAUSAL, PROFILE_CASE.name: PROFILE_CASE}
     for c in (False, True):
         w = bf16_n1024(c)
         ws[w.name] = w
