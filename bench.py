@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
+from exact_attention_83_gb300 import shard  # noqa: E402
 from exact_attention_83_gb300.inputs import (LONG_CAUSAL, Workload, bf16_n1024,  # noqa: E402
                                              make_inputs, sweep)
 
@@ -219,7 +220,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     fa.load_library()
 
-    q, k, v, do = (t.to(dev) for t in make_inputs(w))
+    # weak scaling: each rank runs its own independent copy of the workload
+    q, k, v, do = (t.to(dev) for t in make_inputs(shard.rank_workload(w, rank)))
     B, H, N, D = w.B, w.H, w.N, w.D
     o = torch.empty((B, H, N, D), dtype=q.dtype, device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -238,11 +240,7 @@ def main():
         torch.cuda.synchronize(dev)
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return shard.max_over_ranks(x, dev)
 
     for _ in range(args.warmup):
         step()
