@@ -109,15 +109,31 @@ __device__ __forceinline__ void store_row(uint32_t taddr, float mul, T* row, boo
 // ============================================================================
 // dK / dV
 // ============================================================================
+// Shared memory: K_j and V_j (loaded once), a ring of NQ query tiles Q_i and a
+// ring of ND slots holding dO_i with its L * log2(e) and Delta.  Q_i is read by
+// S^T_i and dK_i, dO_i by dP^T_i and dV_i, so the MMA issue order per query
+// tile i,
+//     dV_i (per half, as P^T_i is ready),  S^T_{i+1},
+//     dK_i (per half, as dS^T_i is ready), dP^T_{i+1},
+// needs Q_{i+1} loaded while tile i is still in use (three Q slots) but dO_{i+1}
+// only after dK_i (two dO slots).  S^T_{i+1} overwrites P^T_i and dP^T_{i+1}
+// overwrites dS^T_i; each is read only by products issued before it.  The next
+// tile's scores are therefore ready while the elementwise warps finish dS_i.
 template <int D>
 struct DkdvCfg : BwdShape<D> {
   using S = BwdShape<D>;
-  static constexpr int NST = D == 128 ? 2 : 4;               // query-tile stages
-  static constexpr int STAGE = 2 * S::TILE + 1024;           // Q, dO, L*log2e, Delta
+  static constexpr int NQ = 3;                               // Q ring slots
+  static constexpr int ND = 2;                               // dO (+ L, Delta) ring slots
+  static constexpr int DSLOT = S::TILE + 1024;               // dO | L*log2e | Delta
   static constexpr int OFF_V = S::TILE;
-  static constexpr int OFF_STAGES = 2 * S::TILE;
-  static constexpr int OFF_BAR = OFF_STAGES + NST * STAGE;
-  static constexpr int SMEM = OFF_BAR + 1024 + 1024;
+  static constexpr int OFF_Q = 2 * S::TILE;
+  static constexpr int OFF_DO = OFF_Q + NQ * S::TILE;
+  static constexpr int OFF_BAR = OFF_DO + ND * DSLOT;
+  static constexpr int BAR_BYTES = 256;
+  // Up to MAX_PAD bytes to bring the dynamic shared memory base to a 1024-byte
+  // boundary (the kernel checks this at entry).
+  static constexpr int MAX_PAD = D == 128 ? 768 : 1024;
+  static constexpr int SMEM = OFF_BAR + BAR_BYTES + MAX_PAD;
   static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + D;
 };
 
@@ -127,23 +143,31 @@ __global__ void __launch_bounds__(320, 1)
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                        const BwdTcArgs a) {
   using C = DkdvCfg<D>;
+  static_assert(C::SMEM <= 232448, "shared memory per block");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad > static_cast<uint32_t>(C::MAX_PAD)) {   // never expected: report, do nothing
+    if (threadIdx.x == 0) atomicCAS(a.status, 0u, static_cast<unsigned int>(FA_ERR_LAUNCH));
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sStage = smem + C::OFF_STAGES;   // stage st: Q | dO | L2 (128 f32) | Delta (128 f32)
+  uint8_t* sQ = smem + C::OFF_Q;            // slot s: Q tile
+  uint8_t* sD = smem + C::OFF_DO;           // slot s: dO tile | L2 (128 f32) | Delta (128 f32)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  Ctl* ctl = reinterpret_cast<Ctl*>(bars + 48);
+  Ctl* ctl = reinterpret_cast<Ctl*>(bars + 28);
   const uint32_t b_kv = smem_u32(&bars[0]);
-  const uint32_t b_qfull0 = smem_u32(&bars[1]);                  // + 8 * stage
-  const uint32_t b_qempty0 = smem_u32(&bars[1 + C::NST]);        // + 8 * stage
-  const uint32_t b_sfull = smem_u32(&bars[1 + 2 * C::NST]);
-  const uint32_t b_dpfull = smem_u32(&bars[2 + 2 * C::NST]);
-  const uint32_t b_pready0 = smem_u32(&bars[3 + 2 * C::NST]);    // + 8 * half
-  const uint32_t b_dsready0 = smem_u32(&bars[5 + 2 * C::NST]);   // + 8 * half
-  const uint32_t b_accdone = smem_u32(&bars[7 + 2 * C::NST]);
-  const uint32_t b_mmadone = smem_u32(&bars[8 + 2 * C::NST]);
+  const uint32_t b_qfull0 = smem_u32(&bars[1]);                  // + 8 * Q slot (3)
+  const uint32_t b_qempty0 = smem_u32(&bars[4]);                 // + 8 * Q slot (3)
+  const uint32_t b_dfull0 = smem_u32(&bars[7]);                  // + 8 * dO slot (2)
+  const uint32_t b_dempty0 = smem_u32(&bars[9]);                 // + 8 * dO slot (2)
+  const uint32_t b_sfull = smem_u32(&bars[11]);
+  const uint32_t b_dpfull = smem_u32(&bars[12]);
+  const uint32_t b_pready0 = smem_u32(&bars[13]);                // + 8 * half
+  const uint32_t b_dsready0 = smem_u32(&bars[15]);               // + 8 * half
+  const uint32_t b_accdone = smem_u32(&bars[17]);
+  const uint32_t b_mmadone = smem_u32(&bars[18]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t id = blockIdx.x;
@@ -157,9 +181,13 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
-    for (int s = 0; s < C::NST; ++s) {
-      mbar_init(b_qfull0 + 8 * s, 32);
+    for (int s = 0; s < C::NQ; ++s) {
+      mbar_init(b_qfull0 + 8 * s, 1);
       mbar_init(b_qempty0 + 8 * s, 1);
+    }
+    for (int s = 0; s < C::ND; ++s) {
+      mbar_init(b_dfull0 + 8 * s, 32);
+      mbar_init(b_dempty0 + 8 * s, 1);
     }
     mbar_init(b_sfull, 1);
     mbar_init(b_dpfull, 1);
@@ -183,8 +211,9 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    // Lane 0 issues the TMA copies; all 32 lanes stage L * log2(e) and Delta
-    // of the query tile (4 rows per lane).  Rows past N get L = +inf, so their
+    // Lane 0 issues the TMA copies.  For each query tile: Q into its Q slot,
+    // then dO into its dO slot, where all 32 lanes also stage L * log2(e) and
+    // Delta (4 rows per lane).  Rows past N get L = +inf, so their
     // probabilities are exactly 0, and Delta = 0.
     if (lane == 0) {
       tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
@@ -195,19 +224,38 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_4d(smem_u32(sV + c * C::CHUNK), &tmv, b_kv, c * 64, static_cast<int32_t>(kt * C::BT), hh, bb);
       }
     }
-    uint32_t last_round[C::NST];
+    uint32_t q_round[C::NQ], d_round[C::ND];
 #pragma unroll
-    for (int s = 0; s < C::NST; ++s) last_round[s] = 0;
+    for (int s = 0; s < C::NQ; ++s) q_round[s] = 0;
+#pragma unroll
+    for (int s = 0; s < C::ND; ++s) d_round[s] = 0;
     bool ok = true;
     for (int it = 0; it < n; ++it) {
-      const int st = it % C::NST;
-      const uint32_t r = static_cast<uint32_t>(it / C::NST);
-      if (r > 0 && !(ok = wait_warp(b_qempty0 + 8 * st, (r - 1) & 1, ctl, a.status, a.timeout_ns)))
-        break;
-      uint8_t* stage = sStage + st * C::STAGE;
-      float* L2s = reinterpret_cast<float*>(stage + 2 * C::TILE);
-      float* Ds = L2s + 128;
       const int64_t q0 = static_cast<int64_t>(i0 + it) * C::BT;
+      // Q_i
+      const int qs = it % C::NQ;
+      const uint32_t qr = static_cast<uint32_t>(it / C::NQ);
+      if (lane == 0) {
+        if (qr > 0 && !wait_bounded(b_qempty0 + 8 * qs, (qr - 1) & 1, ctl, a.status, a.timeout_ns))
+          ok = false;
+        if (ok) {
+          mbar_arrive_expect_tx(b_qfull0 + 8 * qs, C::TILE);
+          for (int c = 0; c < C::DC; ++c)
+            tma_load_4d(smem_u32(sQ + qs * C::TILE + c * C::CHUNK), &tmq, b_qfull0 + 8 * qs, c * 64,
+                        static_cast<int32_t>(q0), hh, bb);
+          q_round[qs] = qr + 1;
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      // dO_i, L, Delta
+      const int ds = it % C::ND;
+      const uint32_t dr = static_cast<uint32_t>(it / C::ND);
+      if (dr > 0 && !(ok = wait_warp(b_dempty0 + 8 * ds, (dr - 1) & 1, ctl, a.status, a.timeout_ns)))
+        break;
+      uint8_t* slot = sD + ds * C::DSLOT;
+      float* L2s = reinterpret_cast<float*>(slot + C::TILE);
+      float* Ds = L2s + 128;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int64_t q = q0 + lane * 4 + t;
@@ -215,24 +263,24 @@ __global__ void __launch_bounds__(320, 1)
         Ds[lane * 4 + t] = q < N ? a.delta[bh * N + q] : 0.f;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(b_qfull0 + 8 * st, 2 * C::TILE);
-        for (int c = 0; c < C::DC; ++c) {
-          tma_load_4d(smem_u32(stage + c * C::CHUNK), &tmq, b_qfull0 + 8 * st, c * 64,
+        mbar_arrive_expect_tx(b_dfull0 + 8 * ds, C::TILE);
+        for (int c = 0; c < C::DC; ++c)
+          tma_load_4d(smem_u32(slot + c * C::CHUNK), &tmdo, b_dfull0 + 8 * ds, c * 64,
                       static_cast<int32_t>(q0), hh, bb);
-          tma_load_4d(smem_u32(stage + C::TILE + c * C::CHUNK), &tmdo, b_qfull0 + 8 * st, c * 64,
-                      static_cast<int32_t>(q0), hh, bb);
-        }
       } else {
-        mbar_arrive(b_qfull0 + 8 * st);
+        mbar_arrive(b_dfull0 + 8 * ds);
       }
-      last_round[st] = r + 1;
+      d_round[ds] = dr + 1;
     }
     // Drain: every copy issued has landed.
     if (lane == 0) {
       wait_bounded(b_kv, 0, ctl, a.status, a.timeout_ns, false);
-      for (int s = 0; s < C::NST; ++s)
-        if (last_round[s]) wait_bounded(b_qfull0 + 8 * s, (last_round[s] - 1) & 1, ctl, a.status,
-                                        a.timeout_ns, false);
+      for (int s = 0; s < C::NQ; ++s)
+        if (q_round[s]) wait_bounded(b_qfull0 + 8 * s, (q_round[s] - 1) & 1, ctl, a.status,
+                                     a.timeout_ns, false);
+      for (int s = 0; s < C::ND; ++s)
+        if (d_round[s]) wait_bounded(b_dfull0 + 8 * s, (d_round[s] - 1) & 1, ctl, a.status,
+                                     a.timeout_ns, false);
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -242,33 +290,42 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t idG = idesc_f16<T>(128, D, false, true);
       const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sV), 16, 1024);
-      const uint64_t dSt0 = sdesc_sw128(smem_u32(sStage), 16, 1024);          // K-major view
-      const uint64_t dSt0mn = sdesc_sw128(smem_u32(sStage), C::CHUNK, 1024);  // MN-major view
-      bool ok = wait_bounded(b_kv, 0, ctl, a.status, a.timeout_ns);
-      for (int it = 0; ok && it < n; ++it) {
-        const int st = it % C::NST;
-        if (!(ok = wait_bounded(b_qfull0 + 8 * st, (it / C::NST) & 1, ctl, a.status, a.timeout_ns)))
-          break;
-        tc_fence_after();
-        const uint64_t stq = dSt0 + static_cast<uint64_t>((st * C::STAGE) >> 4);
-        const uint64_t stdo = stq + static_cast<uint64_t>(C::TILE >> 4);
-        // S^T = K Q^T, then dP^T = V dO^T  (both K-major operands)
+      const uint64_t dQk = sdesc_sw128(smem_u32(sQ), 16, 1024);          // K-major views
+      const uint64_t dDk = sdesc_sw128(smem_u32(sD), 16, 1024);
+      const uint64_t dQm = sdesc_sw128(smem_u32(sQ), C::CHUNK, 1024);    // MN-major views
+      const uint64_t dDm = sdesc_sw128(smem_u32(sD), C::CHUNK, 1024);
+      auto issue_ST = [&](int qs) {   // S^T = K Q^T
+        const uint64_t q = dQk + static_cast<uint64_t>((qs * C::TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_ST, dK0 + off, stq + off, idS, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::COL_ST, dK0 + off, q + off, idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(b_sfull);
+      };
+      auto issue_DPT = [&](int ds) {  // dP^T = V dO^T
+        const uint64_t g = dDk + static_cast<uint64_t>((ds * C::DSLOT) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_DPT, dV0 + off, stdo + off, idS, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::COL_DPT, dV0 + off, g + off, idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(b_dpfull);
-        // dV += P^T dO and dK += dS^T Q, per 64-query half as each is ready.
-        // B operands are the same tiles read MN-major (N = d).
-        const uint64_t mq = dSt0mn + static_cast<uint64_t>((st * C::STAGE) >> 4);
-        const uint64_t mdo = mq + static_cast<uint64_t>(C::TILE >> 4);
+      };
+      bool ok = wait_bounded(b_kv, 0, ctl, a.status, a.timeout_ns) &&
+                wait_bounded(b_qfull0, 0, ctl, a.status, a.timeout_ns) &&
+                wait_bounded(b_dfull0, 0, ctl, a.status, a.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        issue_ST(0);
+        issue_DPT(0);
+      }
+      for (int it = 0; ok && it < n; ++it) {
+        const int qs = it % C::NQ, ds = it % C::ND;
+        const bool next = it + 1 < n;
+        const int qs1 = (it + 1) % C::NQ, ds1 = (it + 1) % C::ND;
+        // dV += P^T dO (B: this tile's dO read MN-major, N = d)
+        const uint64_t mdo = dDm + static_cast<uint64_t>((ds * C::DSLOT) >> 4);
         for (int h = 0; ok && h < 2; ++h) {
           if (!(ok = wait_bounded(b_pready0 + 8 * h, it & 1, ctl, a.status, a.timeout_ns))) break;
           tc_fence_after();
@@ -278,6 +335,16 @@ __global__ void __launch_bounds__(320, 1)
                    mdo + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
                    (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
+        if (!ok) break;
+        if (next) {
+          if (!(ok = wait_bounded(b_qfull0 + 8 * qs1, ((it + 1) / C::NQ) & 1, ctl, a.status,
+                                  a.timeout_ns)))
+            break;
+          tc_fence_after();
+          issue_ST(qs1);
+        }
+        // dK += dS^T Q (B: this tile's Q read MN-major)
+        const uint64_t mq = dQm + static_cast<uint64_t>((qs * C::TILE) >> 4);
         for (int h = 0; ok && h < 2; ++h) {
           if (!(ok = wait_bounded(b_dsready0 + 8 * h, it & 1, ctl, a.status, a.timeout_ns))) break;
           tc_fence_after();
@@ -288,7 +355,15 @@ __global__ void __launch_bounds__(320, 1)
                    (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        mma_commit(b_qempty0 + 8 * st);
+        mma_commit(b_qempty0 + 8 * qs);
+        mma_commit(b_dempty0 + 8 * ds);
+        if (next) {
+          if (!(ok = wait_bounded(b_dfull0 + 8 * ds1, ((it + 1) / C::ND) & 1, ctl, a.status,
+                                  a.timeout_ns)))
+            break;
+          tc_fence_after();
+          issue_DPT(ds1);
+        }
       }
       if (ok) mma_commit(b_accdone);
       mma_commit(b_mmadone);
@@ -304,11 +379,12 @@ __global__ void __launch_bounds__(320, 1)
     const float c = a.c;
     bool ok = true;
     for (int it = 0; it < n; ++it) {
-      const int i = i0 + it, st = it % C::NST;
+      const int i = i0 + it, ds = it % C::ND;
       if (!(ok = wait_warp(b_sfull, it & 1, ctl, a.status, a.timeout_ns))) break;
-      if (!(ok = wait_warp(b_qfull0 + 8 * st, (it / C::NST) & 1, ctl, a.status, a.timeout_ns))) break;
+      // the dO slot's arrival also publishes the staged L and Delta
+      if (!(ok = wait_warp(b_dfull0 + 8 * ds, (it / C::ND) & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
-      const float* L2s = reinterpret_cast<const float*>(sStage + st * C::STAGE + 2 * C::TILE) + 64 * hf;
+      const float* L2s = reinterpret_cast<const float*>(sD + ds * C::DSLOT + C::TILE) + 64 * hf;
       const float* Ds = L2s + 128;
       float p[64];
       tmem_ld64(lane_base + C::COL_ST + 64 * hf, p);
