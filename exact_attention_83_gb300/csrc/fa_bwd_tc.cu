@@ -449,17 +449,39 @@ __global__ void __launch_bounds__(320, 1)
 // ============================================================================
 // dQ
 // ============================================================================
+// Q_i and dO_i are only A operands (of S = Q K^T and dP = dO V^T), so they are
+// copied once into TMEM and their shared memory then holds key tiles: NST
+// stages of K_j | V_j, the last of which first receives Q_i and dO_i.
 template <int D>
 struct DqCfg : BwdShape<D> {
   using S = BwdShape<D>;
-  static constexpr int NST = D == 128 ? 2 : 4;               // key-tile stages (K | V)
+  static constexpr int NST = D == 128 ? 3 : 6;               // key-tile stages (K | V)
   static constexpr int STAGE = 2 * S::TILE;
-  static constexpr int OFF_DO = S::TILE;
-  static constexpr int OFF_STAGES = 2 * S::TILE;
-  static constexpr int OFF_BAR = OFF_STAGES + NST * STAGE;
+  static constexpr int QSLOT = NST - 1;                      // stage that first holds Q | dO
+  static constexpr int OFF_BAR = NST * STAGE;
   static constexpr int SMEM = OFF_BAR + 1024 + 1024;
-  static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DQ = 256;
+  // TMEM: Q and dO (input type, two per column), the dQ accumulator, S and dP
+  // (fp32; dS is written over the first 32 columns of each dP half).
+  static constexpr uint32_t COL_Q = 0, COL_DO = D / 2, COL_DQ = D, COL_S = 256, COL_DP = 384;
 };
+
+// Copies this thread's row of a 128-byte-swizzled 128 x D tile (shared
+// memory) into D / 2 TMEM columns of its lane, two elements per column, as an
+// A operand.
+template <int D>
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int row, uint32_t taddr) {
+#pragma unroll
+  for (int ch = 0; ch < D / 64; ++ch) {
+    const uint8_t* base = tile + ch * (128 * 128) + row * 128;
+    uint32_t w[32];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 x = *reinterpret_cast<const uint4*>(base + ((u ^ (row & 7)) << 4));
+      w[4 * u] = x.x; w[4 * u + 1] = x.y; w[4 * u + 2] = x.z; w[4 * u + 3] = x.w;
+    }
+    tmem_st32(taddr + 32 * ch, w);
+  }
+}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(320, 1)
@@ -467,12 +489,13 @@ __global__ void __launch_bounds__(320, 1)
                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                      const BwdTcArgs a) {
   using C = DqCfg<D>;
+  static_assert(C::SMEM <= 232448, "shared memory per block");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sDO = smem + C::OFF_DO;
-  uint8_t* sStage = smem + C::OFF_STAGES;   // stage st: K | V
+  uint8_t* sStage = smem;                   // stage st: K | V
+  uint8_t* sQ = smem + C::QSLOT * C::STAGE; // Q | dO before they move to TMEM
+  uint8_t* sDO = sQ + C::TILE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   Ctl* ctl = reinterpret_cast<Ctl*>(bars + 48);
   const uint32_t b_q = smem_u32(&bars[0]);
@@ -484,6 +507,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t b_dsready0 = smem_u32(&bars[4 + 2 * C::NST]);   // + 8 * half
   const uint32_t b_accdone = smem_u32(&bars[6 + 2 * C::NST]);
   const uint32_t b_mmadone = smem_u32(&bars[7 + 2 * C::NST]);
+  const uint32_t b_qt = smem_u32(&bars[8 + 2 * C::NST]);         // Q, dO are in TMEM
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t id = blockIdx.x;
@@ -506,6 +530,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int h = 0; h < 2; ++h) mbar_init(b_dsready0 + 8 * h, 128);
     mbar_init(b_accdone, 1);
     mbar_init(b_mmadone, 1);
+    mbar_init(b_qt, 256);
     ctl->abort = 0;
     mbar_fence_init();
   }
@@ -534,8 +559,12 @@ __global__ void __launch_bounds__(320, 1)
       for (int jt = 0; jt < n; ++jt) {
         const int st = jt % C::NST;
         const uint32_t r = static_cast<uint32_t>(jt / C::NST);
-        if (r > 0 && !wait_bounded(b_kvempty0 + 8 * st, (r - 1) & 1, ctl, a.status, a.timeout_ns))
-          break;
+        if (r > 0) {
+          if (!wait_bounded(b_kvempty0 + 8 * st, (r - 1) & 1, ctl, a.status, a.timeout_ns)) break;
+        } else if (st == C::QSLOT) {
+          // this stage still holds Q | dO until they have been copied into TMEM
+          if (!wait_bounded(b_qt, 0, ctl, a.status, a.timeout_ns)) break;
+        }
         uint8_t* stage = sStage + st * C::STAGE;
         mbar_arrive_expect_tx(b_kvfull0 + 8 * st, 2 * C::TILE);
         for (int c = 0; c < C::DC; ++c) {
@@ -554,31 +583,30 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     // Order: S_0, dP_0, then per key tile jt: S_jt+1 (once S_jt has been read
-    // out of TMEM), dQ += dS_jt K_jt (per half as ready), dP_jt+1.
+    // out of TMEM), dQ += dS_jt K_jt (per half as ready), dP_jt+1 (it
+    // overwrites dS_jt, read only by the dQ products issued before it).
     if (lane == 0) {
       const uint32_t idS = idesc_f16<T>(128, C::BT, false, false);
       const uint32_t idG = idesc_f16<T>(128, D, false, true);
-      const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dDOd = sdesc_sw128(smem_u32(sDO), 16, 1024);
       const uint64_t dSt0 = sdesc_sw128(smem_u32(sStage), 16, 1024);
       const uint64_t dSt0mn = sdesc_sw128(smem_u32(sStage), C::CHUNK, 1024);
-      auto issue_S = [&](int st) {
+      auto issue_S = [&](int st) {   // S = Q K^T, Q from TMEM
         const uint64_t kb = dSt0 + static_cast<uint64_t>((st * C::STAGE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_S, dQd + off, kb + off, idS, kk > 0 ? 1u : 0u);
+          mma_ts(tmem + C::COL_S, tmem + C::COL_Q + 8 * kk, kb + off, idS, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_dP = [&](int st) {
+      auto issue_dP = [&](int st) {  // dP = dO V^T, dO from TMEM
         const uint64_t vb = dSt0 + static_cast<uint64_t>((st * C::STAGE + C::TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_DP, dDOd + off, vb + off, idS, kk > 0 ? 1u : 0u);
+          mma_ts(tmem + C::COL_DP, tmem + C::COL_DO + 8 * kk, vb + off, idS, kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns) &&
+      bool ok = wait_bounded(b_qt, 0, ctl, a.status, a.timeout_ns) &&
                 wait_bounded(b_kvfull0, 0, ctl, a.status, a.timeout_ns);
       if (ok) {
         tc_fence_after();
@@ -631,8 +659,15 @@ __global__ void __launch_bounds__(320, 1)
     const float c = a.c;
     const float l2 = qrow < N ? a.lse[bh * N + qrow] * kLog2e : INFINITY;
     const float dl = qrow < N ? a.delta[bh * N + qrow] : 0.f;
-    bool ok = true;
-    for (int jt = 0; jt < n; ++jt) {
+    // Q (warps 0-3) and dO (warps 4-7) into TMEM as A operands.
+    bool ok = wait_warp(b_q, 0, ctl, a.status, a.timeout_ns);
+    if (ok) {
+      tile_row_to_tmem<D>(hf == 0 ? sQ : sDO, row, lane_base + (hf == 0 ? C::COL_Q : C::COL_DO));
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    mbar_arrive(b_qt);
+    for (int jt = 0; ok && jt < n; ++jt) {
       if (!(ok = wait_warp(b_sfull, jt & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
       float p[64];
