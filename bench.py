@@ -44,10 +44,10 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 1040.7 MB per launch measured on 16 heads,
+    # bwd_dkdv_tc_kernel<bf16,128>: 1044.2 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("dkdv", "63a060bd06fb4364b587c9ec8216570b4ac8e28f8a1eeb49acfd0653e401d3f7",
-     "long-bf16-B1-H32-N16384-D128-causal"): 2081.4e6,
+    ("dkdv", "558c14be612ebef4da9c1c4ac9f907c1327a5579e07a8d5f106ae7974d19f2ad",
+     "long-bf16-B1-H32-N16384-D128-causal"): 2088.5e6,
 }
 
 
@@ -291,7 +291,11 @@ def main():
     flops_step = w.fwd_bwd_flops()
     value = world * flops_step / (ms_step * 1e-3) / 1e12
     pk = peaks()
-    peak_dense = pk["bf16_tflops_sustained"]
+    # The timed region lasts tens of milliseconds and the sampled SM clock stays
+    # at its maximum, so the burst cuBLAS rate is the denominator (the more
+    # demanding of the two); the sustained-rate fraction is reported beside it.
+    peak_dense = pk["bf16_tflops"]
+    peak_sustained = pk["bf16_tflops_sustained"]
 
     # dominant kernel: the dK/dV kernel (4 of the 7 N x N x D products of the
     # split backward); its algorithmic flops are 4 products of 2*N^2*D per
@@ -322,7 +326,8 @@ def main():
             "fwd_ms": fwd_only_ms,
             "fwd_frac_of_peak": flops_fwd / (fwd_only_ms * 1e-3) / 1e12 / peak_dense,
             "fwd_bwd_frac_of_peak": value / world / peak_dense,
-            "peak_tflops": peak_dense, "peak_source": pk["source"] + " sustained bf16",
+            "fwd_bwd_frac_of_sustained_peak": value / world / peak_sustained,
+            "peak_tflops": peak_dense, "peak_source": pk["source"] + " burst bf16 (cuBLAS)",
             "kernel_ms": {"fwd": fwd_ms, "preprocess": pre_ms, "bwd_dkdv": dkdv_ms,
                           "bwd_dq": dq_ms},
             "roofline": {"kernel": "bwd_dkdv", "bound": "tensor", "achieved": achieved,
