@@ -28,6 +28,7 @@ std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
 std::mutex g_mu;
 cudaEvent_t g_prof_events[3];
 std::atomic<bool> g_prof_on{false};
+std::atomic<int> g_withhold_next{0};   // one-shot test switch (fa_test_withhold_next_arrival)
 struct DeviceInfo {
   int state = 0;              // 0: not set up, 1: ready, -1: not sm_103
   int sm_count = 0;
@@ -152,7 +153,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   p.B = B; p.H = H; p.N = N; p.D = D;
   p.causal = causal ? 1 : 0; p.scale = scale; p.dtype = dtype;
   p.status = dev->status; p.timeout_ns = g_timeout_ns.load();
-  if (use_tc(dtype) && have_fwd_tc(D, dtype)) return launch_fwd_tc(p, stream);
+  if (use_tc(dtype) && have_fwd_tc(D, dtype)) {
+    p.withhold_arrival = g_withhold_next.exchange(0);
+    return launch_fwd_tc(p, stream);
+  }
   return launch_fwd_ffma(p, stream);
 }
 
@@ -254,6 +258,8 @@ void fa_set_profile_events(const cudaEvent_t* events) {
     g_prof_on.store(false);
   }
 }
+
+void fa_test_withhold_next_arrival(void) { g_withhold_next.store(1); }
 
 int fa_version(void) { return 0x000100; }
 

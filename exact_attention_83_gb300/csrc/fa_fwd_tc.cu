@@ -67,6 +67,7 @@ struct FwdTcArgs {
   float c;                 // scale * log2(e)
   unsigned int* status;
   uint64_t timeout_ns;
+  int withhold_arrival;    // test-only: CTA 0 skips the first S-ready arrival of tile 0
 };
 
 template <typename T, int D>
@@ -205,7 +206,9 @@ __global__ void __launch_bounds__(320, 1)
         for (int g = 0; g < 2; ++g)
           if (ntile[g] > 0) {
             issue_S(g, 0);
-            mma_commit(b_sfull0 + 8 * g);
+            // A test can withhold this arrival in CTA 0 to make the softmax
+            // warps' bounded wait run out (the timeout path, without a fault).
+            if (!(a.withhold_arrival && blockIdx.x == 0 && g == 0)) mma_commit(b_sfull0 + 8 * g);
           }
         mma_commit(b_empty0);
       }
@@ -390,6 +393,7 @@ fa_status run_fwd_tc(const FwdParams& p, cudaStream_t stream) {
   a.c = p.scale * kLog2e;
   a.status = p.status;
   a.timeout_ns = p.timeout_ns;
+  a.withhold_arrival = p.withhold_arrival;
   const int64_t blocks = a.BH * a.npairs;
   if (blocks > 0x7fffffffLL) return FA_ERR_SHAPE;
   auto kern = fwd_tc_kernel<T, D>;

@@ -22,6 +22,7 @@ struct FwdParams {
   fa_dtype dtype;
   unsigned int* status;   // device status word (FA_ERR_TIMEOUT on a wait that ran out)
   uint64_t timeout_ns;    // bound on any single device-side wait
+  int withhold_arrival;   // test-only: CTA 0 skips one mbarrier arrival (see fa.h)
 };
 
 struct PreParams {

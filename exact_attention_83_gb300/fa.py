@@ -42,7 +42,8 @@ STATUS_NAMES = {
 
 EXPORTED = ("fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_get_device_status",
             "fa_status_string", "fa_set_path", "fa_set_wait_timeout_ns",
-            "fa_set_profile_events", "fa_version", "fa_bwd_noalloc")
+            "fa_set_profile_events", "fa_version", "fa_bwd_noalloc",
+            "fa_test_withhold_next_arrival")
 
 
 class FAError(RuntimeError):
@@ -95,6 +96,8 @@ def load_library(path: str = LIB_PATH):
         lib.fa_set_profile_events.argtypes = [ctypes.c_void_p]
         lib.fa_set_profile_events.restype = None
         lib.fa_version.restype = ctypes.c_int
+        lib.fa_test_withhold_next_arrival.argtypes = []
+        lib.fa_test_withhold_next_arrival.restype = None
         if os.environ.get("FA_WAIT_TIMEOUT_NS"):
             lib.fa_set_wait_timeout_ns(int(os.environ["FA_WAIT_TIMEOUT_NS"]))
         _lib = lib
