@@ -73,11 +73,14 @@ def _load():
         lib.oracle_query_rows.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64,
                                           _i64, ctypes.c_int, ctypes.c_double,
                                           _i64, ctypes.POINTER(ctypes.c_int64),
-                                          _dp, _dp, _dp, _dp]
+                                          _dp, _dp, _dp, _dp, _dp, _dp]
         lib.oracle_key_rows.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64,
                                         _i64, ctypes.c_int, ctypes.c_double,
                                         _i64, ctypes.POINTER(ctypes.c_int64),
-                                        _dp, _dp]
+                                        _dp, _dp, _dp, _dp]
+        lib.oracle_magnitudes.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64,
+                                          ctypes.c_int, ctypes.c_double, _dp, _dp, _dp,
+                                          _dp]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
@@ -93,6 +96,10 @@ def _f64(x) -> np.ndarray:
 
 def _ptr(a: np.ndarray):
     return a.ctypes.data_as(_dp)
+
+
+def _ptr_or_null(a):
+    return None if a is None else _ptr(a)
 
 
 def _shape(q: np.ndarray):
@@ -157,33 +164,59 @@ def _rows(rows):
     return rows, rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
 
 
-def query_rows(q, k, v, do, causal: bool, rows, scale: float | None = None):
+def query_rows(q, k, v, do, causal: bool, rows, scale: float | None = None,
+               magnitudes: bool = False):
     """Row-local outputs for sampled query rows (rows: [n, 2] of (b*H+h, i)).
-    Returns dict o [n,D], lse [n], delta [n], dq [n,D]."""
+    Returns dict o [n,D], lse [n], delta [n], dq [n,D]; with magnitudes=True
+    also o_abs, dq_abs [n,D] (the sums of magnitudes()) for those rows."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, D = _shape(q)
     scale = default_scale(D) if scale is None else float(scale)
     rows, rp = _rows(rows)
     n = rows.shape[0]
     o = np.empty((n, D)); L = np.empty((n,)); delta = np.empty((n,)); dq = np.empty((n, D))
+    oa = np.empty((n, D)) if magnitudes else None
+    qa = np.empty((n, D)) if magnitudes else None
     _load().oracle_query_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, N, D,
                               int(bool(causal)), scale, n, rp, _ptr(o), _ptr(L),
-                              _ptr(delta), _ptr(dq))
-    return dict(o=o, lse=L, delta=delta, dq=dq)
+                              _ptr(delta), _ptr(dq), _ptr_or_null(oa), _ptr_or_null(qa))
+    out = dict(o=o, lse=L, delta=delta, dq=dq)
+    if magnitudes:
+        out.update(o_abs=oa, dq_abs=qa)
+    return out
 
 
-def key_rows(q, k, v, do, causal: bool, rows, scale: float | None = None):
+def key_rows(q, k, v, do, causal: bool, rows, scale: float | None = None,
+             magnitudes: bool = False):
     """dK, dV for sampled key rows (rows: [n, 2] of (b*H+h, j)).
-    Returns dict dk [n,D], dv [n,D]."""
+    Returns dict dk [n,D], dv [n,D]; with magnitudes=True also dk_abs, dv_abs."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, N, D = _shape(q)
     scale = default_scale(D) if scale is None else float(scale)
     rows, rp = _rows(rows)
     n = rows.shape[0]
     dk = np.empty((n, D)); dv = np.empty((n, D))
+    ka = np.empty((n, D)) if magnitudes else None
+    va = np.empty((n, D)) if magnitudes else None
     _load().oracle_key_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, N, D,
-                            int(bool(causal)), scale, n, rp, _ptr(dk), _ptr(dv))
-    return dict(dk=dk, dv=dv)
+                            int(bool(causal)), scale, n, rp, _ptr(dk), _ptr(dv),
+                            _ptr_or_null(ka), _ptr_or_null(va))
+    out = dict(dk=dk, dv=dv)
+    if magnitudes:
+        out.update(dk_abs=ka, dv_abs=va)
+    return out
+
+
+def magnitudes(q, k, v, do, causal: bool, scale: float | None = None):
+    """Componentwise magnitude sums for rounding-error bounds: dict o, dq, dk,
+    dv of sum P|V|, scale sum |dS||K|, scale sum |dS||Q|, sum P|dO|."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, H, N, D = _shape(q)
+    scale = default_scale(D) if scale is None else float(scale)
+    o = np.empty((B, H, N, D)); dq = np.empty_like(o); dk = np.empty_like(o); dv = np.empty_like(o)
+    _load().oracle_magnitudes(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B, H, N, D,
+                              int(bool(causal)), scale, _ptr(o), _ptr(dq), _ptr(dk), _ptr(dv))
+    return dict(o=o, dq=dq, dk=dk, dv=dv)
 
 
 def dense(q, k, v, do, causal: bool, scale: float | None = None,

@@ -230,7 +230,8 @@ void oracle_query_rows(const double* Q, const double* K, const double* V,
                        const double* dO, int64_t B, int64_t H, int64_t N,
                        int64_t D, int causal, double scale, int64_t n_rows,
                        const int64_t* rows, double* O_rows, double* L_rows,
-                       double* Delta_rows, double* dQ_rows) {
+                       double* Delta_rows, double* dQ_rows, double* Oabs_rows,
+                       double* dQabs_rows) {
   (void)B; (void)H;
 #pragma omp parallel
   {
@@ -254,6 +255,21 @@ void oracle_query_rows(const double* Q, const double* K, const double* V,
         for (int64_t d = 0; d < D; ++d) dqi[d] += ds * kj[d];
       }
       for (int64_t d = 0; d < D; ++d) dqi[d] *= scale;
+      if (Oabs_rows == nullptr) continue;
+      // magnitude sums, as in oracle_magnitudes
+      double* oa = Oabs_rows + t * D;
+      double* qa = dQabs_rows + t * D;
+      for (int64_t d = 0; d < D; ++d) { oa[d] = 0.0; qa[d] = 0.0; }
+      for (int64_t j = 0; j < nk; ++j) {
+        const double* vj = V + base + j * D;
+        const double* kj = K + base + j * D;
+        const double ads = std::fabs(p[j] * (dot(doi, vj, D) - delta));
+        for (int64_t d = 0; d < D; ++d) {
+          oa[d] += p[j] * std::fabs(vj[d]);
+          qa[d] += ads * std::fabs(kj[d]);
+        }
+      }
+      for (int64_t d = 0; d < D; ++d) qa[d] *= scale;
     }
   }
 }
@@ -265,7 +281,8 @@ void oracle_query_rows(const double* Q, const double* K, const double* V,
 void oracle_key_rows(const double* Q, const double* K, const double* V,
                      const double* dO, int64_t B, int64_t H, int64_t N,
                      int64_t D, int causal, double scale, int64_t n_rows,
-                     const int64_t* rows, double* dK_rows, double* dV_rows) {
+                     const int64_t* rows, double* dK_rows, double* dV_rows,
+                     double* dKabs_rows, double* dVabs_rows) {
   (void)B; (void)H;
   std::vector<int64_t> heads;
   for (int64_t t = 0; t < n_rows; ++t) heads.push_back(rows[2 * t]);
@@ -294,6 +311,11 @@ void oracle_key_rows(const double* Q, const double* K, const double* V,
       double* dkj = dK_rows + t * D;
       double* dvj = dV_rows + t * D;
       for (int64_t d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
+      if (dKabs_rows != nullptr)
+        for (int64_t d = 0; d < D; ++d) {
+          dKabs_rows[t * D + d] = 0.0;
+          dVabs_rows[t * D + d] = 0.0;
+        }
       for (int64_t i = causal ? j : 0; i < N; ++i) {
         const double* qi = Q + base + i * D;
         const double* doi = dO + base + i * D;
@@ -303,8 +325,82 @@ void oracle_key_rows(const double* Q, const double* K, const double* V,
           dvj[d] += pij * doi[d];
           dkj[d] += ds * qi[d];
         }
+        if (dKabs_rows == nullptr) continue;
+        // magnitude sums, as in oracle_magnitudes
+        double* ka = dKabs_rows + t * D;
+        double* va = dVabs_rows + t * D;
+        for (int64_t d = 0; d < D; ++d) {
+          va[d] += pij * std::fabs(doi[d]);
+          ka[d] += std::fabs(ds) * std::fabs(qi[d]);
+        }
       }
       for (int64_t d = 0; d < D; ++d) dkj[d] *= scale;
+      if (dKabs_rows != nullptr)
+        for (int64_t d = 0; d < D; ++d) dKabs_rows[t * D + d] *= scale;
+    }
+  }
+}
+
+// Componentwise magnitude sums of the same products, for rounding-error
+// bounds: a sum of products whose factors each carry a relative error of at
+// most u deviates from the exact sum by at most u times the sum of the
+// products' absolute values (the standard componentwise bound).
+//   Oabs_id  = sum_j P_ij |V_jd|           dVabs_jd = sum_i P_ij |dO_id|
+//   dQabs_id = scale sum_j |dS_ij| |K_jd|  dKabs_jd = scale sum_i |dS_ij| |Q_id|
+// with P, dS as in oracle_fwd_bwd (P >= 0, so no absolute value is needed on it).
+void oracle_magnitudes(const double* Q, const double* K, const double* V,
+                       const double* dO, int64_t B, int64_t H, int64_t N,
+                       int64_t D, int causal, double scale, double* Oabs,
+                       double* dQabs, double* dKabs, double* dVabs) {
+  const int64_t BH = B * H;
+  std::vector<double> L(BH * N), Delta(BH * N);
+#pragma omp parallel
+  {
+    std::vector<double> p(static_cast<size_t>(N)), oi(static_cast<size_t>(D));
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t r = 0; r < BH * N; ++r) {
+      const int64_t bh = r / N, i = r % N;
+      const int64_t base = bh * N * D;
+      const int64_t nk = keys_allowed(i, N, causal);
+      const double* doi = dO + base + i * D;
+      row_forward(Q + base + i * D, K + base, V + base, nk, D, scale, p.data(),
+                  oi.data(), &L[bh * N + i]);
+      const double delta = dot(doi, oi.data(), D);
+      Delta[bh * N + i] = delta;
+      double* oa = Oabs + base + i * D;
+      double* qa = dQabs + base + i * D;
+      for (int64_t d = 0; d < D; ++d) { oa[d] = 0.0; qa[d] = 0.0; }
+      for (int64_t j = 0; j < nk; ++j) {
+        const double* vj = V + base + j * D;
+        const double* kj = K + base + j * D;
+        const double ads = std::fabs(p[j] * (dot(doi, vj, D) - delta));
+        for (int64_t d = 0; d < D; ++d) {
+          oa[d] += p[j] * std::fabs(vj[d]);
+          qa[d] += ads * std::fabs(kj[d]);
+        }
+      }
+      for (int64_t d = 0; d < D; ++d) qa[d] *= scale;
+    }
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t r = 0; r < BH * N; ++r) {
+      const int64_t bh = r / N, j = r % N;
+      const int64_t base = bh * N * D;
+      const double* kj = K + base + j * D;
+      const double* vj = V + base + j * D;
+      double* ka = dKabs + base + j * D;
+      double* va = dVabs + base + j * D;
+      for (int64_t d = 0; d < D; ++d) { ka[d] = 0.0; va[d] = 0.0; }
+      for (int64_t i = causal ? j : 0; i < N; ++i) {
+        const double* qi = Q + base + i * D;
+        const double* doi = dO + base + i * D;
+        const double pij = std::exp(scale * dot(qi, kj, D) - L[bh * N + i]);
+        const double ads = std::fabs(pij * (dot(doi, vj, D) - Delta[bh * N + i]));
+        for (int64_t d = 0; d < D; ++d) {
+          va[d] += pij * std::fabs(doi[d]);
+          ka[d] += ads * std::fabs(qi[d]);
+        }
+      }
+      for (int64_t d = 0; d < D; ++d) ka[d] *= scale;
     }
   }
 }

@@ -265,3 +265,31 @@ def test_sampled_rows_match_full(causal):
         np.testing.assert_allclose(qr["dq"][t], full["dq"][b, h, i], rtol=0, atol=1e-13)
         np.testing.assert_allclose(kr["dk"][t], full["dk"][b, h, i], rtol=0, atol=1e-13)
         np.testing.assert_allclose(kr["dv"][t], full["dv"][b, h, i], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_magnitudes_bound_the_values_and_match_them_for_one_signed_terms(causal):
+    """sum |terms| >= |sum of terms| everywhere, with equality when every term
+    has the same sign (V >= 0 for O, dO >= 0 for dV)."""
+    q, k, v, do = (rnd((2, 2, 60, 8), s, 2.0) for s in (90, 91, 92, 93))
+    g = oracle.fwd_bwd(q, k, v, do, causal)
+    m = oracle.magnitudes(q, k, v, do, causal)
+    for key in ("o", "dq", "dk", "dv"):
+        assert (m[key] >= np.abs(g[key]) - 1e-12).all(), key
+    vp, dop = np.abs(v), np.abs(do)
+    g2 = oracle.fwd_bwd(q, k, vp, dop, causal)
+    m2 = oracle.magnitudes(q, k, vp, dop, causal)
+    np.testing.assert_allclose(m2["o"], g2["o"], rtol=1e-13, atol=0)
+    np.testing.assert_allclose(m2["dv"], g2["dv"], rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_magnitudes_equal_full_magnitudes(causal):
+    q, k, v, do = (rnd((2, 3, 70, 16), s, 4.0) for s in (94, 95, 96, 97))
+    m = oracle.magnitudes(q, k, v, do, causal)
+    rows = np.array([[0, 0], [1, 69], [4, 33], [5, 1]])
+    qr = oracle.query_rows(q, k, v, do, causal, rows, magnitudes=True)
+    kr = oracle.key_rows(q, k, v, do, causal, rows, magnitudes=True)
+    b, h, i = rows[:, 0] // 3, rows[:, 0] % 3, rows[:, 1]
+    for key, src in (("o", qr), ("dq", qr), ("dk", kr), ("dv", kr)):
+        np.testing.assert_allclose(src[key + "_abs"], m[key][b, h, i], rtol=1e-12, atol=1e-300)
