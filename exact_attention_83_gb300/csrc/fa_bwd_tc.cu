@@ -51,6 +51,7 @@ struct BwdTcArgs {
   void* out0;              // dK/dV kernel: dV;  dQ kernel: dQ
   void* out1;              // dK/dV kernel: dK
   int64_t H, N, BH, ntiles;
+  int dreal;               // head dimension stored (<= D; narrower ones run zero-padded)
   int64_t s0[4], s1[4];    // strides of out0, out1
   int causal;
   float c;                 // scale * log2(e)
@@ -81,29 +82,6 @@ __device__ __forceinline__ void tmem_st_packed64(uint32_t taddr, const float (&x
 #pragma unroll
   for (int i = 0; i < 32; ++i) w[i] = pack2<T>(x[2 * i], x[2 * i + 1]);
   tmem_st32(taddr, w);
-}
-
-// Epilogue: NCOL fp32 columns of this thread's lane (starting at taddr), times
-// `mul`, rounded to T, stored to a row of global memory (when `store`).
-template <typename T, int NCOL>
-__device__ __forceinline__ void store_row(uint32_t taddr, float mul, T* row, bool store) {
-#pragma unroll
-  for (int cc = 0; cc < NCOL / 32; ++cc) {
-    uint32_t t[32];
-    tmem_ld32(taddr + 32 * cc, t);
-    tmem_wait_ld();
-    reg_fence32(t);
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      w[i] = pack2<T>(__uint_as_float(t[2 * i]) * mul, __uint_as_float(t[2 * i + 1]) * mul);
-    if (store) {
-      uint4* dst = reinterpret_cast<uint4*>(row + 32 * cc);
-#pragma unroll
-      for (int v4 = 0; v4 < 4; ++v4)
-        dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
-    }
-  }
 }
 
 // ============================================================================
@@ -430,10 +408,10 @@ __global__ void __launch_bounds__(320, 1)
       const bool store = key < N;
       if (hf == 0) {
         T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hh * a.s0[1] + key * a.s0[2];
-        store_row<T, D>(lane_base + C::COL_DV, 1.f, out, store);
+        store_row_cols<T>(lane_base + C::COL_DV, 1.f, out, store, a.dreal);
       } else {
         T* out = static_cast<T*>(a.out1) + bb * a.s1[0] + hh * a.s1[1] + key * a.s1[2];
-        store_row<T, D>(lane_base + C::COL_DK, a.scale, out, store);
+        store_row_cols<T>(lane_base + C::COL_DK, a.scale, out, store, a.dreal);
       }
     }
   }
@@ -699,8 +677,12 @@ __global__ void __launch_bounds__(320, 1)
     if (ok) ok = wait_warp(b_accdone, 0, ctl, a.status, a.timeout_ns);
     if (ok) {
       tc_fence_after();
-      T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hh * a.s0[1] + qrow * a.s0[2] + (D / 2) * hf;
-      store_row<T, D / 2>(lane_base + C::COL_DQ + (D / 2) * hf, a.scale, out, qrow < N);
+      // each warpgroup stores half the columns; a zero-padded narrow head
+      // dimension is stored by warpgroup 0 alone
+      const int half = a.dreal == D ? D / 2 : (hf == 0 ? a.dreal : 0);
+      const int c0 = a.dreal == D ? (D / 2) * hf : 0;
+      T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hh * a.s0[1] + qrow * a.s0[2] + c0;
+      if (half > 0) store_row_cols<T>(lane_base + C::COL_DQ + c0, a.scale, out, qrow < N, half);
     }
   }
 
@@ -714,13 +696,15 @@ __global__ void __launch_bounds__(320, 1)
 
 template <typename T, int D>
 fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
+  // Tensor maps carry the true head dimension (zero fill past it).
   CUtensorMap mq, mk, mv, mdo;
-  if (!encode_tile_map(&mq, p.q, p.dtype, p.B, p.H, p.N, D, p.sq, 128, 64) ||
-      !encode_tile_map(&mk, p.k, p.dtype, p.B, p.H, p.N, D, p.sk, 128, 64) ||
-      !encode_tile_map(&mv, p.v, p.dtype, p.B, p.H, p.N, D, p.sv, 128, 64) ||
-      !encode_tile_map(&mdo, p.dout, p.dtype, p.B, p.H, p.N, D, p.sdo, 128, 64))
+  if (!encode_tile_map(&mq, p.q, p.dtype, p.B, p.H, p.N, p.D, p.sq, 128, 64) ||
+      !encode_tile_map(&mk, p.k, p.dtype, p.B, p.H, p.N, p.D, p.sk, 128, 64) ||
+      !encode_tile_map(&mv, p.v, p.dtype, p.B, p.H, p.N, p.D, p.sv, 128, 64) ||
+      !encode_tile_map(&mdo, p.dout, p.dtype, p.B, p.H, p.N, p.D, p.sdo, 128, 64))
     return FA_ERR_LAUNCH;
   BwdTcArgs a{};
+  a.dreal = static_cast<int>(p.D);
   a.lse = p.lse; a.delta = p.delta;
   a.H = p.H; a.N = p.N; a.BH = p.B * p.H; a.ntiles = (p.N + 127) / 128;
   a.causal = p.causal;
@@ -758,15 +742,18 @@ fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-bool have_bwd_tc(int64_t D, fa_dtype dt) { return (D == 64 || D == 128) && dt != FA_F32; }
+// D = 16 and 32 run through the D = 64 kernels, zero-padded by the TMA loads.
+bool have_bwd_tc(int64_t D, fa_dtype dt) {
+  return (D == 16 || D == 32 || D == 64 || D == 128) && dt != FA_F32;
+}
 
 fa_status launch_bwd_tc(const BwdParams& p, cudaStream_t s) {
   if (p.dtype == FA_BF16) {
     if (p.D == 128) return run_bwd_tc<__nv_bfloat16, 128>(p, s);
-    if (p.D == 64) return run_bwd_tc<__nv_bfloat16, 64>(p, s);
+    if (p.D <= 64) return run_bwd_tc<__nv_bfloat16, 64>(p, s);
   } else if (p.dtype == FA_F16) {
     if (p.D == 128) return run_bwd_tc<__half, 128>(p, s);
-    if (p.D == 64) return run_bwd_tc<__half, 64>(p, s);
+    if (p.D <= 64) return run_bwd_tc<__half, 64>(p, s);
   }
   return FA_ERR_ARG;
 }

@@ -62,6 +62,7 @@ struct FwdTcArgs {
   void* o;
   float* lse;
   int64_t H, N, BH, npairs;
+  int dreal;               // head dimension stored (<= D; narrower ones run zero-padded)
   int64_t so[4];
   int causal;
   float c;                 // scale * log2(e)
@@ -348,23 +349,7 @@ __global__ void __launch_bounds__(320, 1)
       const float inv = 1.f / l;
       const bool store = qrow < N;
       T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hh * a.so[1] + qrow * a.so[2];
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t t[32];
-        tmem_ld32(tO + 32 * cc, t);
-        tmem_wait_ld();
-        reg_fence32(t);
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack2<T>(__uint_as_float(t[2 * i]) * inv, __uint_as_float(t[2 * i + 1]) * inv);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * cc);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
-        }
-      }
+      store_row_cols<T>(tO, inv, orow, store, a.dreal);
       if (store) a.lse[bh * N + qrow] = (m + log2f(l)) * kLn2;
     }
   }
@@ -380,12 +365,15 @@ __global__ void __launch_bounds__(320, 1)
 template <typename T, int D>
 fa_status run_fwd_tc(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
+  // Tensor maps carry the true head dimension; a narrower one than D reads
+  // as zeros past its end (TMA fill), which leaves every product exact.
   CUtensorMap mq, mk, mv;
-  if (!encode_tile_map(&mq, p.q, p.dtype, p.B, p.H, p.N, D, p.sq, 128, 64) ||
-      !encode_tile_map(&mk, p.k, p.dtype, p.B, p.H, p.N, D, p.sk, 128, 64) ||
-      !encode_tile_map(&mv, p.v, p.dtype, p.B, p.H, p.N, D, p.sv, 128, 64))
+  if (!encode_tile_map(&mq, p.q, p.dtype, p.B, p.H, p.N, p.D, p.sq, 128, 64) ||
+      !encode_tile_map(&mk, p.k, p.dtype, p.B, p.H, p.N, p.D, p.sk, 128, 64) ||
+      !encode_tile_map(&mv, p.v, p.dtype, p.B, p.H, p.N, p.D, p.sv, 128, 64))
     return FA_ERR_LAUNCH;
   FwdTcArgs a{};
+  a.dreal = static_cast<int>(p.D);
   a.o = p.o; a.lse = p.lse;
   a.H = p.H; a.N = p.N; a.BH = p.B * p.H; a.npairs = (p.N + 255) / 256;
   for (int i = 0; i < 4; ++i) a.so[i] = p.so[i];
@@ -406,15 +394,18 @@ fa_status run_fwd_tc(const FwdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-bool have_fwd_tc(int64_t D, fa_dtype dt) { return (D == 64 || D == 128) && dt != FA_F32; }
+// D = 16 and 32 run through the D = 64 kernel, zero-padded by the TMA loads.
+bool have_fwd_tc(int64_t D, fa_dtype dt) {
+  return (D == 16 || D == 32 || D == 64 || D == 128) && dt != FA_F32;
+}
 
 fa_status launch_fwd_tc(const FwdParams& p, cudaStream_t s) {
   if (p.dtype == FA_BF16) {
     if (p.D == 128) return run_fwd_tc<__nv_bfloat16, 128>(p, s);
-    if (p.D == 64) return run_fwd_tc<__nv_bfloat16, 64>(p, s);
+    if (p.D <= 64) return run_fwd_tc<__nv_bfloat16, 64>(p, s);
   } else if (p.dtype == FA_F16) {
     if (p.D == 128) return run_fwd_tc<__half, 128>(p, s);
-    if (p.D == 64) return run_fwd_tc<__half, 64>(p, s);
+    if (p.D <= 64) return run_fwd_tc<__half, 64>(p, s);
   }
   return FA_ERR_ARG;
 }

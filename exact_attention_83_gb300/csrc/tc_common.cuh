@@ -207,6 +207,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 
+// 16 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // Register fence: makes the compiler treat the 32 registers as redefined at
 // this point, so no use of a tcgen05.ld destination is scheduled before the
 // tcgen05.wait::ld that precedes this call (and no tcgen05.st source is reused
@@ -219,6 +231,13 @@ __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
                  "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
                  "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
                  "+r"(r[30]), "+r"(r[31])::"memory");
+}
+
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])::"memory");
 }
 
 // ---------------------------------------------------------------- descriptors
@@ -257,6 +276,54 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+}  // namespace tc
+}  // namespace fa
+
+namespace fa {
+namespace tc {
+
+// Epilogue store: `ncols` (a multiple of 16, at most 128, uniform across the
+// warp) fp32 columns of this thread's TMEM lane starting at taddr, times
+// `mul`, rounded to T and written to `row` (16-byte vector stores) when
+// `store`.  Used with ncols < the accumulator width when a narrow head
+// dimension runs zero-padded through a wider kernel.
+template <typename T>
+__device__ __forceinline__ void store_row_cols(uint32_t taddr, float mul, T* row, bool store,
+                                               int ncols) {
+  int c = 0;
+  for (; c + 32 <= ncols; c += 32) {
+    uint32_t t[32];
+    tmem_ld32(taddr + c, t);
+    tmem_wait_ld();
+    reg_fence32(t);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      w[i] = pack2<T>(__uint_as_float(t[2 * i]) * mul, __uint_as_float(t[2 * i + 1]) * mul);
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(row + c);
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4)
+        dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+    }
+  }
+  if (c < ncols) {   // 16 columns left
+    uint32_t t[16];
+    tmem_ld16(taddr + c, t);
+    tmem_wait_ld();
+    reg_fence16(t);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      w[i] = pack2<T>(__uint_as_float(t[2 * i]) * mul, __uint_as_float(t[2 * i + 1]) * mul);
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(row + c);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
 }
 
 }  // namespace tc
