@@ -20,6 +20,7 @@ Recipe (every workload):
 from __future__ import annotations
 
 import dataclasses
+import itertools
 import math
 
 import torch
@@ -111,3 +112,96 @@ def coverage(D: int, N: int, dtype: str, causal: bool) -> Workload:
 
 LONG_CAUSAL = Workload("long-bf16-B1-H32-N16384-D128-causal", 1, 32, 16384, 128,
                        "bf16", True)
+
+
+# ---------------------------------------------------------------- general problems
+@dataclasses.dataclass(frozen=True)
+class GeneralWorkload:
+    """Query and key lengths that differ, grouped key/value heads, packed
+    variable lengths (seqlens_q / seqlens_k set) and dropout of the weights.
+    Fixed lengths: q, do [B, Hq, Nq, D], k, v [B, Hkv, Nk, D].  Packed:
+    q, do [sum(seqlens_q), Hq, D], k, v [sum(seqlens_k), Hkv, D]; B is the
+    number of sequences, Nq / Nk their maxima."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    D: int
+    dtype: str
+    causal: bool
+    seqlens_q: tuple | None = None
+    seqlens_k: tuple | None = None
+    dropout_p: float = 0.0
+    seed: int = 0
+    drop_seed: int = 0x5EED
+    drop_offset: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def packed(self) -> bool:
+        return self.seqlens_q is not None
+
+    def pairs(self) -> int:
+        """(query, key) pairs attended per query head: sum over sequences of
+        Nq*Nk, or of sum_i min(i + 1, Nk) when causal (top-left mask)."""
+        lens = (list(zip(self.seqlens_q, self.seqlens_k)) if self.packed
+                else [(self.Nq, self.Nk)] * self.B)
+        tot = 0
+        for nq, nk in lens:
+            if not self.causal:
+                tot += nq * nk
+            else:
+                m = min(nq, nk)          # rows 0..m-1 see i+1 keys, the rest all nk
+                tot += m * (m + 1) // 2 + (nq - m) * nk
+        return tot
+
+    def fwd_flops(self) -> float:
+        """Two matmuls over the attended pairs, 2 flops per multiply-add."""
+        return 4.0 * self.Hq * self.D * self.pairs()
+
+    def fwd_bwd_flops(self) -> float:
+        return 3.5 * self.fwd_flops()
+
+
+def make_general_inputs(w: GeneralWorkload, device="cpu"):
+    """(q, k, v, do, cu_q, cu_k): randn in float32 in the order Q, K, V, dO from
+    the seeded CPU generator, rounded to the dtype; cu_* are int32 offsets
+    (None for fixed lengths)."""
+    g = torch.Generator("cpu")
+    g.manual_seed(w.seed)
+    dt = DTYPES[w.dtype]
+    if w.packed:
+        tq, tk = sum(w.seqlens_q), sum(w.seqlens_k)
+        shapes = [(tq, w.Hq, w.D), (tk, w.Hkv, w.D), (tk, w.Hkv, w.D), (tq, w.Hq, w.D)]
+    else:
+        shapes = [(w.B, w.Hq, w.Nq, w.D), (w.B, w.Hkv, w.Nk, w.D), (w.B, w.Hkv, w.Nk, w.D),
+                  (w.B, w.Hq, w.Nq, w.D)]
+    out = [torch.randn(s, generator=g, dtype=torch.float32).to(dt) for s in shapes]
+    cu_q = cu_k = None
+    if w.packed:
+        cu_q = torch.tensor([0] + list(itertools.accumulate(w.seqlens_q)), dtype=torch.int32)
+        cu_k = torch.tensor([0] + list(itertools.accumulate(w.seqlens_k)), dtype=torch.int32)
+    if device != "cpu":
+        out = [t.to(device) for t in out]
+        if cu_q is not None:
+            cu_q, cu_k = cu_q.to(device), cu_k.to(device)
+    return (*out, cu_q, cu_k)
+
+
+def seqlen_mix(total: int, lo: int, hi: int, seed: int) -> tuple:
+    """Sequence lengths drawn uniformly from [lo, hi] (seeded) until they sum
+    to `total` (the last one is cut to fit)."""
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    lens, acc = [], 0
+    while acc < total:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=g))
+        n = min(n, total - acc)
+        lens.append(n)
+        acc += n
+    return tuple(lens)

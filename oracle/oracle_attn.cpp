@@ -26,19 +26,41 @@
 //    Scratch in Triton", step 5, prints a garbled version of these equations;
 //    it is not followed.
 //
+// General problems.  The Triton page's test harness runs shapes whose query
+// and key counts differ, with the causal mask the lower triangle of the
+// Nq x Nk score matrix; the pages name grouped-query and multi-query
+// attention, variable-length batches and dropout as branches they leave out,
+// without defining them.  The oracle takes their plainest readings:
+//  * grouped heads: Hq query heads and Hkv key/value heads, Hq % Hkv == 0;
+//    query head h reads key/value head h / (Hq / Hkv); dK, dV of a key/value
+//    head sum the contributions of every query head that reads it;
+//  * variable lengths (Python wrapper): each packed sequence is its own
+//    problem, positions counted from its first row;
+//  * dropout: each weight P_ij is multiplied by Z_ij = keep_ij / (1 - p)
+//    before the product with V (O = (P o Z) V); L stays the log-sum-exp of the
+//    undropped scores; then dV = (P o Z)^T dO and dS = P o (Z o dP - Delta),
+//    Delta = rowsum(dO o O) as before.  keep_ij is drawn from Philox4x32-10
+//    (Salmon et al., SC 2011) at counter (j / 4, i, flat head, offset); word
+//    j mod 4 is compared with floor(p * 2^32).
+//
 // Readings where the pages are open (each is also listed in the design notes):
 //  * masked keys are excluded exactly (weight 0, never a finite sentinel);
-//  * L is in natural-log units and always fp64 here;
+//  * L is in natural-log units and always fp64 here; a row with no key at all
+//    has L = -inf and O = 0 (the empty sum);
 //  * Delta uses the oracle's own fp64 O.
 //
-// Layout: every tensor is a dense row-major [B, H, N, D] array of doubles
-// (L and Delta are [B, H, N]).  Inputs are the exact values of the rounded
-// device inputs (fp16/bf16/fp32 -> double is exact).
+// Layout: every tensor is a dense row-major array of doubles: Q, O, dO, dQ
+// [B, Hq, Nq, D]; K, V, dK, dV [B, Hkv, Nk, D]; L and Delta [B, Hq, Nq].
+// Inputs are the exact values of the rounded device inputs (fp16/bf16/fp32
+// -> double is exact).
 //
 // Pins: softmax rows sum to 1; closed forms for constant V, causal row 0,
 // Q = 0 and N = 1; finite differences of the forward; sum_j dK_j = 0;
 // sum_j dV_j = sum_i dO_i; tile-size invariance; agreement with the dense
-// N x N materialisation and with a library routine.  See tests/test_oracle_pins.py.
+// N x N materialisation and with a library routine (tests/test_oracle_pins.py);
+// Nq != Nk and grouped heads against the library routine, Philox known-answer
+// vectors, dropout gradients against finite differences, packed against
+// batched numbering (tests/test_oracle_pins_general.py).
 
 #include <cmath>
 #include <cstdint>
@@ -59,38 +81,220 @@ inline double dot(const double* a, const double* b, int64_t D) {
   return s;
 }
 
-// Number of keys query row i may attend to: all N, or keys 0..i when causal
+// Number of keys query row i may attend to: all Nk, or keys 0..i when causal
 // (top-left aligned mask, "FlashAttention-2 from PyTorch to Triton", kernel's
-// causal predicate).
-inline int64_t keys_allowed(int64_t i, int64_t N, int causal) {
-  return causal ? (i + 1) : N;
+// causal predicate and its test harness, which builds the mask as the lower
+// triangle of the Nq x Nk score matrix).
+inline int64_t keys_allowed(int64_t i, int64_t Nk, int causal) {
+  return causal ? std::min(i + 1, Nk) : Nk;
+}
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
+// as 1, 2, 3", SC 2011): ten rounds; a round multiplies counter words 0 and 2
+// by the two round multipliers and mixes the high and low halves of the
+// products with words 1 and 3 and the key; the key is advanced by the two
+// Weyl increments between rounds.
+void philox(const uint32_t ctr[4], uint32_t k0, uint32_t k1, uint32_t out[4]) {
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c0;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
+    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ k0;
+    const uint32_t n1 = static_cast<uint32_t>(p1);
+    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ k1;
+    const uint32_t n3 = static_cast<uint32_t>(p0);
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Dropout of the attention weights (none when on == 0): weight (i, j) of flat
+// query head bh0 + (b * Hq + h) is kept iff word (j mod 4) of Philox4x32-10 at
+// counter (j / 4, i, bh0 + b * Hq + h, offset) under key (key0, key1) is
+// >= thr; a kept weight is multiplied by rscale = 1 / (1 - p).  i and j are
+// positions within the sequence; bh0 lets a packed batch pass one sequence at
+// a time with its own head numbering.
+typedef struct {
+  int on;
+  uint32_t thr;
+  double rscale;
+  uint32_t key0, key1, offset;
+  int64_t bh0;
+} oracle_dropout;
+
+}  // extern "C"
+
+namespace {
+
+// Z_ij of one weight, 1 without dropout.
+inline double zfac(const oracle_dropout* dr, int64_t i, int64_t j, int64_t bh) {
+  if (dr == nullptr || !dr->on) return 1.0;
+  const uint32_t ctr[4] = {static_cast<uint32_t>(j >> 2), static_cast<uint32_t>(i),
+                           static_cast<uint32_t>(dr->bh0 + bh), dr->offset};
+  uint32_t w[4];
+  philox(ctr, dr->key0, dr->key1, w);
+  return w[j & 3] >= dr->thr ? dr->rscale : 0.0;
 }
 
 // Forward for one query row (the plain definition).
 //   s_j = scale * q_i . k_j          for allowed j
 //   m   = max_j s_j
-//   L   = m + log sum_j exp(s_j - m)           (= log sum_j exp(s_j))
+//   L   = m + log sum_j exp(s_j - m)           (= log sum_j exp(s_j); -inf
+//                                               when no key is allowed)
 //   p_j = exp(s_j - L)
-//   o_i = sum_j p_j v_j
-// `s` is scratch of at least N doubles; on return it holds p_j.
+//   o_i = sum_j z_j p_j v_j          (z_j = 1 without dropout)
+// `s` is scratch of at least nk doubles; on return it holds p_j.  z is null
+// (no dropout) or holds z_j.
 void row_forward(const double* qi, const double* K, const double* V,
-                 int64_t nk, int64_t D, double scale,
+                 int64_t nk, int64_t D, double scale, const double* z,
                  double* s, double* oi, double* Li) {
   double m = -std::numeric_limits<double>::infinity();
   for (int64_t j = 0; j < nk; ++j) {
     s[j] = scale * dot(qi, K + j * D, D);
     m = std::max(m, s[j]);
   }
+  for (int64_t d = 0; d < D; ++d) oi[d] = 0.0;
+  if (nk == 0) {
+    *Li = -std::numeric_limits<double>::infinity();
+    return;
+  }
   double sum = 0.0;
   for (int64_t j = 0; j < nk; ++j) sum += std::exp(s[j] - m);
   const double L = m + std::log(sum);
-  for (int64_t d = 0; d < D; ++d) oi[d] = 0.0;
   for (int64_t j = 0; j < nk; ++j) {
     s[j] = std::exp(s[j] - L);
+    const double w = z ? z[j] * s[j] : s[j];
     const double* vj = V + j * D;
-    for (int64_t d = 0; d < D; ++d) oi[d] += s[j] * vj[d];
+    for (int64_t d = 0; d < D; ++d) oi[d] += w * vj[d];
   }
   *Li = L;
+}
+
+// Shapes of one call: Q, O, dO, dQ [B, Hq, Nq, D]; K, V, dK, dV [B, Hkv, Nk,
+// D]; L, Delta [B, Hq, Nq].  Query head h reads key/value head h / (Hq / Hkv).
+struct Dims {
+  int64_t B, Hq, Hkv, Nq, Nk, D;
+  int64_t G() const { return Hq / Hkv; }
+  // base offsets of query head qh = b*Hq + h and of its key/value head
+  int64_t qbase(int64_t qh) const { return qh * Nq * D; }
+  int64_t kbase(int64_t qh) const { return ((qh / Hq) * Hkv + (qh % Hq) / G()) * Nk * D; }
+};
+
+// Pass 1 for one query row: O_i, L_i, Delta_i = dO_i . O_i and
+//   dQ_i = scale * sum_j P_ij (Z_ij (dO_i . v_j) - Delta_i) k_j
+// (dQ and Delta only when dO is non-null).  Optionally the magnitude sums
+//   Oabs_i = sum_j Z_ij P_ij |v_j|,  dQabs_i = scale * sum_j |dS_ij| |k_j|.
+void query_row(const Dims& dm, const double* Q, const double* K, const double* V,
+               const double* dO, int causal, double scale, const oracle_dropout* dr,
+               int64_t qh, int64_t i, std::vector<double>& p, std::vector<double>& z,
+               double* oi, double* Li, double* Deltai, double* dqi, double* oabs,
+               double* dqabs) {
+  const int64_t D = dm.D;
+  const int64_t qb = dm.qbase(qh), kb = dm.kbase(qh);
+  const int64_t nk = keys_allowed(i, dm.Nk, causal);
+  const bool drop = dr && dr->on;
+  if (drop)
+    for (int64_t j = 0; j < nk; ++j) z[j] = zfac(dr, i, j, qh);
+  row_forward(Q + qb + i * D, K + kb, V + kb, nk, D, scale, drop ? z.data() : nullptr,
+              p.data(), oi, Li);
+  if (oabs) {
+    for (int64_t d = 0; d < D; ++d) oabs[d] = 0.0;
+    for (int64_t j = 0; j < nk; ++j) {
+      const double w = (drop ? z[j] : 1.0) * p[j];
+      const double* vj = V + kb + j * D;
+      for (int64_t d = 0; d < D; ++d) oabs[d] += w * std::fabs(vj[d]);
+    }
+  }
+  if (!dO) return;
+  const double* doi = dO + qb + i * D;
+  const double delta = dot(doi, oi, D);
+  if (Deltai) *Deltai = delta;
+  for (int64_t d = 0; d < D; ++d) dqi[d] = 0.0;
+  if (dqabs)
+    for (int64_t d = 0; d < D; ++d) dqabs[d] = 0.0;
+  for (int64_t j = 0; j < nk; ++j) {
+    const double* kj = K + kb + j * D;
+    const double dpt = dot(doi, V + kb + j * D, D);
+    const double ds = p[j] * ((drop ? z[j] : 1.0) * dpt - delta);
+    for (int64_t d = 0; d < D; ++d) dqi[d] += ds * kj[d];
+    if (dqabs)
+      for (int64_t d = 0; d < D; ++d) dqabs[d] += std::fabs(ds) * std::fabs(kj[d]);
+  }
+  for (int64_t d = 0; d < D; ++d) dqi[d] *= scale;
+  if (dqabs)
+    for (int64_t d = 0; d < D; ++d) dqabs[d] *= scale;
+}
+
+// Pass 2 for one key row j of flat key/value head kh = b*Hkv + hk: over every
+// query head h of its group and every query i that may attend to key j (all i,
+// or i >= j when causal),
+//   P_ij = exp(scale q_i . k_j - L_i),  Z_ij as above,  dP_ij = dO_i . v_j,
+//   dS_ij = P_ij (Z_ij dP_ij - Delta_i),
+//   dV_j = sum Z_ij P_ij dO_i,  dK_j = scale * sum dS_ij q_i.
+// L and Delta are the full [B, Hq, Nq] arrays.  Optionally the magnitude sums
+//   dVabs_j = sum Z_ij P_ij |dO_i|,  dKabs_j = scale * sum |dS_ij| |q_i|.
+void key_row(const Dims& dm, const double* Q, const double* K, const double* V,
+             const double* dO, const double* L, const double* Delta, int causal,
+             double scale, const oracle_dropout* dr, int64_t kh, int64_t j, double* dkj,
+             double* dvj, double* dkabs, double* dvabs) {
+  const int64_t D = dm.D, G = dm.G();
+  const int64_t b = kh / dm.Hkv, hk = kh % dm.Hkv;
+  const double* kj = K + kh * dm.Nk * D + j * D;
+  const double* vj = V + kh * dm.Nk * D + j * D;
+  for (int64_t d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
+  if (dkabs)
+    for (int64_t d = 0; d < D; ++d) { dkabs[d] = 0.0; dvabs[d] = 0.0; }
+  for (int64_t g = 0; g < G; ++g) {
+    const int64_t qh = b * dm.Hq + hk * G + g;
+    const int64_t qb = dm.qbase(qh);
+    for (int64_t i = causal ? j : 0; i < dm.Nq; ++i) {
+      const double* qi = Q + qb + i * D;
+      const double* doi = dO + qb + i * D;
+      const double pij = std::exp(scale * dot(qi, kj, D) - L[qh * dm.Nq + i]);
+      const double z = zfac(dr, i, j, qh);
+      const double ds = pij * (z * dot(doi, vj, D) - Delta[qh * dm.Nq + i]);
+      for (int64_t d = 0; d < D; ++d) {
+        dvj[d] += z * pij * doi[d];
+        dkj[d] += ds * qi[d];
+      }
+      if (dkabs)
+        for (int64_t d = 0; d < D; ++d) {
+          dvabs[d] += z * pij * std::fabs(doi[d]);
+          dkabs[d] += std::fabs(ds) * std::fabs(qi[d]);
+        }
+    }
+  }
+  for (int64_t d = 0; d < D; ++d) dkj[d] *= scale;
+  if (dkabs)
+    for (int64_t d = 0; d < D; ++d) dkabs[d] *= scale;
+}
+
+// L and Delta of every query row of the listed flat query heads (pass 1
+// without dQ), for pass 2.
+void stats_for_heads(const Dims& dm, const double* Q, const double* K, const double* V,
+                     const double* dO, int causal, double scale, const oracle_dropout* dr,
+                     const std::vector<int64_t>& qheads, double* L, double* Delta) {
+  for (const int64_t qh : qheads) {
+#pragma omp parallel
+    {
+      std::vector<double> p(static_cast<size_t>(dm.Nk)), z(static_cast<size_t>(dm.Nk)),
+          oi(static_cast<size_t>(dm.D));
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t i = 0; i < dm.Nq; ++i) {
+        query_row(dm, Q, K, V, nullptr, causal, scale, dr, qh, i, p, z, oi.data(),
+                  &L[qh * dm.Nq + i], nullptr, nullptr, nullptr, nullptr);
+        Delta[qh * dm.Nq + i] = dot(dO + dm.qbase(qh) + i * dm.D, oi.data(), dm.D);
+      }
+    }
+  }
 }
 
 }  // namespace
@@ -113,294 +317,155 @@ void oracle_set_num_threads(int n) {
 #endif
 }
 
-// Forward: O [B,H,N,D], L [B,H,N].
-void oracle_fwd(const double* Q, const double* K, const double* V,
-                int64_t B, int64_t H, int64_t N, int64_t D,
-                int causal, double scale, double* O, double* L) {
-  const int64_t BH = B * H;
+// Philox4x32-10 of one counter under one key (for the generator's pins).
+void oracle_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* out) {
+  philox(ctr, key[0], key[1], out);
+}
+
+// Forward: O [B,Hq,Nq,D], L [B,Hq,Nq].
+void oracle_fwd(const double* Q, const double* K, const double* V, int64_t B,
+                int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D, int causal,
+                double scale, const oracle_dropout* dr, double* O, double* L) {
+  const Dims dm{B, Hq, Hkv, Nq, Nk, D};
 #pragma omp parallel
   {
-    std::vector<double> s(static_cast<size_t>(N));
+    std::vector<double> p(static_cast<size_t>(Nk)), z(static_cast<size_t>(Nk));
 #pragma omp for schedule(dynamic, 16)
-    for (int64_t r = 0; r < BH * N; ++r) {
-      const int64_t bh = r / N, i = r % N;
-      const int64_t base = bh * N * D;
-      row_forward(Q + base + i * D, K + base, V + base,
-                  keys_allowed(i, N, causal), D, scale, s.data(),
-                  O + base + i * D, L + bh * N + i);
+    for (int64_t r = 0; r < B * Hq * Nq; ++r) {
+      const int64_t qh = r / Nq, i = r % Nq;
+      query_row(dm, Q, K, V, nullptr, causal, scale, dr, qh, i, p, z,
+                O + dm.qbase(qh) + i * D, L + qh * Nq + i, nullptr, nullptr, nullptr,
+                nullptr);
     }
   }
 }
 
-// Forward for a list of sampled rows.  rows[2*t] = flat head index b*H+h,
+// Forward for a list of sampled rows.  rows[2*t] = flat query head b*Hq+h,
 // rows[2*t+1] = query index i.  O_rows [n_rows, D], L_rows [n_rows].
-void oracle_fwd_rows(const double* Q, const double* K, const double* V,
-                     int64_t B, int64_t H, int64_t N, int64_t D,
-                     int causal, double scale, int64_t n_rows,
+void oracle_fwd_rows(const double* Q, const double* K, const double* V, int64_t B,
+                     int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
+                     int causal, double scale, const oracle_dropout* dr, int64_t n_rows,
                      const int64_t* rows, double* O_rows, double* L_rows) {
-  (void)B; (void)H;
+  const Dims dm{B, Hq, Hkv, Nq, Nk, D};
 #pragma omp parallel
   {
-    std::vector<double> s(static_cast<size_t>(N));
+    std::vector<double> p(static_cast<size_t>(Nk)), z(static_cast<size_t>(Nk));
 #pragma omp for schedule(dynamic, 1)
-    for (int64_t t = 0; t < n_rows; ++t) {
-      const int64_t bh = rows[2 * t], i = rows[2 * t + 1];
-      const int64_t base = bh * N * D;
-      row_forward(Q + base + i * D, K + base, V + base,
-                  keys_allowed(i, N, causal), D, scale, s.data(),
-                  O_rows + t * D, L_rows + t);
-    }
+    for (int64_t t = 0; t < n_rows; ++t)
+      query_row(dm, Q, K, V, nullptr, causal, scale, dr, rows[2 * t], rows[2 * t + 1], p, z,
+                O_rows + t * D, L_rows + t, nullptr, nullptr, nullptr, nullptr);
   }
 }
 
-// Forward and backward.  Outputs O, L, Delta, dQ, dK, dV.
-//
-// Pass 1, one query row at a time (rows are independent):
-//   O_i, L_i, P_i as in row_forward;
-//   Delta_i = dO_i . O_i                         (rowsum(dO o O))
-//   dP_ij   = dO_i . v_j
-//   dS_ij   = P_ij (dP_ij - Delta_i)
-//   dQ_i    = scale * sum_j dS_ij k_j
-// Pass 2, one key row at a time (keys are independent):
-//   for every query i that may attend to key j (all i, or i >= j if causal):
-//     P_ij = exp(scale q_i.k_j - L_i),  dP_ij = dO_i . v_j,
-//     dS_ij = P_ij (dP_ij - Delta_i)
-//   dV_j = sum_i P_ij dO_i,   dK_j = scale * sum_i dS_ij q_i
-void oracle_fwd_bwd(const double* Q, const double* K, const double* V,
-                    const double* dO, int64_t B, int64_t H, int64_t N,
-                    int64_t D, int causal, double scale, double* O, double* L,
-                    double* Delta, double* dQ, double* dK, double* dV) {
-  const int64_t BH = B * H;
+// Forward and backward.  Outputs O, L, Delta, dQ (query-shaped) and dK, dV
+// (key-shaped): pass 1 over every query row, then pass 2 over every key row.
+void oracle_fwd_bwd(const double* Q, const double* K, const double* V, const double* dO,
+                    int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
+                    int causal, double scale, const oracle_dropout* dr, double* O,
+                    double* L, double* Delta, double* dQ, double* dK, double* dV) {
+  const Dims dm{B, Hq, Hkv, Nq, Nk, D};
 #pragma omp parallel
   {
-    std::vector<double> p(static_cast<size_t>(N));
+    std::vector<double> p(static_cast<size_t>(Nk)), z(static_cast<size_t>(Nk));
 #pragma omp for schedule(dynamic, 16)
-    for (int64_t r = 0; r < BH * N; ++r) {
-      const int64_t bh = r / N, i = r % N;
-      const int64_t base = bh * N * D;
-      const int64_t nk = keys_allowed(i, N, causal);
-      const double* doi = dO + base + i * D;
-      double* oi = O + base + i * D;
-      row_forward(Q + base + i * D, K + base, V + base, nk, D, scale,
-                  p.data(), oi, L + bh * N + i);
-      const double delta = dot(doi, oi, D);
-      Delta[bh * N + i] = delta;
-      double* dqi = dQ + base + i * D;
-      for (int64_t d = 0; d < D; ++d) dqi[d] = 0.0;
-      for (int64_t j = 0; j < nk; ++j) {
-        const double dp = dot(doi, V + base + j * D, D);
-        const double ds = p[j] * (dp - delta);
-        const double* kj = K + base + j * D;
-        for (int64_t d = 0; d < D; ++d) dqi[d] += ds * kj[d];
-      }
-      for (int64_t d = 0; d < D; ++d) dqi[d] *= scale;
+    for (int64_t r = 0; r < B * Hq * Nq; ++r) {
+      const int64_t qh = r / Nq, i = r % Nq;
+      const int64_t at = dm.qbase(qh) + i * D;
+      query_row(dm, Q, K, V, dO, causal, scale, dr, qh, i, p, z, O + at, L + qh * Nq + i,
+                Delta + qh * Nq + i, dQ + at, nullptr, nullptr);
     }
-
 #pragma omp for schedule(dynamic, 16)
-    for (int64_t r = 0; r < BH * N; ++r) {
-      const int64_t bh = r / N, j = r % N;
-      const int64_t base = bh * N * D;
-      const double* kj = K + base + j * D;
-      const double* vj = V + base + j * D;
-      double* dkj = dK + base + j * D;
-      double* dvj = dV + base + j * D;
-      for (int64_t d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
-      const int64_t i0 = causal ? j : 0;
-      for (int64_t i = i0; i < N; ++i) {
-        const double* qi = Q + base + i * D;
-        const double* doi = dO + base + i * D;
-        const double pij = std::exp(scale * dot(qi, kj, D) - L[bh * N + i]);
-        const double dp = dot(doi, vj, D);
-        const double ds = pij * (dp - Delta[bh * N + i]);
-        for (int64_t d = 0; d < D; ++d) {
-          dvj[d] += pij * doi[d];
-          dkj[d] += ds * qi[d];
-        }
-      }
-      for (int64_t d = 0; d < D; ++d) dkj[d] *= scale;
+    for (int64_t r = 0; r < B * Hkv * Nk; ++r) {
+      const int64_t kh = r / Nk, j = r % Nk;
+      const int64_t at = kh * Nk * D + j * D;
+      key_row(dm, Q, K, V, dO, L, Delta, causal, scale, dr, kh, j, dK + at, dV + at, nullptr,
+              nullptr);
     }
   }
 }
 
 // Sampled query rows: O_i, L_i, Delta_i and dQ_i are row-local (they need
 // only query row i and every key), so they are computed one row at a time
-// with the same formulas as pass 1 of oracle_fwd_bwd.
-// rows[2*t] = flat head index b*H+h, rows[2*t+1] = query index i.
-void oracle_query_rows(const double* Q, const double* K, const double* V,
-                       const double* dO, int64_t B, int64_t H, int64_t N,
-                       int64_t D, int causal, double scale, int64_t n_rows,
-                       const int64_t* rows, double* O_rows, double* L_rows,
+// with pass 1.  rows[2*t] = flat query head b*Hq+h, rows[2*t+1] = i.
+// Oabs_rows / dQabs_rows: the magnitude sums of oracle_magnitudes, or null.
+void oracle_query_rows(const double* Q, const double* K, const double* V, const double* dO,
+                       int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk,
+                       int64_t D, int causal, double scale, const oracle_dropout* dr,
+                       int64_t n_rows, const int64_t* rows, double* O_rows, double* L_rows,
                        double* Delta_rows, double* dQ_rows, double* Oabs_rows,
                        double* dQabs_rows) {
-  (void)B; (void)H;
+  const Dims dm{B, Hq, Hkv, Nq, Nk, D};
 #pragma omp parallel
   {
-    std::vector<double> p(static_cast<size_t>(N));
+    std::vector<double> p(static_cast<size_t>(Nk)), z(static_cast<size_t>(Nk));
 #pragma omp for schedule(dynamic, 1)
-    for (int64_t t = 0; t < n_rows; ++t) {
-      const int64_t bh = rows[2 * t], i = rows[2 * t + 1];
-      const int64_t base = bh * N * D;
-      const int64_t nk = keys_allowed(i, N, causal);
-      const double* doi = dO + base + i * D;
-      double* oi = O_rows + t * D;
-      row_forward(Q + base + i * D, K + base, V + base, nk, D, scale, p.data(),
-                  oi, L_rows + t);
-      const double delta = dot(doi, oi, D);
-      Delta_rows[t] = delta;
-      double* dqi = dQ_rows + t * D;
-      for (int64_t d = 0; d < D; ++d) dqi[d] = 0.0;
-      for (int64_t j = 0; j < nk; ++j) {
-        const double ds = p[j] * (dot(doi, V + base + j * D, D) - delta);
-        const double* kj = K + base + j * D;
-        for (int64_t d = 0; d < D; ++d) dqi[d] += ds * kj[d];
-      }
-      for (int64_t d = 0; d < D; ++d) dqi[d] *= scale;
-      if (Oabs_rows == nullptr) continue;
-      // magnitude sums, as in oracle_magnitudes
-      double* oa = Oabs_rows + t * D;
-      double* qa = dQabs_rows + t * D;
-      for (int64_t d = 0; d < D; ++d) { oa[d] = 0.0; qa[d] = 0.0; }
-      for (int64_t j = 0; j < nk; ++j) {
-        const double* vj = V + base + j * D;
-        const double* kj = K + base + j * D;
-        const double ads = std::fabs(p[j] * (dot(doi, vj, D) - delta));
-        for (int64_t d = 0; d < D; ++d) {
-          oa[d] += p[j] * std::fabs(vj[d]);
-          qa[d] += ads * std::fabs(kj[d]);
-        }
-      }
-      for (int64_t d = 0; d < D; ++d) qa[d] *= scale;
-    }
+    for (int64_t t = 0; t < n_rows; ++t)
+      query_row(dm, Q, K, V, dO, causal, scale, dr, rows[2 * t], rows[2 * t + 1], p, z,
+                O_rows + t * D, L_rows + t, Delta_rows + t, dQ_rows + t * D,
+                Oabs_rows ? Oabs_rows + t * D : nullptr,
+                dQabs_rows ? dQabs_rows + t * D : nullptr);
   }
 }
 
 // Sampled key rows: dK_j and dV_j need L_i and Delta_i of every query of the
-// head, so those are computed first for each head that holds a sampled key
-// (pass 1 of oracle_fwd_bwd without dQ), then pass 2 runs for the sampled
-// keys only.  rows as in oracle_query_rows, with j in place of i.
-void oracle_key_rows(const double* Q, const double* K, const double* V,
-                     const double* dO, int64_t B, int64_t H, int64_t N,
-                     int64_t D, int causal, double scale, int64_t n_rows,
+// query heads that read key/value head kh, so those are computed first (pass
+// 1 without dQ), then pass 2 runs for the sampled keys only.
+// rows[2*t] = flat key/value head b*Hkv+hk, rows[2*t+1] = key index j.
+void oracle_key_rows(const double* Q, const double* K, const double* V, const double* dO,
+                     int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
+                     int causal, double scale, const oracle_dropout* dr, int64_t n_rows,
                      const int64_t* rows, double* dK_rows, double* dV_rows,
                      double* dKabs_rows, double* dVabs_rows) {
-  (void)B; (void)H;
-  std::vector<int64_t> heads;
-  for (int64_t t = 0; t < n_rows; ++t) heads.push_back(rows[2 * t]);
-  std::sort(heads.begin(), heads.end());
-  heads.erase(std::unique(heads.begin(), heads.end()), heads.end());
-  std::vector<double> L(N), Delta(N);
-  for (const int64_t bh : heads) {
-    const int64_t base = bh * N * D;
-#pragma omp parallel
-    {
-      std::vector<double> p(static_cast<size_t>(N)), oi(static_cast<size_t>(D));
-#pragma omp for schedule(dynamic, 16)
-      for (int64_t i = 0; i < N; ++i) {
-        row_forward(Q + base + i * D, K + base, V + base,
-                    keys_allowed(i, N, causal), D, scale, p.data(), oi.data(),
-                    &L[i]);
-        Delta[i] = dot(dO + base + i * D, oi.data(), D);
-      }
-    }
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t t = 0; t < n_rows; ++t) {
-      if (rows[2 * t] != bh) continue;
-      const int64_t j = rows[2 * t + 1];
-      const double* kj = K + base + j * D;
-      const double* vj = V + base + j * D;
-      double* dkj = dK_rows + t * D;
-      double* dvj = dV_rows + t * D;
-      for (int64_t d = 0; d < D; ++d) { dkj[d] = 0.0; dvj[d] = 0.0; }
-      if (dKabs_rows != nullptr)
-        for (int64_t d = 0; d < D; ++d) {
-          dKabs_rows[t * D + d] = 0.0;
-          dVabs_rows[t * D + d] = 0.0;
-        }
-      for (int64_t i = causal ? j : 0; i < N; ++i) {
-        const double* qi = Q + base + i * D;
-        const double* doi = dO + base + i * D;
-        const double pij = std::exp(scale * dot(qi, kj, D) - L[i]);
-        const double ds = pij * (dot(doi, vj, D) - Delta[i]);
-        for (int64_t d = 0; d < D; ++d) {
-          dvj[d] += pij * doi[d];
-          dkj[d] += ds * qi[d];
-        }
-        if (dKabs_rows == nullptr) continue;
-        // magnitude sums, as in oracle_magnitudes
-        double* ka = dKabs_rows + t * D;
-        double* va = dVabs_rows + t * D;
-        for (int64_t d = 0; d < D; ++d) {
-          va[d] += pij * std::fabs(doi[d]);
-          ka[d] += std::fabs(ds) * std::fabs(qi[d]);
-        }
-      }
-      for (int64_t d = 0; d < D; ++d) dkj[d] *= scale;
-      if (dKabs_rows != nullptr)
-        for (int64_t d = 0; d < D; ++d) dKabs_rows[t * D + d] *= scale;
-    }
+  const Dims dm{B, Hq, Hkv, Nq, Nk, D};
+  const int64_t G = dm.G();
+  std::vector<int64_t> qheads;
+  for (int64_t t = 0; t < n_rows; ++t) {
+    const int64_t kh = rows[2 * t];
+    for (int64_t g = 0; g < G; ++g) qheads.push_back((kh / Hkv) * Hq + (kh % Hkv) * G + g);
   }
+  std::sort(qheads.begin(), qheads.end());
+  qheads.erase(std::unique(qheads.begin(), qheads.end()), qheads.end());
+  std::vector<double> L(static_cast<size_t>(B * Hq * Nq)), Delta(L.size());
+  stats_for_heads(dm, Q, K, V, dO, causal, scale, dr, qheads, L.data(), Delta.data());
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t t = 0; t < n_rows; ++t)
+    key_row(dm, Q, K, V, dO, L.data(), Delta.data(), causal, scale, dr, rows[2 * t],
+            rows[2 * t + 1], dK_rows + t * D, dV_rows + t * D,
+            dKabs_rows ? dKabs_rows + t * D : nullptr, dVabs_rows ? dVabs_rows + t * D : nullptr);
 }
 
 // Componentwise magnitude sums of the same products, for rounding-error
 // bounds: a sum of products whose factors each carry a relative error of at
 // most u deviates from the exact sum by at most u times the sum of the
 // products' absolute values (the standard componentwise bound).
-//   Oabs_id  = sum_j P_ij |V_jd|           dVabs_jd = sum_i P_ij |dO_id|
+//   Oabs_id  = sum_j Z P_ij |V_jd|         dVabs_jd = sum_i Z P_ij |dO_id|
 //   dQabs_id = scale sum_j |dS_ij| |K_jd|  dKabs_jd = scale sum_i |dS_ij| |Q_id|
-// with P, dS as in oracle_fwd_bwd (P >= 0, so no absolute value is needed on it).
-void oracle_magnitudes(const double* Q, const double* K, const double* V,
-                       const double* dO, int64_t B, int64_t H, int64_t N,
-                       int64_t D, int causal, double scale, double* Oabs,
+// with P, Z, dS as in oracle_fwd_bwd (P, Z >= 0, so no absolute value is
+// needed on them).
+void oracle_magnitudes(const double* Q, const double* K, const double* V, const double* dO,
+                       int64_t B, int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D,
+                       int causal, double scale, const oracle_dropout* dr, double* Oabs,
                        double* dQabs, double* dKabs, double* dVabs) {
-  const int64_t BH = B * H;
-  std::vector<double> L(BH * N), Delta(BH * N);
+  const Dims dm{B, Hq, Hkv, Nq, Nk, D};
+  std::vector<double> L(static_cast<size_t>(B * Hq * Nq)), Delta(L.size());
 #pragma omp parallel
   {
-    std::vector<double> p(static_cast<size_t>(N)), oi(static_cast<size_t>(D));
+    std::vector<double> p(static_cast<size_t>(Nk)), z(static_cast<size_t>(Nk)),
+        oi(static_cast<size_t>(D)), dqi(static_cast<size_t>(D));
 #pragma omp for schedule(dynamic, 16)
-    for (int64_t r = 0; r < BH * N; ++r) {
-      const int64_t bh = r / N, i = r % N;
-      const int64_t base = bh * N * D;
-      const int64_t nk = keys_allowed(i, N, causal);
-      const double* doi = dO + base + i * D;
-      row_forward(Q + base + i * D, K + base, V + base, nk, D, scale, p.data(),
-                  oi.data(), &L[bh * N + i]);
-      const double delta = dot(doi, oi.data(), D);
-      Delta[bh * N + i] = delta;
-      double* oa = Oabs + base + i * D;
-      double* qa = dQabs + base + i * D;
-      for (int64_t d = 0; d < D; ++d) { oa[d] = 0.0; qa[d] = 0.0; }
-      for (int64_t j = 0; j < nk; ++j) {
-        const double* vj = V + base + j * D;
-        const double* kj = K + base + j * D;
-        const double ads = std::fabs(p[j] * (dot(doi, vj, D) - delta));
-        for (int64_t d = 0; d < D; ++d) {
-          oa[d] += p[j] * std::fabs(vj[d]);
-          qa[d] += ads * std::fabs(kj[d]);
-        }
-      }
-      for (int64_t d = 0; d < D; ++d) qa[d] *= scale;
+    for (int64_t r = 0; r < B * Hq * Nq; ++r) {
+      const int64_t qh = r / Nq, i = r % Nq;
+      const int64_t at = dm.qbase(qh) + i * D;
+      query_row(dm, Q, K, V, dO, causal, scale, dr, qh, i, p, z, oi.data(), &L[qh * Nq + i],
+                &Delta[qh * Nq + i], dqi.data(), Oabs + at, dQabs + at);
     }
 #pragma omp for schedule(dynamic, 16)
-    for (int64_t r = 0; r < BH * N; ++r) {
-      const int64_t bh = r / N, j = r % N;
-      const int64_t base = bh * N * D;
-      const double* kj = K + base + j * D;
-      const double* vj = V + base + j * D;
-      double* ka = dKabs + base + j * D;
-      double* va = dVabs + base + j * D;
-      for (int64_t d = 0; d < D; ++d) { ka[d] = 0.0; va[d] = 0.0; }
-      for (int64_t i = causal ? j : 0; i < N; ++i) {
-        const double* qi = Q + base + i * D;
-        const double* doi = dO + base + i * D;
-        const double pij = std::exp(scale * dot(qi, kj, D) - L[bh * N + i]);
-        const double ads = std::fabs(pij * (dot(doi, vj, D) - Delta[bh * N + i]));
-        for (int64_t d = 0; d < D; ++d) {
-          va[d] += pij * std::fabs(doi[d]);
-          ka[d] += ads * std::fabs(qi[d]);
-        }
-      }
-      for (int64_t d = 0; d < D; ++d) ka[d] *= scale;
+    for (int64_t r = 0; r < B * Hkv * Nk; ++r) {
+      const int64_t kh = r / Nk, j = r % Nk;
+      const int64_t at = kh * Nk * D + j * D;
+      std::vector<double> dk(static_cast<size_t>(D)), dv(static_cast<size_t>(D));
+      key_row(dm, Q, K, V, dO, L.data(), Delta.data(), causal, scale, dr, kh, j, dk.data(),
+              dv.data(), dKabs + at, dVabs + at);
     }
   }
 }
