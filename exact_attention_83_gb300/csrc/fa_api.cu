@@ -117,6 +117,127 @@ fa_status check_scale(float scale) {
 
 bool use_tc(fa_dtype dt) { return g_path.load() == FA_PATH_AUTO && dt != FA_F32; }
 
+// A validated fa_problem.
+struct Problem {
+  Geo g;
+  int64_t D;
+  int causal;
+  float scale;
+  fa_dtype dtype;
+  Dropout drop;
+};
+
+fa_status check_problem(const fa_problem* pr, Problem* out) {
+  if (!pr) return FA_ERR_NULL;
+  const fa_dtype dt = pr->dtype;
+  if (dt != FA_F32 && dt != FA_F16 && dt != FA_BF16) return FA_ERR_DTYPE;
+  if (pr->B < 1 || pr->Hq < 1 || pr->Hkv < 1 || pr->Nq < 1 || pr->Nk < 1) return FA_ERR_SHAPE;
+  if (pr->Hq % pr->Hkv != 0) return FA_ERR_SHAPE;
+  const int64_t D = pr->D;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return FA_ERR_HEADDIM;
+  const bool packed = pr->cu_seqlens_q != nullptr;
+  if (packed != (pr->cu_seqlens_k != nullptr)) return FA_ERR_SHAPE;
+  if (packed && (pr->total_q < 1 || pr->total_k < 1)) return FA_ERR_SHAPE;
+  if (packed && (reinterpret_cast<uintptr_t>(pr->cu_seqlens_q) % 4 != 0 ||
+                 reinterpret_cast<uintptr_t>(pr->cu_seqlens_k) % 4 != 0))
+    return FA_ERR_ALIGN;
+  Geo g{};
+  g.B = pr->B; g.Hq = pr->Hq; g.Hkv = pr->Hkv; g.G = pr->Hq / pr->Hkv;
+  g.Nq = pr->Nq; g.Nk = pr->Nk;
+  g.cu_q = pr->cu_seqlens_q; g.cu_k = pr->cu_seqlens_k;
+  g.rows_q = packed ? pr->total_q : pr->Nq;
+  g.rows_k = packed ? pr->total_k : pr->Nk;
+  g.Bt = packed ? 1 : pr->B;
+  // Every element count, and the int32 quantities the kernels use (flat head
+  // index, row positions, grid sizes), must fit.
+  int64_t t;
+  const int64_t heads[2] = {g.Hq, g.Hkv}, rows[2] = {g.rows_q, g.rows_k};
+  for (int i = 0; i < 2; ++i)
+    if (!mul_ok(g.Bt, heads[i], &t) || !mul_ok(t, rows[i], &t) || !mul_ok(t, D * 8, &t))
+      return FA_ERR_SHAPE;
+  if (!mul_ok(g.B, g.Hq, &t) || t > (int64_t)INT32_MAX) return FA_ERR_SHAPE;
+  // TMA row coordinates are int32 and run up to one tile past the last row.
+  const int64_t row_max = (int64_t)INT32_MAX - 1024;
+  if (g.rows_q > row_max || g.rows_k > row_max || g.Nq > row_max || g.Nk > row_max)
+    return FA_ERR_SHAPE;
+  FA_TRY(check_scale(pr->scale));
+  const float p = pr->dropout_p;
+  if (!(p >= 0.f && p < 1.f)) return FA_ERR_ARG;
+  Dropout d{};
+  if (p > 0.f) {
+    d.on = 1;
+    const double thr = std::floor(static_cast<double>(p) * 4294967296.0);
+    d.thr = static_cast<uint32_t>(thr < 4294967295.0 ? thr : 4294967295.0);
+    d.rscale = static_cast<float>(1.0 / (1.0 - static_cast<double>(p)));
+    d.key0 = static_cast<uint32_t>(pr->seed & 0xffffffffu);
+    d.key1 = static_cast<uint32_t>(pr->seed >> 32);
+    d.offset = pr->offset;
+  }
+  out->g = g; out->D = D; out->causal = pr->causal ? 1 : 0; out->scale = pr->scale;
+  out->dtype = dt; out->drop = d;
+  return FA_OK;
+}
+
+fa_status run_fwd(const Problem& pb, const void* q, const int64_t* sq, const void* k,
+                  const int64_t* sk, const void* v, const int64_t* sv, void* o,
+                  const int64_t* so, float* lse, cudaStream_t stream) {
+  FwdParams p{};
+  const Geo& g = pb.g;
+  FA_TRY(check_tensor(q, sq, g.Bt, g.Hq, g.rows_q, pb.dtype, p.sq));
+  FA_TRY(check_tensor(k, sk, g.Bt, g.Hkv, g.rows_k, pb.dtype, p.sk));
+  FA_TRY(check_tensor(v, sv, g.Bt, g.Hkv, g.rows_k, pb.dtype, p.sv));
+  FA_TRY(check_tensor(o, so, g.Bt, g.Hq, g.rows_q, pb.dtype, p.so));
+  FA_TRY(check_f32_vec(lse));
+  DeviceInfo* dev = nullptr;
+  FA_TRY(device_setup(&dev));
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+  p.g = g; p.D = pb.D;
+  p.causal = pb.causal; p.scale = pb.scale; p.dtype = pb.dtype; p.drop = pb.drop;
+  p.status = dev->status; p.timeout_ns = g_timeout_ns.load();
+  if (use_tc(pb.dtype) && have_fwd_tc(pb.D, pb.dtype)) {
+    p.withhold_arrival = g_withhold_next.exchange(0);
+    return launch_fwd_tc(p, stream);
+  }
+  return launch_fwd_ffma(p, stream);
+}
+
+fa_status run_bwd(const Problem& pb, const void* q, const int64_t* sq, const void* k,
+                  const int64_t* sk, const void* v, const int64_t* sv, const void* dout,
+                  const int64_t* sdo, const float* lse, const float* delta, void* dq,
+                  const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
+                  const int64_t* sdv, cudaStream_t stream) {
+  BwdParams p{};
+  const Geo& g = pb.g;
+  FA_TRY(check_tensor(q, sq, g.Bt, g.Hq, g.rows_q, pb.dtype, p.sq));
+  FA_TRY(check_tensor(k, sk, g.Bt, g.Hkv, g.rows_k, pb.dtype, p.sk));
+  FA_TRY(check_tensor(v, sv, g.Bt, g.Hkv, g.rows_k, pb.dtype, p.sv));
+  FA_TRY(check_tensor(dout, sdo, g.Bt, g.Hq, g.rows_q, pb.dtype, p.sdo));
+  FA_TRY(check_tensor(dq, sdq, g.Bt, g.Hq, g.rows_q, pb.dtype, p.sdq));
+  FA_TRY(check_tensor(dk, sdk, g.Bt, g.Hkv, g.rows_k, pb.dtype, p.sdk));
+  FA_TRY(check_tensor(dv, sdv, g.Bt, g.Hkv, g.rows_k, pb.dtype, p.sdv));
+  FA_TRY(check_f32_vec(lse));
+  FA_TRY(check_f32_vec(delta));
+  DeviceInfo* dev = nullptr;
+  FA_TRY(device_setup(&dev));
+  p.q = q; p.k = k; p.v = v; p.dout = dout; p.lse = lse; p.delta = delta;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.g = g; p.D = pb.D;
+  p.causal = pb.causal; p.scale = pb.scale; p.dtype = pb.dtype; p.drop = pb.drop;
+  p.status = dev->status; p.timeout_ns = g_timeout_ns.load();
+  p.prof = g_prof_on.load() ? g_prof_events : nullptr;
+  if (use_tc(pb.dtype) && have_bwd_tc(pb.D, pb.dtype)) return launch_bwd_tc(p, stream);
+  return launch_bwd_ffma(p, stream);
+}
+
+// fa_problem of the square, equal-heads, fixed-length, no-dropout entry points.
+fa_problem square_problem(int64_t B, int64_t H, int64_t N, int64_t D, int causal, float scale,
+                          fa_dtype dtype) {
+  fa_problem pr{};
+  pr.B = B; pr.Hq = H; pr.Hkv = H; pr.Nq = N; pr.Nk = N; pr.D = D;
+  pr.causal = causal; pr.scale = scale; pr.dtype = dtype;
+  return pr;
+}
+
 }  // namespace
 
 int device_sm_count() {
@@ -139,25 +260,19 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  const int64_t* sq, const int64_t* sk, const int64_t* sv,
                  const int64_t* so, int causal, float scale, fa_dtype dtype,
                  cudaStream_t stream) {
-  FwdParams p{};
   FA_TRY(check_shape(B, H, N, D, dtype));
-  FA_TRY(check_tensor(q, sq, B, H, N, dtype, p.sq));
-  FA_TRY(check_tensor(k, sk, B, H, N, dtype, p.sk));
-  FA_TRY(check_tensor(v, sv, B, H, N, dtype, p.sv));
-  FA_TRY(check_tensor(o, so, B, H, N, dtype, p.so));
-  FA_TRY(check_f32_vec(lse));
-  FA_TRY(check_scale(scale));
-  DeviceInfo* dev = nullptr;
-  FA_TRY(device_setup(&dev));
-  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
-  p.B = B; p.H = H; p.N = N; p.D = D;
-  p.causal = causal ? 1 : 0; p.scale = scale; p.dtype = dtype;
-  p.status = dev->status; p.timeout_ns = g_timeout_ns.load();
-  if (use_tc(dtype) && have_fwd_tc(D, dtype)) {
-    p.withhold_arrival = g_withhold_next.exchange(0);
-    return launch_fwd_tc(p, stream);
-  }
-  return launch_fwd_ffma(p, stream);
+  const fa_problem pr = square_problem(B, H, N, D, causal, scale, dtype);
+  Problem pb{};
+  FA_TRY(check_problem(&pr, &pb));
+  return run_fwd(pb, q, sq, k, sk, v, sv, o, so, lse, stream);
+}
+
+fa_status fa_fwd_ex(const fa_problem* prob, const void* q, const int64_t* sq, const void* k,
+                    const int64_t* sk, const void* v, const int64_t* sv, void* o,
+                    const int64_t* so, float* lse, cudaStream_t stream) {
+  Problem pb{};
+  FA_TRY(check_problem(prob, &pb));
+  return run_fwd(pb, q, sq, k, sk, v, sv, o, so, lse, stream);
 }
 
 fa_status fa_bwd_preprocess(const void* o, const void* dout, float* delta,
@@ -183,28 +298,23 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout,
                  const int64_t* sdo, const int64_t* sdq, const int64_t* sdk,
                  const int64_t* sdv, int causal, float scale, fa_dtype dtype,
                  cudaStream_t stream) {
-  BwdParams p{};
   FA_TRY(check_shape(B, H, N, D, dtype));
-  FA_TRY(check_tensor(q, sq, B, H, N, dtype, p.sq));
-  FA_TRY(check_tensor(k, sk, B, H, N, dtype, p.sk));
-  FA_TRY(check_tensor(v, sv, B, H, N, dtype, p.sv));
-  FA_TRY(check_tensor(dout, sdo, B, H, N, dtype, p.sdo));
-  FA_TRY(check_tensor(dq, sdq, B, H, N, dtype, p.sdq));
-  FA_TRY(check_tensor(dk, sdk, B, H, N, dtype, p.sdk));
-  FA_TRY(check_tensor(dv, sdv, B, H, N, dtype, p.sdv));
-  FA_TRY(check_f32_vec(lse));
-  FA_TRY(check_f32_vec(delta));
-  FA_TRY(check_scale(scale));
-  DeviceInfo* dev = nullptr;
-  FA_TRY(device_setup(&dev));
-  p.q = q; p.k = k; p.v = v; p.dout = dout; p.lse = lse; p.delta = delta;
-  p.dq = dq; p.dk = dk; p.dv = dv;
-  p.B = B; p.H = H; p.N = N; p.D = D;
-  p.causal = causal ? 1 : 0; p.scale = scale; p.dtype = dtype;
-  p.status = dev->status; p.timeout_ns = g_timeout_ns.load();
-  p.prof = g_prof_on.load() ? g_prof_events : nullptr;
-  if (use_tc(dtype) && have_bwd_tc(D, dtype)) return launch_bwd_tc(p, stream);
-  return launch_bwd_ffma(p, stream);
+  const fa_problem pr = square_problem(B, H, N, D, causal, scale, dtype);
+  Problem pb{};
+  FA_TRY(check_problem(&pr, &pb));
+  return run_bwd(pb, q, sq, k, sk, v, sv, dout, sdo, lse, delta, dq, sdq, dk, sdk, dv, sdv,
+                 stream);
+}
+
+fa_status fa_bwd_ex(const fa_problem* prob, const void* q, const int64_t* sq, const void* k,
+                    const int64_t* sk, const void* v, const int64_t* sv, const void* dout,
+                    const int64_t* sdo, const float* lse, const float* delta, void* dq,
+                    const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
+                    const int64_t* sdv, cudaStream_t stream) {
+  Problem pb{};
+  FA_TRY(check_problem(prob, &pb));
+  return run_bwd(pb, q, sq, k, sk, v, sv, dout, sdo, lse, delta, dq, sdq, dk, sdk, dv, sdv,
+                 stream);
 }
 
 fa_status fa_get_device_status(cudaStream_t stream) {
@@ -237,6 +347,7 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_SCALE: return "FA_ERR_SCALE: scale must be finite and > 0";
     case FA_ERR_ARG: return "FA_ERR_ARG: invalid argument";
     case FA_ERR_SCRATCH: return "FA_ERR_SCRATCH: B*H*N exceeds FA_NOALLOC_MAX_ROWS";
+    case FA_ERR_SEQLENS: return "FA_ERR_SEQLENS: packed sequence offsets are inconsistent";
   }
   return "unknown fa_status";
 }

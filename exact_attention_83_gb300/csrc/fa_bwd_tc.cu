@@ -50,12 +50,15 @@ struct BwdTcArgs {
   const float* delta;
   void* out0;              // dK/dV kernel: dV;  dQ kernel: dQ
   void* out1;              // dK/dV kernel: dK
-  int64_t H, N, BH, ntiles;
+  Geo g;
+  int64_t BH;              // dK/dV kernel: B * Hkv;  dQ kernel: B * Hq
+  int64_t ntiles;          // dK/dV kernel: key tiles;  dQ kernel: query tiles (longest sequence)
   int dreal;               // head dimension stored (<= D; narrower ones run zero-padded)
   int64_t s0[4], s1[4];    // strides of out0, out1
   int causal;
   float c;                 // scale * log2(e)
   float scale;
+  Dropout drop;
   unsigned int* status;
   uint64_t timeout_ns;
 };
@@ -115,7 +118,7 @@ struct DkdvCfg : BwdShape<D> {
   static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + D;
 };
 
-template <typename T, int D>
+template <typename T, int D, bool DROP>
 __global__ void __launch_bounds__(320, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -149,13 +152,35 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t id = blockIdx.x;
-  const int64_t bh = id % a.BH;
+  const int64_t bhk = id % a.BH;                // b * Hkv + key/value head
   const int64_t kt = id / a.BH;                 // key tile; low tiles (most work) first
-  const int32_t hh = static_cast<int32_t>(bh % a.H), bb = static_cast<int32_t>(bh / a.H);
-  const int64_t N = a.N;
-  const int nq = static_cast<int>(a.ntiles);
+  const int64_t bseq = bhk / a.g.Hkv;
+  const int32_t hk = static_cast<int32_t>(bhk % a.g.Hkv);
+  const SeqView sv = seq_view(a.g, bseq);
+  if (!sv.ok) {
+    if (threadIdx.x == 0) record_status(a.status, FA_ERR_SEQLENS);
+    return;
+  }
+  const int64_t Nq = sv.nq, Nk = sv.nk;
+  if (kt * C::BT >= Nk) return;                 // this key tile lies past the sequence
+  const int32_t bb = static_cast<int32_t>(sv.b);
+  const int nq = static_cast<int>((Nq + C::BT - 1) / C::BT);
   const int i0 = a.causal ? static_cast<int>(kt) : 0;   // first query tile
-  const int n = nq - i0;                                 // query tiles to visit (>= 1)
+  const int per = nq > i0 ? nq - i0 : 0;                 // query tiles per query head
+  const int n = per * static_cast<int>(a.g.G);           // (query head, query tile) steps
+  if (n == 0) {
+    // No query attends to these keys: dK = dV = 0.
+    if (warp < 8) {
+      const int64_t key = kt * C::BT + (warp & 3) * 32 + lane;
+      if (key < Nk) {
+        const int64_t* st = (warp >> 2) ? a.s1 : a.s0;
+        T* out = static_cast<T*>((warp >> 2) ? a.out1 : a.out0) + bb * st[0] + hk * st[1] +
+                 (sv.k0 + key) * st[2];
+        for (int d = 0; d < a.dreal; ++d) out[d] = Elem<T>::from_f32(0.f);
+      }
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
@@ -198,8 +223,10 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
       mbar_arrive_expect_tx(b_kv, 2 * C::TILE);
       for (int c = 0; c < C::DC; ++c) {
-        tma_load_4d(smem_u32(sK + c * C::CHUNK), &tmk, b_kv, c * 64, static_cast<int32_t>(kt * C::BT), hh, bb);
-        tma_load_4d(smem_u32(sV + c * C::CHUNK), &tmv, b_kv, c * 64, static_cast<int32_t>(kt * C::BT), hh, bb);
+        tma_load_4d(smem_u32(sK + c * C::CHUNK), &tmk, b_kv, c * 64,
+                    static_cast<int32_t>(sv.k0 + kt * C::BT), hk, bb);
+        tma_load_4d(smem_u32(sV + c * C::CHUNK), &tmv, b_kv, c * 64,
+                    static_cast<int32_t>(sv.k0 + kt * C::BT), hk, bb);
       }
     }
     uint32_t q_round[C::NQ], d_round[C::ND];
@@ -209,7 +236,8 @@ __global__ void __launch_bounds__(320, 1)
     for (int s = 0; s < C::ND; ++s) d_round[s] = 0;
     bool ok = true;
     for (int it = 0; it < n; ++it) {
-      const int64_t q0 = static_cast<int64_t>(i0 + it) * C::BT;
+      const int64_t q0 = static_cast<int64_t>(i0 + it % per) * C::BT;     // within the sequence
+      const int32_t hq = static_cast<int32_t>(hk * a.g.G + it / per);
       // Q_i
       const int qs = it % C::NQ;
       const uint32_t qr = static_cast<uint32_t>(it / C::NQ);
@@ -220,7 +248,7 @@ __global__ void __launch_bounds__(320, 1)
           mbar_arrive_expect_tx(b_qfull0 + 8 * qs, C::TILE);
           for (int c = 0; c < C::DC; ++c)
             tma_load_4d(smem_u32(sQ + qs * C::TILE + c * C::CHUNK), &tmq, b_qfull0 + 8 * qs, c * 64,
-                        static_cast<int32_t>(q0), hh, bb);
+                        static_cast<int32_t>(sv.q0 + q0), hq, bb);
           q_round[qs] = qr + 1;
         }
       }
@@ -237,14 +265,15 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int64_t q = q0 + lane * 4 + t;
-        L2s[lane * 4 + t] = q < N ? a.lse[bh * N + q] * kLog2e : INFINITY;
-        Ds[lane * 4 + t] = q < N ? a.delta[bh * N + q] : 0.f;
+        const int64_t li = lse_index(a.g, sv, hq, q);
+        L2s[lane * 4 + t] = q < Nq ? a.lse[li] * kLog2e : INFINITY;
+        Ds[lane * 4 + t] = q < Nq ? a.delta[li] : 0.f;
       }
       if (lane == 0) {
         mbar_arrive_expect_tx(b_dfull0 + 8 * ds, C::TILE);
         for (int c = 0; c < C::DC; ++c)
           tma_load_4d(smem_u32(slot + c * C::CHUNK), &tmdo, b_dfull0 + 8 * ds, c * 64,
-                      static_cast<int32_t>(q0), hh, bb);
+                      static_cast<int32_t>(sv.q0 + q0), hq, bb);
       } else {
         mbar_arrive(b_dfull0 + 8 * ds);
       }
@@ -357,7 +386,7 @@ __global__ void __launch_bounds__(320, 1)
     const float c = a.c;
     bool ok = true;
     for (int it = 0; it < n; ++it) {
-      const int i = i0 + it, ds = it % C::ND;
+      const int i = i0 + it % per, ds = it % C::ND;
       if (!(ok = wait_warp(b_sfull, it & 1, ctl, a.status, a.timeout_ns))) break;
       // the dO slot's arrival also publishes the staged L and Delta
       if (!(ok = wait_warp(b_dfull0 + 8 * ds, (it / C::ND) & 1, ctl, a.status, a.timeout_ns))) break;
@@ -380,7 +409,24 @@ __global__ void __launch_bounds__(320, 1)
         for (int q = 0; q < 64; ++q)
           if (64 * hf + q < row) p[q] = 0.f;
       }
-      tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, p);
+      uint64_t keep = 0;   // dropout: bit q set iff weight (query 64*hf + q, this key) is kept
+      if constexpr (DROP) {
+        const uint32_t bhq = static_cast<uint32_t>(bseq * a.g.Hq + hk * a.g.G + it / per);
+        const uint32_t jg = static_cast<uint32_t>(key >> 2), w = static_cast<uint32_t>(key & 3);
+        const int64_t qbase = static_cast<int64_t>(i) * C::BT + 64 * hf;
+        float pd[64];
+#pragma unroll
+        for (int q = 0; q < 64; ++q) {
+          const uint32_t bits = keep_bits(a.drop, jg, static_cast<uint32_t>(qbase + q), bhq);
+          const bool kq = (bits >> w) & 1u;
+          keep |= static_cast<uint64_t>(kq) << q;
+          pd[q] = kq ? p[q] * a.drop.rscale : 0.f;
+        }
+        tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, pd);
+      } else {
+        tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, p);
+      }
+      (void)keep;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(b_pready0 + 8 * hf);
@@ -389,13 +435,22 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       float dp[64];
       tmem_ld64(lane_base + C::COL_DPT + 64 * hf, dp);
+      if constexpr (DROP) {
+        // dS = P o (Z o dP - Delta), Z = keep / (1 - p)
 #pragma unroll
-      for (int q = 0; q < 64; q += 4) {
-        const float4 d4 = *reinterpret_cast<const float4*>(Ds + q);
-        dp[q] = p[q] * (dp[q] - d4.x);
-        dp[q + 1] = p[q + 1] * (dp[q + 1] - d4.y);
-        dp[q + 2] = p[q + 2] * (dp[q + 2] - d4.z);
-        dp[q + 3] = p[q + 3] * (dp[q + 3] - d4.w);
+        for (int q = 0; q < 64; ++q) {
+          const float z = ((keep >> q) & 1u) ? a.drop.rscale : 0.f;
+          dp[q] = p[q] * fmaf(z, dp[q], -Ds[q]);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 64; q += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(Ds + q);
+          dp[q] = p[q] * (dp[q] - d4.x);
+          dp[q + 1] = p[q + 1] * (dp[q + 1] - d4.y);
+          dp[q + 2] = p[q + 2] * (dp[q + 2] - d4.z);
+          dp[q + 3] = p[q + 3] * (dp[q + 3] - d4.w);
+        }
       }
       tmem_st_packed64<T>(lane_base + C::COL_DPT + 64 * hf, dp);
       tmem_wait_st();
@@ -405,12 +460,12 @@ __global__ void __launch_bounds__(320, 1)
     if (ok) ok = wait_warp(b_accdone, 0, ctl, a.status, a.timeout_ns);
     if (ok) {
       tc_fence_after();
-      const bool store = key < N;
+      const bool store = key < Nk;
       if (hf == 0) {
-        T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hh * a.s0[1] + key * a.s0[2];
+        T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hk * a.s0[1] + (sv.k0 + key) * a.s0[2];
         store_row_cols<T>(lane_base + C::COL_DV, 1.f, out, store, a.dreal);
       } else {
-        T* out = static_cast<T*>(a.out1) + bb * a.s1[0] + hh * a.s1[1] + key * a.s1[2];
+        T* out = static_cast<T*>(a.out1) + bb * a.s1[0] + hk * a.s1[1] + (sv.k0 + key) * a.s1[2];
         store_row_cols<T>(lane_base + C::COL_DK, a.scale, out, store, a.dreal);
       }
     }
@@ -461,7 +516,7 @@ __device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int row, u
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool DROP>
 __global__ void __launch_bounds__(320, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -489,12 +544,31 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t id = blockIdx.x;
-  const int64_t bh = id % a.BH;
+  const int64_t bh = id % a.BH;                 // b * Hq + h
   const int64_t qt = a.causal ? (a.ntiles - 1 - id / a.BH) : (id / a.BH);   // longest first
-  const int32_t hh = static_cast<int32_t>(bh % a.H), bb = static_cast<int32_t>(bh / a.H);
-  const int64_t N = a.N;
-  const int nk = static_cast<int>(a.ntiles);
-  const int n = a.causal ? static_cast<int>(qt) + 1 : nk;   // key tiles to visit
+  const int64_t h = bh % a.g.Hq;
+  const SeqView sv = seq_view(a.g, bh / a.g.Hq);
+  if (!sv.ok) {
+    if (threadIdx.x == 0) record_status(a.status, FA_ERR_SEQLENS);
+    return;
+  }
+  const int64_t Nq = sv.nq, Nk = sv.nk;
+  if (qt * C::BT >= Nq) return;                 // this query tile lies past the sequence
+  const int32_t hq = static_cast<int32_t>(h), hk = static_cast<int32_t>(h / a.g.G);
+  const int32_t bb = static_cast<int32_t>(sv.b);
+  const int nk = static_cast<int>((Nk + C::BT - 1) / C::BT);
+  const int n = a.causal ? min(static_cast<int>(qt) + 1, nk) : nk;   // key tiles to visit
+  if (n == 0) {
+    // No key at all (an empty key sequence): dQ = 0.
+    if (warp < 4) {
+      const int64_t qrow = qt * C::BT + warp * 32 + lane;
+      if (qrow < Nq) {
+        T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hq * a.s0[1] + (sv.q0 + qrow) * a.s0[2];
+        for (int d = 0; d < a.dreal; ++d) out[d] = Elem<T>::from_f32(0.f);
+      }
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
@@ -528,8 +602,10 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
       mbar_arrive_expect_tx(b_q, 2 * C::TILE);
       for (int c = 0; c < C::DC; ++c) {
-        tma_load_4d(smem_u32(sQ + c * C::CHUNK), &tmq, b_q, c * 64, static_cast<int32_t>(qt * C::BT), hh, bb);
-        tma_load_4d(smem_u32(sDO + c * C::CHUNK), &tmdo, b_q, c * 64, static_cast<int32_t>(qt * C::BT), hh, bb);
+        tma_load_4d(smem_u32(sQ + c * C::CHUNK), &tmq, b_q, c * 64,
+                    static_cast<int32_t>(sv.q0 + qt * C::BT), hq, bb);
+        tma_load_4d(smem_u32(sDO + c * C::CHUNK), &tmdo, b_q, c * 64,
+                    static_cast<int32_t>(sv.q0 + qt * C::BT), hq, bb);
       }
       uint32_t last_round[C::NST];
 #pragma unroll
@@ -546,9 +622,10 @@ __global__ void __launch_bounds__(320, 1)
         uint8_t* stage = sStage + st * C::STAGE;
         mbar_arrive_expect_tx(b_kvfull0 + 8 * st, 2 * C::TILE);
         for (int c = 0; c < C::DC; ++c) {
-          tma_load_4d(smem_u32(stage + c * C::CHUNK), &tmk, b_kvfull0 + 8 * st, c * 64, jt * C::BT, hh, bb);
+          const int32_t krow = static_cast<int32_t>(sv.k0 + static_cast<int64_t>(jt) * C::BT);
+          tma_load_4d(smem_u32(stage + c * C::CHUNK), &tmk, b_kvfull0 + 8 * st, c * 64, krow, hk, bb);
           tma_load_4d(smem_u32(stage + C::TILE + c * C::CHUNK), &tmv, b_kvfull0 + 8 * st, c * 64,
-                      jt * C::BT, hh, bb);
+                      krow, hk, bb);
         }
         last_round[st] = r + 1;
       }
@@ -635,8 +712,9 @@ __global__ void __launch_bounds__(320, 1)
     const int64_t qrow = qt * C::BT + row;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c = a.c;
-    const float l2 = qrow < N ? a.lse[bh * N + qrow] * kLog2e : INFINITY;
-    const float dl = qrow < N ? a.delta[bh * N + qrow] : 0.f;
+    const int64_t li = lse_index(a.g, sv, h, qrow);
+    const float l2 = qrow < Nq ? a.lse[li] * kLog2e : INFINITY;
+    const float dl = qrow < Nq ? a.delta[li] : 0.f;
     // Q (warps 0-3) and dO (warps 4-7) into TMEM as A operands.
     bool ok = wait_warp(b_q, 0, ctl, a.status, a.timeout_ns);
     if (ok) {
@@ -655,7 +733,7 @@ __global__ void __launch_bounds__(320, 1)
       // keys past N (last tile) and keys after the query (diagonal tile)
       int lim = 63;
       if (a.causal && jt == qt) lim = row - 64 * hf;
-      if (jt == nk - 1) lim = min(lim, static_cast<int>(N - 1 - static_cast<int64_t>(jt) * C::BT) - 64 * hf);
+      if (jt == nk - 1) lim = min(lim, static_cast<int>(Nk - 1 - static_cast<int64_t>(jt) * C::BT) - 64 * hf);
 #pragma unroll
       for (int q = 0; q < 64; ++q) p[q] = ex2(fmaf(p[q], c, -l2));
       if (lim < 63) {
@@ -667,8 +745,23 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       float dp[64];
       tmem_ld64(lane_base + C::COL_DP + 64 * hf, dp);
+      if constexpr (DROP) {
+        // dS = P o (Z o dP - Delta), Z = keep / (1 - p)
+        const int64_t kbase = static_cast<int64_t>(jt) * C::BT + 64 * hf;
 #pragma unroll
-      for (int q = 0; q < 64; ++q) dp[q] = p[q] * (dp[q] - dl);
+        for (int q = 0; q < 64; q += 4) {
+          const uint32_t bits = keep_bits(a.drop, static_cast<uint32_t>((kbase + q) >> 2),
+                                          static_cast<uint32_t>(qrow), static_cast<uint32_t>(bh));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float z = ((bits >> e) & 1u) ? a.drop.rscale : 0.f;
+            dp[q + e] = p[q + e] * fmaf(z, dp[q + e], -dl);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 64; ++q) dp[q] = p[q] * (dp[q] - dl);
+      }
       tmem_st_packed64<T>(lane_base + C::COL_DP + 64 * hf, dp);
       tmem_wait_st();
       tc_fence_before();
@@ -681,8 +774,8 @@ __global__ void __launch_bounds__(320, 1)
       // dimension is stored by warpgroup 0 alone
       const int half = a.dreal == D ? D / 2 : (hf == 0 ? a.dreal : 0);
       const int c0 = a.dreal == D ? (D / 2) * hf : 0;
-      T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hh * a.s0[1] + qrow * a.s0[2] + c0;
-      if (half > 0) store_row_cols<T>(lane_base + C::COL_DQ + c0, a.scale, out, qrow < N, half);
+      T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hq * a.s0[1] + (sv.q0 + qrow) * a.s0[2] + c0;
+      if (half > 0) store_row_cols<T>(lane_base + C::COL_DQ + c0, a.scale, out, qrow < Nq, half);
     }
   }
 
@@ -694,50 +787,61 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool DROP>
 fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
+  const Geo& g = p.g;
   // Tensor maps carry the true head dimension (zero fill past it).
   CUtensorMap mq, mk, mv, mdo;
-  if (!encode_tile_map(&mq, p.q, p.dtype, p.B, p.H, p.N, p.D, p.sq, 128, 64) ||
-      !encode_tile_map(&mk, p.k, p.dtype, p.B, p.H, p.N, p.D, p.sk, 128, 64) ||
-      !encode_tile_map(&mv, p.v, p.dtype, p.B, p.H, p.N, p.D, p.sv, 128, 64) ||
-      !encode_tile_map(&mdo, p.dout, p.dtype, p.B, p.H, p.N, p.D, p.sdo, 128, 64))
+  if (!encode_tile_map(&mq, p.q, p.dtype, g.Bt, g.Hq, g.rows_q, p.D, p.sq, 128, 64) ||
+      !encode_tile_map(&mk, p.k, p.dtype, g.Bt, g.Hkv, g.rows_k, p.D, p.sk, 128, 64) ||
+      !encode_tile_map(&mv, p.v, p.dtype, g.Bt, g.Hkv, g.rows_k, p.D, p.sv, 128, 64) ||
+      !encode_tile_map(&mdo, p.dout, p.dtype, g.Bt, g.Hq, g.rows_q, p.D, p.sdo, 128, 64))
     return FA_ERR_LAUNCH;
   BwdTcArgs a{};
   a.dreal = static_cast<int>(p.D);
   a.lse = p.lse; a.delta = p.delta;
-  a.H = p.H; a.N = p.N; a.BH = p.B * p.H; a.ntiles = (p.N + 127) / 128;
+  a.g = g;
   a.causal = p.causal;
   a.c = p.scale * kLog2e;
   a.scale = p.scale;
+  a.drop = p.drop;
   a.status = p.status;
   a.timeout_ns = p.timeout_ns;
-  const int64_t blocks = a.BH * a.ntiles;
-  if (blocks > 0x7fffffffLL) return FA_ERR_SHAPE;
 
-  // dK / dV
+  // dK / dV: one CTA per (b, key/value head, key tile)
+  a.BH = g.B * g.Hkv; a.ntiles = (g.Nk + 127) / 128;
+  const int64_t blocks1 = a.BH * a.ntiles;
+  if (blocks1 > 0x7fffffffLL) return FA_ERR_SHAPE;
   a.out0 = p.dv; a.out1 = p.dk;
   for (int i = 0; i < 4; ++i) { a.s0[i] = p.sdv[i]; a.s1[i] = p.sdk[i]; }
-  auto k1 = bwd_dkdv_tc_kernel<T, D>;
+  auto k1 = bwd_dkdv_tc_kernel<T, D, DROP>;
   if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM) != cudaSuccess)
     return FA_ERR_LAUNCH;
   prof_record(p, 0, stream);
-  k1<<<dim3(static_cast<unsigned>(blocks)), dim3(DkdvCfg<D>::THREADS), DkdvCfg<D>::SMEM, stream>>>(
+  k1<<<dim3(static_cast<unsigned>(blocks1)), dim3(DkdvCfg<D>::THREADS), DkdvCfg<D>::SMEM, stream>>>(
       mq, mk, mv, mdo, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   prof_record(p, 1, stream);
 
-  // dQ
+  // dQ: one CTA per (b, query head, query tile)
+  a.BH = g.B * g.Hq; a.ntiles = (g.Nq + 127) / 128;
+  const int64_t blocks2 = a.BH * a.ntiles;
+  if (blocks2 > 0x7fffffffLL) return FA_ERR_SHAPE;
   a.out0 = p.dq; a.out1 = nullptr;
   for (int i = 0; i < 4; ++i) { a.s0[i] = p.sdq[i]; a.s1[i] = 0; }
-  auto k2 = bwd_dq_tc_kernel<T, D>;
+  auto k2 = bwd_dq_tc_kernel<T, D, DROP>;
   if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM) != cudaSuccess)
     return FA_ERR_LAUNCH;
-  k2<<<dim3(static_cast<unsigned>(blocks)), dim3(DqCfg<D>::THREADS), DqCfg<D>::SMEM, stream>>>(
+  k2<<<dim3(static_cast<unsigned>(blocks2)), dim3(DqCfg<D>::THREADS), DqCfg<D>::SMEM, stream>>>(
       mq, mk, mv, mdo, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   prof_record(p, 2, stream);
   return FA_OK;
+}
+
+template <typename T, int D>
+fa_status run_bwd_tc_any(const BwdParams& p, cudaStream_t s) {
+  return p.drop.on ? run_bwd_tc<T, D, true>(p, s) : run_bwd_tc<T, D, false>(p, s);
 }
 
 }  // namespace
@@ -749,11 +853,11 @@ bool have_bwd_tc(int64_t D, fa_dtype dt) {
 
 fa_status launch_bwd_tc(const BwdParams& p, cudaStream_t s) {
   if (p.dtype == FA_BF16) {
-    if (p.D == 128) return run_bwd_tc<__nv_bfloat16, 128>(p, s);
-    if (p.D <= 64) return run_bwd_tc<__nv_bfloat16, 64>(p, s);
+    if (p.D == 128) return run_bwd_tc_any<__nv_bfloat16, 128>(p, s);
+    if (p.D <= 64) return run_bwd_tc_any<__nv_bfloat16, 64>(p, s);
   } else if (p.dtype == FA_F16) {
-    if (p.D == 128) return run_bwd_tc<__half, 128>(p, s);
-    if (p.D <= 64) return run_bwd_tc<__half, 64>(p, s);
+    if (p.D == 128) return run_bwd_tc_any<__half, 128>(p, s);
+    if (p.D <= 64) return run_bwd_tc_any<__half, 64>(p, s);
   }
   return FA_ERR_ARG;
 }

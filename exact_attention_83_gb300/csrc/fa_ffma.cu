@@ -49,10 +49,13 @@ struct FfmaArgs {
   const void* q; const void* k; const void* v; const void* dout;
   void* o; float* lse; const float* lse_in; const float* delta;
   void* dq; void* dk; void* dv;
-  int64_t H, N, BH, ntiles;
+  Geo g;
+  int64_t BH, ntiles;    // flat heads of the grid (B*Hq, or B*Hkv for dK/dV) and tiles
   int64_t sq[4], sk[4], sv[4], so[4], sdo[4], sdq[4], sdk[4], sdv[4];
   int causal;
   float scale;
+  Dropout drop;
+  unsigned int* status;
   const BwdParams* bp;   // host-side only: the call's parameters (profiling events)
 };
 
@@ -67,6 +70,14 @@ __device__ __forceinline__ void block_coords(const FfmaArgs& a, bool heavy_last_
   tile = heavy_last_tile ? (a.ntiles - 1 - t) : t;
 }
 
+// Dropout factor Z_ij of query i, key j (positions in the sequence) of flat
+// query head bhq: 1 / (1 - p) if kept, else 0.
+__device__ __forceinline__ float drop_factor(const Dropout& d, int64_t i, int64_t j, int64_t bhq) {
+  const uint32_t bits = keep_bits(d, static_cast<uint32_t>(j >> 2), static_cast<uint32_t>(i),
+                                  static_cast<uint32_t>(bhq));
+  return ((bits >> (j & 3)) & 1u) ? d.rscale : 0.f;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(NT) fwd_ffma_kernel(FfmaArgs a) {
   extern __shared__ float sm[];
@@ -78,13 +89,20 @@ __global__ void __launch_bounds__(NT) fwd_ffma_kernel(FfmaArgs a) {
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   int64_t bh, qt;
   block_coords(a, a.causal != 0, bh, qt);
-  const int64_t b = bh / a.H, h = bh % a.H, N = a.N;
-  const T* q = static_cast<const T*>(a.q) + b * a.sq[0] + h * a.sq[1];
-  const T* k = static_cast<const T*>(a.k) + b * a.sk[0] + h * a.sk[1];
-  const T* v = static_cast<const T*>(a.v) + b * a.sv[0] + h * a.sv[1];
-  T* o = static_cast<T*>(a.o) + b * a.so[0] + h * a.so[1];
+  const int64_t h = bh % a.g.Hq, hk = h / a.g.G;
+  const SeqView sv = seq_view(a.g, bh / a.g.Hq);
+  if (!sv.ok) {
+    if (threadIdx.x == 0) record_status(a.status, FA_ERR_SEQLENS);
+    return;
+  }
+  const int64_t Nq = sv.nq, Nk = sv.nk;
   const int64_t q0 = qt * BT;
-  stage_tile<T, D>(Qs, q, a.sq[2], q0, N);
+  if (q0 >= Nq) return;
+  const T* q = static_cast<const T*>(a.q) + sv.b * a.sq[0] + h * a.sq[1] + sv.q0 * a.sq[2];
+  const T* k = static_cast<const T*>(a.k) + sv.b * a.sk[0] + hk * a.sk[1] + sv.k0 * a.sk[2];
+  const T* v = static_cast<const T*>(a.v) + sv.b * a.sv[0] + hk * a.sv[1] + sv.k0 * a.sv[2];
+  T* o = static_cast<T*>(a.o) + sv.b * a.so[0] + h * a.so[1] + sv.q0 * a.so[2];
+  stage_tile<T, D>(Qs, q, a.sq[2], q0, Nq);
 
   const float c = a.scale * kLog2e;   // scores are kept in the log2 domain
   float m[4], l[4], acc[4][E];
@@ -94,11 +112,11 @@ __global__ void __launch_bounds__(NT) fwd_ffma_kernel(FfmaArgs a) {
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[i][e] = 0.f;
   }
-  const int64_t kend = a.causal ? min(N, q0 + BT) : N;
+  const int64_t kend = a.causal ? min(Nk, q0 + BT) : Nk;
   for (int64_t k0 = 0; k0 < kend; k0 += BT) {
     __syncthreads();
-    stage_tile<T, D>(Ks, k, a.sk[2], k0, N);
-    stage_tile<T, D>(Vs, v, a.sv[2], k0, N);
+    stage_tile<T, D>(Ks, k, a.sk[2], k0, Nk);
+    stage_tile<T, D>(Vs, v, a.sv[2], k0, Nk);
     __syncthreads();
     float s[4][4];
 #pragma unroll
@@ -119,14 +137,14 @@ __global__ void __launch_bounds__(NT) fwd_ffma_kernel(FfmaArgs a) {
     }
     // Ragged keys past N and (on the diagonal tile) keys after the query are
     // excluded.  Interior tiles skip the test.
-    const bool edge = (k0 + BT > N) || (a.causal && k0 + BT - 1 > q0);
+    const bool edge = (k0 + BT > Nk) || (a.causal && k0 + BT - 1 > q0);
     if (edge) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int64_t kp = k0 + tx + 16 * j, qp = q0 + ty * 4 + i;
-          if (kp >= N || (a.causal && kp > qp)) s[i][j] = -INFINITY;
+          if (kp >= Nk || (a.causal && kp > qp)) s[i][j] = -INFINITY;
         }
     }
 #pragma unroll
@@ -140,7 +158,9 @@ __global__ void __launch_bounds__(NT) fwd_ffma_kernel(FfmaArgs a) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float p = exp2f(fmaf(s[i][j], c, -m_new));
-        Ps[(ty * 4 + i) * PLD + tx + 16 * j] = p;
+        // l sums the undropped weights; P V takes the dropped, rescaled ones
+        const float z = a.drop.on ? drop_factor(a.drop, q0 + ty * 4 + i, k0 + tx + 16 * j, bh) : 1.f;
+        Ps[(ty * 4 + i) * PLD + tx + 16 * j] = p * z;
         sum += p;
       }
 #pragma unroll
@@ -167,11 +187,14 @@ __global__ void __launch_bounds__(NT) fwd_ffma_kernel(FfmaArgs a) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t row = q0 + ty * 4 + i;
-    if (row >= N) continue;
+    if (row >= Nq) continue;
+    // a row with no key at all (empty key sequence): O = 0, L = -inf
+    const bool any = l[i] > 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e)
-      o[row * a.so[2] + tx + 16 * e] = Elem<T>::from_f32(acc[i][e] / l[i]);
-    if (tx == 0) a.lse[bh * N + row] = (m[i] + log2f(l[i])) * kLn2;
+      o[row * a.so[2] + tx + 16 * e] = Elem<T>::from_f32(any ? acc[i][e] / l[i] : 0.f);
+    if (tx == 0)
+      a.lse[lse_index(a.g, sv, h, row)] = l[i] > 0.f ? (m[i] + log2f(l[i])) * kLn2 : -INFINITY;
   }
 }
 
@@ -190,18 +213,21 @@ __global__ void __launch_bounds__(NT) bwd_dkdv_ffma_kernel(FfmaArgs a) {
   float* L2s = dSs + BT * PLD;   // L * log2(e) of the staged query rows
   float* Dls = L2s + BT;         // Delta of the staged query rows
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  int64_t bh, kt;
-  block_coords(a, false, bh, kt);
-  const int64_t b = bh / a.H, h = bh % a.H, N = a.N;
-  const T* q = static_cast<const T*>(a.q) + b * a.sq[0] + h * a.sq[1];
-  const T* k = static_cast<const T*>(a.k) + b * a.sk[0] + h * a.sk[1];
-  const T* v = static_cast<const T*>(a.v) + b * a.sv[0] + h * a.sv[1];
-  const T* g = static_cast<const T*>(a.dout) + b * a.sdo[0] + h * a.sdo[1];
-  const float* L = a.lse_in + bh * N;
-  const float* Dl = a.delta + bh * N;
+  int64_t bhk, kt;
+  block_coords(a, false, bhk, kt);
+  const int64_t bseq = bhk / a.g.Hkv, hk = bhk % a.g.Hkv;
+  const SeqView sv = seq_view(a.g, bseq);
+  if (!sv.ok) {
+    if (threadIdx.x == 0) record_status(a.status, FA_ERR_SEQLENS);
+    return;
+  }
+  const int64_t Nq = sv.nq, Nk = sv.nk;
   const int64_t k0 = kt * BT;
-  stage_tile<T, D>(Ks, k, a.sk[2], k0, N);
-  stage_tile<T, D>(Vs, v, a.sv[2], k0, N);
+  if (k0 >= Nk) return;
+  const T* k = static_cast<const T*>(a.k) + sv.b * a.sk[0] + hk * a.sk[1] + sv.k0 * a.sk[2];
+  const T* v = static_cast<const T*>(a.v) + sv.b * a.sv[0] + hk * a.sv[1] + sv.k0 * a.sv[2];
+  stage_tile<T, D>(Ks, k, a.sk[2], k0, Nk);
+  stage_tile<T, D>(Vs, v, a.sv[2], k0, Nk);
   const float c = a.scale * kLog2e;
   float dk[4][E], dv[4][E];
 #pragma unroll
@@ -209,14 +235,20 @@ __global__ void __launch_bounds__(NT) bwd_dkdv_ffma_kernel(FfmaArgs a) {
 #pragma unroll
     for (int e = 0; e < E; ++e) { dk[i][e] = 0.f; dv[i][e] = 0.f; }
 
-  for (int64_t q0 = a.causal ? k0 : 0; q0 < N; q0 += BT) {
+  // every query head that reads this key/value head, then its query tiles
+  for (int64_t hg = 0; hg < a.g.G; ++hg)
+  for (int64_t q0 = a.causal ? k0 : 0; q0 < Nq; q0 += BT) {
+    const int64_t h = hk * a.g.G + hg, bhq = bseq * a.g.Hq + h;
+    const T* q = static_cast<const T*>(a.q) + sv.b * a.sq[0] + h * a.sq[1] + sv.q0 * a.sq[2];
+    const T* g = static_cast<const T*>(a.dout) + sv.b * a.sdo[0] + h * a.sdo[1] + sv.q0 * a.sdo[2];
     __syncthreads();
-    stage_tile<T, D>(Qs, q, a.sq[2], q0, N);
-    stage_tile<T, D>(dOs, g, a.sdo[2], q0, N);
+    stage_tile<T, D>(Qs, q, a.sq[2], q0, Nq);
+    stage_tile<T, D>(dOs, g, a.sdo[2], q0, Nq);
     if (threadIdx.x < BT) {
       const int64_t row = q0 + threadIdx.x;
-      L2s[threadIdx.x] = row < N ? L[row] * kLog2e : 0.f;
-      Dls[threadIdx.x] = row < N ? Dl[row] : 0.f;
+      const int64_t li = lse_index(a.g, sv, h, row);
+      L2s[threadIdx.x] = row < Nq ? a.lse_in[li] * kLog2e : 0.f;
+      Dls[threadIdx.x] = row < Nq ? a.delta[li] : 0.f;
     }
     __syncthreads();
     // Transposed score and dP tiles: element (key 4*ty+i, query tx+16*j).
@@ -246,10 +278,12 @@ __global__ void __launch_bounds__(NT) bwd_dkdv_ffma_kernel(FfmaArgs a) {
       for (int j = 0; j < 4; ++j) {
         const int ql = tx + 16 * j;
         const int64_t qp = q0 + ql, kp = k0 + ty * 4 + i;
-        const bool keep = qp < N && (!a.causal || kp <= qp);
+        const bool keep = qp < Nq && (!a.causal || kp <= qp);
         const float p = keep ? exp2f(fmaf(s[i][j], c, -L2s[ql])) : 0.f;
-        Ps[(ty * 4 + i) * PLD + ql] = p;
-        dSs[(ty * 4 + i) * PLD + ql] = p * (dp[i][j] - Dls[ql]);
+        // dropout: dV takes P o Z, dS = P o (Z o dP - Delta)
+        const float z = a.drop.on ? drop_factor(a.drop, qp, kp, bhq) : 1.f;
+        Ps[(ty * 4 + i) * PLD + ql] = p * z;
+        dSs[(ty * 4 + i) * PLD + ql] = p * fmaf(z, dp[i][j], -Dls[ql]);
       }
     __syncthreads();
 #pragma unroll 2
@@ -268,12 +302,12 @@ __global__ void __launch_bounds__(NT) bwd_dkdv_ffma_kernel(FfmaArgs a) {
         }
     }
   }
-  T* dkp = static_cast<T*>(a.dk) + b * a.sdk[0] + h * a.sdk[1];
-  T* dvp = static_cast<T*>(a.dv) + b * a.sdv[0] + h * a.sdv[1];
+  T* dkp = static_cast<T*>(a.dk) + sv.b * a.sdk[0] + hk * a.sdk[1] + sv.k0 * a.sdk[2];
+  T* dvp = static_cast<T*>(a.dv) + sv.b * a.sdv[0] + hk * a.sdv[1] + sv.k0 * a.sdv[2];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t row = k0 + ty * 4 + i;
-    if (row >= N) continue;
+    if (row >= Nk) continue;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       dkp[row * a.sdk[2] + tx + 16 * e] = Elem<T>::from_f32(dk[i][e] * a.scale);
@@ -295,29 +329,37 @@ __global__ void __launch_bounds__(NT) bwd_dq_ffma_kernel(FfmaArgs a) {
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   int64_t bh, qt;
   block_coords(a, a.causal != 0, bh, qt);
-  const int64_t b = bh / a.H, h = bh % a.H, N = a.N;
-  const T* q = static_cast<const T*>(a.q) + b * a.sq[0] + h * a.sq[1];
-  const T* k = static_cast<const T*>(a.k) + b * a.sk[0] + h * a.sk[1];
-  const T* v = static_cast<const T*>(a.v) + b * a.sv[0] + h * a.sv[1];
-  const T* g = static_cast<const T*>(a.dout) + b * a.sdo[0] + h * a.sdo[1];
+  const int64_t h = bh % a.g.Hq, hk = h / a.g.G;
+  const SeqView sv = seq_view(a.g, bh / a.g.Hq);
+  if (!sv.ok) {
+    if (threadIdx.x == 0) record_status(a.status, FA_ERR_SEQLENS);
+    return;
+  }
+  const int64_t Nq = sv.nq, Nk = sv.nk;
   const int64_t q0 = qt * BT;
-  stage_tile<T, D>(Qs, q, a.sq[2], q0, N);
-  stage_tile<T, D>(dOs, g, a.sdo[2], q0, N);
+  if (q0 >= Nq) return;
+  const T* q = static_cast<const T*>(a.q) + sv.b * a.sq[0] + h * a.sq[1] + sv.q0 * a.sq[2];
+  const T* k = static_cast<const T*>(a.k) + sv.b * a.sk[0] + hk * a.sk[1] + sv.k0 * a.sk[2];
+  const T* v = static_cast<const T*>(a.v) + sv.b * a.sv[0] + hk * a.sv[1] + sv.k0 * a.sv[2];
+  const T* g = static_cast<const T*>(a.dout) + sv.b * a.sdo[0] + h * a.sdo[1] + sv.q0 * a.sdo[2];
+  stage_tile<T, D>(Qs, q, a.sq[2], q0, Nq);
+  stage_tile<T, D>(dOs, g, a.sdo[2], q0, Nq);
   const float c = a.scale * kLog2e;
   float L2[4], Dl[4], dq[4][E];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t row = q0 + ty * 4 + i;
-    L2[i] = row < N ? a.lse_in[bh * N + row] * kLog2e : 0.f;
-    Dl[i] = row < N ? a.delta[bh * N + row] : 0.f;
+    const int64_t li = lse_index(a.g, sv, h, row);
+    L2[i] = row < Nq ? a.lse_in[li] * kLog2e : 0.f;
+    Dl[i] = row < Nq ? a.delta[li] : 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) dq[i][e] = 0.f;
   }
-  const int64_t kend = a.causal ? min(N, q0 + BT) : N;
+  const int64_t kend = a.causal ? min(Nk, q0 + BT) : Nk;
   for (int64_t k0 = 0; k0 < kend; k0 += BT) {
     __syncthreads();
-    stage_tile<T, D>(Ks, k, a.sk[2], k0, N);
-    stage_tile<T, D>(Vs, v, a.sv[2], k0, N);
+    stage_tile<T, D>(Ks, k, a.sk[2], k0, Nk);
+    stage_tile<T, D>(Vs, v, a.sv[2], k0, Nk);
     __syncthreads();
     float s[4][4], dp[4][4];
 #pragma unroll
@@ -344,9 +386,10 @@ __global__ void __launch_bounds__(NT) bwd_dq_ffma_kernel(FfmaArgs a) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int64_t kp = k0 + tx + 16 * j, qp = q0 + ty * 4 + i;
-        const bool keep = kp < N && (!a.causal || kp <= qp);
+        const bool keep = kp < Nk && (!a.causal || kp <= qp);
         const float p = keep ? exp2f(fmaf(s[i][j], c, -L2[i])) : 0.f;
-        dSs[(ty * 4 + i) * PLD + tx + 16 * j] = p * (dp[i][j] - Dl[i]);
+        const float z = a.drop.on ? drop_factor(a.drop, qp, kp, bh) : 1.f;
+        dSs[(ty * 4 + i) * PLD + tx + 16 * j] = p * fmaf(z, dp[i][j], -Dl[i]);
       }
     __syncthreads();
 #pragma unroll 4
@@ -362,11 +405,11 @@ __global__ void __launch_bounds__(NT) bwd_dq_ffma_kernel(FfmaArgs a) {
         for (int e = 0; e < E; ++e) dq[i][e] = fmaf(ds[i], kv[e], dq[i][e]);
     }
   }
-  T* dqp = static_cast<T*>(a.dq) + b * a.sdq[0] + h * a.sdq[1];
+  T* dqp = static_cast<T*>(a.dq) + sv.b * a.sdq[0] + h * a.sdq[1] + sv.q0 * a.sdq[2];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t row = q0 + ty * 4 + i;
-    if (row >= N) continue;
+    if (row >= Nq) continue;
 #pragma unroll
     for (int e = 0; e < E; ++e)
       dqp[row * a.sdq[2] + tx + 16 * e] = Elem<T>::from_f32(dq[i][e] * a.scale);
@@ -391,11 +434,14 @@ fa_status run_fwd(const FfmaArgs& a, cudaStream_t s) {
   return launch(fwd_ffma_kernel<T, D>, fwd_smem(D), a.BH * a.ntiles, a, s);
 }
 template <typename T, int D>
-fa_status run_bwd(const FfmaArgs& a, cudaStream_t s) {
+fa_status run_bwd(const FfmaArgs& a0, cudaStream_t s) {
+  FfmaArgs a = a0;
   prof_record(*a.bp, 0, s);
+  a.BH = a.g.B * a.g.Hkv; a.ntiles = (a.g.Nk + BT - 1) / BT;
   fa_status st = launch(bwd_dkdv_ffma_kernel<T, D>, dkdv_smem(D), a.BH * a.ntiles, a, s);
   if (st != FA_OK) return st;
   prof_record(*a.bp, 1, s);
+  a.BH = a.g.B * a.g.Hq; a.ntiles = (a.g.Nq + BT - 1) / BT;
   st = launch(bwd_dq_ffma_kernel<T, D>, dq_smem(D), a.BH * a.ntiles, a, s);
   prof_record(*a.bp, 2, s);
   return st;
@@ -427,9 +473,9 @@ void copy4(int64_t* dst, const int64_t* src) { for (int i = 0; i < 4; ++i) dst[i
 fa_status launch_fwd_ffma(const FwdParams& p, cudaStream_t s) {
   FfmaArgs a{};
   a.q = p.q; a.k = p.k; a.v = p.v; a.o = p.o; a.lse = p.lse;
-  a.H = p.H; a.N = p.N; a.BH = p.B * p.H; a.ntiles = (p.N + BT - 1) / BT;
+  a.g = p.g; a.BH = p.g.B * p.g.Hq; a.ntiles = (p.g.Nq + BT - 1) / BT;
   copy4(a.sq, p.sq); copy4(a.sk, p.sk); copy4(a.sv, p.sv); copy4(a.so, p.so);
-  a.causal = p.causal; a.scale = p.scale;
+  a.causal = p.causal; a.scale = p.scale; a.drop = p.drop; a.status = p.status;
   FA_DISPATCH(run_fwd, p.dtype, p.D, a, s);
 }
 
@@ -437,10 +483,10 @@ fa_status launch_bwd_ffma(const BwdParams& p, cudaStream_t s) {
   FfmaArgs a{};
   a.q = p.q; a.k = p.k; a.v = p.v; a.dout = p.dout; a.lse_in = p.lse; a.delta = p.delta;
   a.dq = p.dq; a.dk = p.dk; a.dv = p.dv;
-  a.H = p.H; a.N = p.N; a.BH = p.B * p.H; a.ntiles = (p.N + BT - 1) / BT;
+  a.g = p.g;
   copy4(a.sq, p.sq); copy4(a.sk, p.sk); copy4(a.sv, p.sv); copy4(a.sdo, p.sdo);
   copy4(a.sdq, p.sdq); copy4(a.sdk, p.sdk); copy4(a.sdv, p.sdv);
-  a.causal = p.causal; a.scale = p.scale;
+  a.causal = p.causal; a.scale = p.scale; a.drop = p.drop; a.status = p.status;
   a.bp = &p;
   FA_DISPATCH(run_bwd, p.dtype, p.D, a, s);
 }

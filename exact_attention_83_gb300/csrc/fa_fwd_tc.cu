@@ -61,17 +61,19 @@ struct FwdCfg {
 struct FwdTcArgs {
   void* o;
   float* lse;
-  int64_t H, N, BH, npairs;
+  Geo g;
+  int64_t BH, npairs;      // B * Hq; query-tile pairs of the longest sequence
   int dreal;               // head dimension stored (<= D; narrower ones run zero-padded)
   int64_t so[4];
   int causal;
   float c;                 // scale * log2(e)
+  Dropout drop;
   unsigned int* status;
   uint64_t timeout_ns;
   int withhold_arrival;    // test-only: CTA 0 skips the first S-ready arrival of tile 0
 };
 
-template <typename T, int D>
+template <typename T, int D, bool DROP>
 __global__ void __launch_bounds__(320, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const FwdTcArgs a) {
@@ -94,19 +96,39 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t id = blockIdx.x;
-  const int64_t bh = id % a.BH;
+  const int64_t bh = id % a.BH;                 // b * Hq + h
   const int64_t pr = a.causal ? (a.npairs - 1 - id / a.BH) : (id / a.BH);
-  const int32_t hh = static_cast<int32_t>(bh % a.H), bb = static_cast<int32_t>(bh / a.H);
-  const int64_t N = a.N;
-  const int nk = static_cast<int>((N + C::BN - 1) / C::BN);
+  const int64_t h = bh % a.g.Hq;
+  const SeqView sv = seq_view(a.g, bh / a.g.Hq);
+  if (!sv.ok) {
+    if (threadIdx.x == 0) record_status(a.status, FA_ERR_SEQLENS);
+    return;
+  }
+  const int64_t Nq = sv.nq, Nk = sv.nk;
+  if (2 * pr * C::BM >= Nq) return;             // both query tiles lie past this sequence
+  const int32_t hq = static_cast<int32_t>(h), hk = static_cast<int32_t>(h / a.g.G);
+  const int32_t bb = static_cast<int32_t>(sv.b);
+  const int nk = static_cast<int>((Nk + C::BN - 1) / C::BN);
   int ntile[2];
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
     const int64_t qt = 2 * pr + g;
     const int64_t diag = qt + 1;   // key tiles up to and including the diagonal
-    ntile[g] = (qt * C::BM >= N) ? 0 : (a.causal ? static_cast<int>(diag < nk ? diag : nk) : nk);
+    ntile[g] = (qt * C::BM >= Nq) ? 0 : (a.causal ? static_cast<int>(diag < nk ? diag : nk) : nk);
   }
   const int nmax = max(ntile[0], ntile[1]);
+  if (nmax == 0) {
+    // No key at all (an empty key sequence): O = 0 and L = -inf.
+    if (warp < 8) {
+      const int64_t qrow = (2 * pr + (warp >> 2)) * C::BM + (warp & 3) * 32 + lane;
+      if (qrow < Nq) {
+        T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qrow) * a.so[2];
+        for (int d = 0; d < a.dreal; ++d) orow[d] = Elem<T>::from_f32(0.f);
+        a.lse[lse_index(a.g, sv, h, qrow)] = -INFINITY;
+      }
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
@@ -147,7 +169,7 @@ __global__ void __launch_bounds__(320, 1)
         if (ntile[g] == 0) continue;
         for (int c = 0; c < C::DC; ++c)
           tma_load_4d(smem_u32(sQ + g * C::TILE + c * C::CHUNK), &tmq, b_q, c * 64,
-                      static_cast<int32_t>((2 * pr + g) * C::BM), hh, bb);
+                      static_cast<int32_t>(sv.q0 + (2 * pr + g) * C::BM), hq, bb);
       }
       bool ok = true;
       for (int j = 0; ok && j < nmax; ++j) {
@@ -160,7 +182,7 @@ __global__ void __launch_bounds__(320, 1)
           mbar_arrive_expect_tx(b_full0 + 8 * s, C::TILE);
           for (int c = 0; c < C::DC; ++c)
             tma_load_4d(smem_u32(sRing + s * C::TILE + c * C::CHUNK), kv ? &tmv : &tmk,
-                        b_full0 + 8 * s, c * 64, j * C::BN, hh, bb);
+                        b_full0 + 8 * s, c * 64, static_cast<int32_t>(sv.k0 + j * C::BN), hk, bb);
           issued[s] = r + 1;
         }
       }
@@ -254,8 +276,12 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tO = lane_base + C::COL_O0 + D * g;
     const float c = a.c;
     float m = -INFINITY, l = 0.f;
+    uint32_t keepq = 0;            // dropout: keep bits of the current group of four keys
+    (void)keepq;
     bool ok = true;
     const int n = ntile[g];
+    // last valid key column of the last key tile
+    const int lim_last = static_cast<int>(Nk - 1 - static_cast<int64_t>(nk - 1) * C::BN);
     for (int j = 0; j < n; ++j) {
       if (!(ok = wait_warp(b_sfull0 + 8 * g, j & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
@@ -280,7 +306,7 @@ __global__ void __launch_bounds__(320, 1)
       // diagonal tile, the only one a causal row can straddle).
       int lim = C::BN - 1;
       if (a.causal && j == qt) lim = r;
-      if (j == nk - 1) lim = min(lim, static_cast<int>(N - 1 - static_cast<int64_t>(j) * C::BN));
+      if (j == nk - 1) lim = min(lim, lim_last);
       if (lim < C::BN - 1) {
 #pragma unroll
         for (int kk = 0; kk < C::BN; ++kk)
@@ -320,7 +346,19 @@ __global__ void __launch_bounds__(320, 1)
           const float p1 = ex2(fmaf(s[64 * half + 2 * i + 1], c, negm));
           sum0 += p0;
           sum1 += p1;
-          pk[i] = pack2<T>(p0, p1);
+          if constexpr (DROP) {
+            // l sums the undropped weights; P V takes the dropped, rescaled ones
+            uint32_t bits = 0;
+            const int key = j * C::BN + 64 * half + 2 * i;
+            if ((i & 1) == 0)
+              keepq = keep_bits(a.drop, static_cast<uint32_t>(key >> 2), static_cast<uint32_t>(qrow),
+                                static_cast<uint32_t>(bh));
+            bits = keepq >> (2 * (i & 1));
+            pk[i] = pack2<T>((bits & 1u) ? p0 * a.drop.rscale : 0.f,
+                             (bits & 2u) ? p1 * a.drop.rscale : 0.f);
+          } else {
+            pk[i] = pack2<T>(p0, p1);
+          }
         }
         tmem_st32(tS + 32 * half, pk);
       }
@@ -347,10 +385,10 @@ __global__ void __launch_bounds__(320, 1)
     if (ok && n > 0) {
       tc_fence_after();
       const float inv = 1.f / l;
-      const bool store = qrow < N;
-      T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hh * a.so[1] + qrow * a.so[2];
+      const bool store = qrow < Nq;
+      T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qrow) * a.so[2];
       store_row_cols<T>(tO, inv, orow, store, a.dreal);
-      if (store) a.lse[bh * N + qrow] = (m + log2f(l)) * kLn2;
+      if (store) a.lse[lse_index(a.g, sv, h, qrow)] = (m + log2f(l)) * kLn2;
     }
   }
 
@@ -365,26 +403,29 @@ __global__ void __launch_bounds__(320, 1)
 template <typename T, int D>
 fa_status run_fwd_tc(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
+  const Geo& g = p.g;
   // Tensor maps carry the true head dimension; a narrower one than D reads
   // as zeros past its end (TMA fill), which leaves every product exact.
   CUtensorMap mq, mk, mv;
-  if (!encode_tile_map(&mq, p.q, p.dtype, p.B, p.H, p.N, p.D, p.sq, 128, 64) ||
-      !encode_tile_map(&mk, p.k, p.dtype, p.B, p.H, p.N, p.D, p.sk, 128, 64) ||
-      !encode_tile_map(&mv, p.v, p.dtype, p.B, p.H, p.N, p.D, p.sv, 128, 64))
+  if (!encode_tile_map(&mq, p.q, p.dtype, g.Bt, g.Hq, g.rows_q, p.D, p.sq, 128, 64) ||
+      !encode_tile_map(&mk, p.k, p.dtype, g.Bt, g.Hkv, g.rows_k, p.D, p.sk, 128, 64) ||
+      !encode_tile_map(&mv, p.v, p.dtype, g.Bt, g.Hkv, g.rows_k, p.D, p.sv, 128, 64))
     return FA_ERR_LAUNCH;
   FwdTcArgs a{};
   a.dreal = static_cast<int>(p.D);
   a.o = p.o; a.lse = p.lse;
-  a.H = p.H; a.N = p.N; a.BH = p.B * p.H; a.npairs = (p.N + 255) / 256;
+  a.g = g;
+  a.BH = g.B * g.Hq; a.npairs = (g.Nq + 255) / 256;
   for (int i = 0; i < 4; ++i) a.so[i] = p.so[i];
   a.causal = p.causal;
   a.c = p.scale * kLog2e;
+  a.drop = p.drop;
   a.status = p.status;
   a.timeout_ns = p.timeout_ns;
   a.withhold_arrival = p.withhold_arrival;
   const int64_t blocks = a.BH * a.npairs;
   if (blocks > 0x7fffffffLL) return FA_ERR_SHAPE;
-  auto kern = fwd_tc_kernel<T, D>;
+  auto kern = p.drop.on ? fwd_tc_kernel<T, D, true> : fwd_tc_kernel<T, D, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
       cudaSuccess)
     return FA_ERR_LAUNCH;

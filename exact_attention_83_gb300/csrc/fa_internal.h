@@ -11,16 +11,45 @@
 
 namespace fa {
 
-// Parameters of one forward call, validated by the ABI layer.
+// Problem geometry, validated by the ABI layer.
+//  Fixed lengths: B sequences of Nq query and Nk key rows; a tensor row is
+//  addressed as (b, h, n).  Packed variable lengths: cu_q / cu_k hold B+1
+//  offsets into rows_q / rows_k packed rows, the tensors have one batch entry
+//  (b-stride unused), and sequence b's row n is packed row cu[b] + n.
+//  Query head h reads key/value head h / G.
+struct Geo {
+  int64_t B, Hq, Hkv, G;     // G = Hq / Hkv
+  int64_t Nq, Nk;            // rows per sequence (upper bounds when packed)
+  const int32_t* cu_q;       // device, B+1 entries, or null (fixed lengths)
+  const int32_t* cu_k;
+  int64_t rows_q, rows_k;    // tensor rows per (b, h): Nq, Nk, or the packed totals
+  int64_t Bt;                // batch extent of the tensors: B, or 1 when packed
+};
+
+// Dropout of the attention weights: weight (i, j) of query head h in sequence
+// b is kept iff word (j mod 4) of Philox4x32-10 (Salmon, Moraes, Dror and
+// Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011) at counter
+// (j / 4, i, b * Hq + h, offset) under key (key0, key1) is >= thr; kept
+// weights are multiplied by rscale = 1 / (1 - p).
+struct Dropout {
+  int on;
+  uint32_t thr;
+  float rscale;
+  uint32_t key0, key1, offset;
+};
+
+// Parameters of one forward call.
 struct FwdParams {
   const void* q; const void* k; const void* v;
   void* o; float* lse;
-  int64_t B, H, N, D;
+  Geo g;
+  int64_t D;
   int64_t sq[4], sk[4], sv[4], so[4];   // element strides (b, h, n, d), d == 1
   int causal;
   float scale;
   fa_dtype dtype;
-  unsigned int* status;   // device status word (FA_ERR_TIMEOUT on a wait that ran out)
+  Dropout drop;
+  unsigned int* status;   // device status word (first error a kernel records)
   uint64_t timeout_ns;    // bound on any single device-side wait
   int withhold_arrival;   // test-only: CTA 0 skips one mbarrier arrival (see fa.h)
 };
@@ -36,15 +65,74 @@ struct BwdParams {
   const void* q; const void* k; const void* v; const void* dout;
   const float* lse; const float* delta;
   void* dq; void* dk; void* dv;
-  int64_t B, H, N, D;
+  Geo g;
+  int64_t D;
   int64_t sq[4], sk[4], sv[4], sdo[4], sdq[4], sdk[4], sdv[4];
   int causal;
   float scale;
   fa_dtype dtype;
+  Dropout drop;
   unsigned int* status;
   uint64_t timeout_ns;
   const cudaEvent_t* prof;   // 3 events to record around the two kernels, or null
 };
+
+#ifdef __CUDACC__
+// One sequence as a kernel sees it: batch coordinate of the tensors, first
+// query / key row, lengths.  ok is false when packed offsets are inconsistent
+// (decreasing, past the packed rows, or longer than Nq / Nk); the caller then
+// records FA_ERR_SEQLENS and touches nothing of that sequence.
+struct SeqView {
+  int64_t b, q0, k0, nq, nk;
+  bool ok;
+};
+
+__device__ __forceinline__ SeqView seq_view(const Geo& g, int64_t b) {
+  SeqView v;
+  if (g.cu_q == nullptr) {
+    v.b = b; v.q0 = 0; v.k0 = 0; v.nq = g.Nq; v.nk = g.Nk; v.ok = true;
+    return v;
+  }
+  const int64_t q0 = __ldg(g.cu_q + b), q1 = __ldg(g.cu_q + b + 1);
+  const int64_t k0 = __ldg(g.cu_k + b), k1 = __ldg(g.cu_k + b + 1);
+  v.b = 0; v.q0 = q0; v.k0 = k0; v.nq = q1 - q0; v.nk = k1 - k0;
+  v.ok = q0 >= 0 && q1 >= q0 && q1 <= g.rows_q && v.nq <= g.Nq &&
+         k0 >= 0 && k1 >= k0 && k1 <= g.rows_k && v.nk <= g.Nk;
+  return v;
+}
+
+// Index of (b, h, row) in the fp32 lse / delta arrays: [Bt, Hq, rows_q].
+__device__ __forceinline__ int64_t lse_index(const Geo& g, const SeqView& v, int64_t h,
+                                             int64_t row) {
+  return (v.b * g.Hq + h) * g.rows_q + v.q0 + row;
+}
+
+__device__ __forceinline__ void record_status(unsigned int* status, unsigned int code) {
+  atomicCAS(status, 0u, code);
+}
+
+// Philox4x32-10: ten rounds of the published round function, the key bumped
+// by the two Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// The four keep decisions for keys 4*jg .. 4*jg+3 of query row i in flat
+// head bh (= b * Hq + h), as bits 0..3.
+__device__ __forceinline__ uint32_t keep_bits(const Dropout& d, uint32_t jg, uint32_t i,
+                                              uint32_t bh) {
+  const uint4 r = philox4x32_10(make_uint4(jg, i, bh, d.offset), d.key0, d.key1);
+  return (r.x >= d.thr ? 1u : 0u) | (r.y >= d.thr ? 2u : 0u) | (r.z >= d.thr ? 4u : 0u) |
+         (r.w >= d.thr ? 8u : 0u);
+}
+#endif
 
 // Records prof[i] on s when profiling events are set.
 inline void prof_record(const BwdParams& p, int i, cudaStream_t s) {

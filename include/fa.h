@@ -32,7 +32,9 @@
  * Alignment.  Every tensor base must be 16-byte aligned and every b/h/n stride
  * times the element size must be a multiple of 16 bytes (tiles move by TMA).
  *
- * Shapes.  B, H, N >= 1; D in {16, 32, 64, 128}; Q, K and V share N.
+ * Shapes.  B, H, N >= 1; D in {16, 32, 64, 128}; Q, K and V share N
+ * (fa_fwd_ex / fa_bwd_ex below lift this: Nq != Nk, grouped key/value heads,
+ * packed variable lengths, dropout).
  * scale must be finite and > 0 (use 1/sqrt(D) for standard attention).
  *
  * Ownership.  The caller allocates every buffer.  The library allocates no
@@ -82,7 +84,8 @@ typedef enum {
   FA_ERR_ARCH = 9,     /* the current device is not sm_103                      */
   FA_ERR_SCALE = 10,   /* scale is not finite and > 0                          */
   FA_ERR_ARG = 11,     /* another invalid argument (e.g. an unknown option)    */
-  FA_ERR_SCRATCH = 12  /* fa_bwd_noalloc: B*H*N exceeds FA_NOALLOC_MAX_ROWS    */
+  FA_ERR_SCRATCH = 12, /* fa_bwd_noalloc: B*H*N exceeds FA_NOALLOC_MAX_ROWS    */
+  FA_ERR_SEQLENS = 13  /* device-reported: packed offsets inconsistent (below) */
 } fa_status;
 
 /*
@@ -156,11 +159,99 @@ FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, con
                                 float scale, fa_dtype dtype, cudaStream_t stream);
 
 /*
+ * General problem for fa_fwd_ex / fa_bwd_ex: query and key lengths that
+ * differ, fewer key/value heads than query heads, packed variable-length
+ * sequences, and dropout of the attention weights.  fa_fwd / fa_bwd are the
+ * case Hq = Hkv, Nq = Nk, fixed lengths, no dropout.
+ *
+ *   B          number of sequences, >= 1
+ *   Hq, Hkv    query heads and key/value heads, >= 1, Hq % Hkv == 0.  Query
+ *              head h reads key/value head h / (Hq / Hkv): consecutive query
+ *              heads share one (grouped-query attention; Hkv = 1 is
+ *              multi-query attention).  dK, dV sum over the sharing heads.
+ *   Nq, Nk     fixed lengths: the query / key rows of every sequence (>= 1).
+ *              Packed: upper bounds on any sequence's rows (>= 1; the grid is
+ *              sized by them).
+ *   D          head dimension, 16, 32, 64 or 128
+ *   cu_seqlens_q, cu_seqlens_k
+ *              both NULL: fixed lengths.  Q, O, dO, dQ are [B, Hq, Nq, D];
+ *              K, V, dK, dV are [B, Hkv, Nk, D]; lse and delta are fp32
+ *              [B, Hq, Nq].
+ *              Both set: DEVICE arrays of B+1 int32 offsets into packed rows,
+ *              non-decreasing, from >= 0 up to <= total_q / total_k.
+ *              Sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+ *              of packed tensors [total_q, Hq, D] (pass their strides as a
+ *              [1, Hq, total_q, D] view: the b-stride is ignored) and key rows
+ *              cu_seqlens_k[b] .. likewise of [total_k, Hkv, D]; lse and delta
+ *              are fp32 [Hq, total_q].  A sequence may be empty.  A sequence
+ *              whose offsets break these rules (or is longer than Nq / Nk) is
+ *              skipped and the kernels record FA_ERR_SEQLENS, which
+ *              fa_get_device_status reports; no memory outside the tensors is
+ *              touched.
+ *   total_q, total_k  packed rows (>= 1); ignored for fixed lengths
+ *   causal     key j is kept for query i iff j <= i, both counted from the
+ *              sequence's first row (top-left aligned, as for fa_fwd)
+ *   scale, dtype  as for fa_fwd
+ *   dropout_p  0 <= p < 1.  With p > 0 each attention weight P_ij of query
+ *              head h in sequence b is kept iff word (j mod 4) of
+ *              Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
+ *              Numbers: As Easy as 1, 2, 3", SC 2011) with counter
+ *              (j / 4, i, b*Hq + h, offset) and key (seed mod 2^32,
+ *              seed / 2^32) is >= floor(p * 2^32); i, j are positions within
+ *              the sequence.  Kept weights are scaled by 1 / (1 - p):
+ *              O = (P o Z) V with Z_ij = keep_ij / (1 - p).  L stays the
+ *              log-sum-exp of the undropped scores.  fa_bwd_ex with the same
+ *              seed and offset rebuilds the same mask:
+ *              dV = (P o Z)^T dO, dS = P o (Z o (dO V^T) - Delta).
+ *
+ * Rows with no key at all (an empty key sequence) get O = 0 and L = -inf;
+ * keys that no query attends to get dK = dV = 0.
+ */
+typedef struct fa_problem {
+  int64_t B, Hq, Hkv, Nq, Nk, D;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  int64_t total_q, total_k;
+  int causal;
+  float scale;
+  fa_dtype dtype;
+  float dropout_p;
+  uint64_t seed;
+  uint32_t offset;
+} fa_problem;
+
+/*
+ * Forward for a general problem.  Tensors as described for fa_problem, with
+ * 4 element strides each in the order (b, h, n, d) as for fa_fwd.  Validation
+ * and error codes as for fa_fwd, plus FA_ERR_SHAPE for Hq % Hkv != 0 or
+ * cu_seqlens pointers of which only one is set, and FA_ERR_ARG for dropout_p
+ * outside [0, 1).
+ */
+FA_API fa_status fa_fwd_ex(const fa_problem* prob, const void* q, const int64_t* sq,
+                           const void* k, const int64_t* sk, const void* v,
+                           const int64_t* sv, void* o, const int64_t* so, float* lse,
+                           cudaStream_t stream);
+
+/*
+ * Backward for a general problem: dQ, dK, dV from Q, K, V, dO, the forward's
+ * lse and delta = rowsum(dO o O) (fa_bwd_preprocess over the Q-shaped rows:
+ * B, Hq, Nq for fixed lengths; 1, Hq, total_q for packed ones).  Same problem
+ * description (seed and offset included) as the forward call.
+ */
+FA_API fa_status fa_bwd_ex(const fa_problem* prob, const void* q, const int64_t* sq,
+                           const void* k, const int64_t* sk, const void* v,
+                           const int64_t* sv, const void* dout, const int64_t* sdo,
+                           const float* lse, const float* delta, void* dq,
+                           const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
+                           const int64_t* sdv, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device.  Returns FA_OK, FA_ERR_TIMEOUT if a kernel's bounded wait on
  * an mbarrier ran out since the last call (that kernel's outputs are then
- * undefined; the CUDA context stays usable), or FA_ERR_LAUNCH if the stream
- * reported a CUDA error.
+ * undefined; the CUDA context stays usable), FA_ERR_SEQLENS if a kernel met
+ * inconsistent packed offsets, or FA_ERR_LAUNCH if the stream reported a CUDA
+ * error.  The first error recorded since the last call wins.
  */
 FA_API fa_status fa_get_device_status(cudaStream_t stream);
 
