@@ -34,8 +34,9 @@ sys.path.insert(0, ROOT)
 import torch  # noqa: E402
 
 from exact_attention_83_gb300 import shard  # noqa: E402
-from exact_attention_83_gb300.inputs import (LONG_CAUSAL, Workload, bf16_n1024,  # noqa: E402
-                                             make_inputs, sweep)
+from exact_attention_83_gb300.inputs import (LONG_CAUSAL, GeneralWorkload, Workload,  # noqa: E402
+                                             bf16_n1024, make_general_inputs, make_inputs,
+                                             seqlen_mix, sweep)
 
 METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 peak"
 
@@ -56,8 +57,27 @@ MEASURED_TRAFFIC = {
 PROFILE_CASE = Workload("long-bf16-B1-H16-N16384-D128-causal", 1, 16, 16384, 128, "bf16", True)
 
 
+# General problems at the size of the long causal shape (32 query heads of
+# 16384 rows, D = 128, bf16): grouped and multi-query heads, packed sequences,
+# dropout, and cross-attention-like lengths.
+_MIX = seqlen_mix(65536, 512, 8192, seed=1)
+GENERAL = [
+    GeneralWorkload("gqa-bf16-B1-Hq32-Hkv8-N16384-D128-causal", 1, 32, 8, 16384, 16384, 128,
+                    "bf16", True),
+    GeneralWorkload("mqa-bf16-B1-Hq32-Hkv1-N16384-D128-causal", 1, 32, 1, 16384, 16384, 128,
+                    "bf16", True),
+    GeneralWorkload("dropout0.1-bf16-B1-H32-N16384-D128-causal", 1, 32, 32, 16384, 16384, 128,
+                    "bf16", True, dropout_p=0.1),
+    GeneralWorkload("varlen-bf16-64k-tokens-len512-8192-Hq32-Hkv8-D128-causal", len(_MIX), 32, 8,
+                    max(_MIX), max(_MIX), 128, "bf16", True, seqlens_q=_MIX, seqlens_k=_MIX),
+    GeneralWorkload("cross-bf16-B4-H32-Nq4096-Nk16384-D128-full", 4, 32, 32, 4096, 16384, 128,
+                    "bf16", False),
+]
+
+
 def workloads():
     ws = {LONG_CAUSAL.name: LONG_CAUSAL, PROFILE_CASE.name: PROFILE_CASE}
+    ws.update({g.name: g for g in GENERAL})
     for c in (False, True):
         w = bf16_n1024(c)
         ws[w.name] = w
@@ -207,6 +227,15 @@ def main():
     w = workloads()[args.workload]
     world, rank, local = dist_env()
 
+    if isinstance(w, GeneralWorkload):
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable":
+                                  "the reference arm is timed on the long causal workload"}))
+            return
+        run_general(args, w, world, rank, local)
+        return
+
     if args.impl == "reference":
         if rank == 0:
             run_reference(args, w)
@@ -337,6 +366,101 @@ def main():
             "gpu_launches": 4 * args.steps,
             "e2e": e2e,
             "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
+    """fa_fwd_ex + fa_bwd_preprocess + fa_bwd_ex on a general problem; the same
+    JSON line as the main workload (no e2e or CPU-baseline leg).  FLOPs count
+    the attended (query, key) pairs exactly (causal: sum_i min(i + 1, Nk))."""
+    from exact_attention_83_gb300 import fa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    fa.load_library()
+    q, k, v, do, cu_q, cu_k = make_general_inputs(w, dev)
+    kw = dict(dropout_p=w.dropout_p, seed=w.drop_seed, offset=w.drop_offset)
+    if w.packed:
+        kw.update(cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=w.Nq, max_seqlen_k=w.Nk)
+    o = torch.empty_like(q)
+    lse_shape = (w.Hq, q.shape[0]) if w.packed else (w.B, w.Hq, w.Nq)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    delta = torch.empty_like(lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    o4, do4 = fa._as4(o, w.packed), fa._as4(do, w.packed)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        fa.fwd_ex(q, k, v, o, lse, w.causal, w.scale, **kw)
+        fa.bwd_preprocess(o4, do4, delta)
+        fa.bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale, **kw)
+    barrier()
+    if fa.device_status() != 0:
+        raise RuntimeError("device status not OK after warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for e in ev:
+        for x in e:
+            x.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            e = ev[i]
+            e[0].record(stream)
+            fa.fwd_ex(q, k, v, o, lse, w.causal, w.scale, **kw)
+            e[1].record(stream)
+            fa.bwd_preprocess(o4, do4, delta)
+            fa.set_profile_events(e[2:5])
+            fa.bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale, **kw)
+        end.record(stream)
+        barrier()
+    fa.set_profile_events(None)
+    if fa.device_status() != 0:
+        raise RuntimeError("device status not OK after the timed region")
+    ms_step = shard.max_over_ranks(start.elapsed_time(end), dev) / args.steps
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    pre_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    dq_ms = statistics.median(e[3].elapsed_time(e[4]) for e in ev)
+    value = world * w.fwd_bwd_flops() / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+    peak = pk["bf16_tflops"]
+    dkdv_flops = 4 * 2.0 * w.D * w.Hq * w.pairs()
+    achieved = dkdv_flops / (dkdv_ms * 1e-3) / 1e12
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq,
+                       "Nk": w.Nk, "D": w.D, "causal": w.causal, "packed": w.packed,
+                       "dropout_p": w.dropout_p, "parallelism": f"replicas{world}",
+                       "flops": "4*D*Hq*(attended pairs), backward credited 2.5x"},
+            "fwd_tflops": w.fwd_flops() / (fwd_ms * 1e-3) / 1e12, "fwd_ms": fwd_ms,
+            "fwd_frac_of_peak": w.fwd_flops() / (fwd_ms * 1e-3) / 1e12 / peak,
+            "fwd_bwd_frac_of_peak": value / world / peak,
+            "peak_tflops": peak, "peak_source": pk["source"] + " burst bf16 (cuBLAS)",
+            "kernel_ms": {"fwd": fwd_ms, "preprocess": pre_ms, "bwd_dkdv": dkdv_ms,
+                          "bwd_dq": dq_ms},
+            "roofline": {"kernel": "bwd_dkdv", "bound": "tensor", "achieved": achieved,
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": None},
+            "clocks": clocks.summary(),
+            "gpu_launches": 4 * args.steps,
+            "e2e": None,
+            "cpu_baseline": None,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
