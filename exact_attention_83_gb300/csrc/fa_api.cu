@@ -166,8 +166,8 @@ fa_status check_problem(const fa_problem* pr, Problem* out) {
   Dropout d{};
   if (p > 0.f) {
     d.on = 1;
-    const double thr = std::floor(static_cast<double>(p) * 4294967296.0);
-    d.thr = static_cast<uint32_t>(thr < 4294967295.0 ? thr : 4294967295.0);
+    const double thr = std::floor(static_cast<double>(p) * 65536.0);
+    d.thr = static_cast<uint32_t>(thr < 65535.0 ? thr : 65535.0);
     d.rscale = static_cast<float>(1.0 / (1.0 - static_cast<double>(p)));
     d.key0 = static_cast<uint32_t>(pr->seed & 0xffffffffu);
     d.key1 = static_cast<uint32_t>(pr->seed >> 32);

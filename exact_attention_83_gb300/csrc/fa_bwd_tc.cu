@@ -411,17 +411,29 @@ __global__ void __launch_bounds__(320, 1)
       }
       uint64_t keep = 0;   // dropout: bit q set iff weight (query 64*hf + q, this key) is kept
       if constexpr (DROP) {
+        // The eight lanes of an octet hold eight consecutive keys, which one
+        // generator call covers for one query.  Lane e of the octet draws for
+        // query 8t + e, the octet exchanges the eight 8-bit results, and each
+        // lane keeps the bit of its own key for the eight queries.
         const uint32_t bhq = static_cast<uint32_t>(bseq * a.g.Hq + hk * a.g.G + it / per);
-        const uint32_t jg = static_cast<uint32_t>(key >> 2), w = static_cast<uint32_t>(key & 3);
+        const uint32_t jg = static_cast<uint32_t>(key >> 3);
+        const int e = lane & 7;
         const int64_t qbase = static_cast<int64_t>(i) * C::BT + 64 * hf;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          uint64_t x = static_cast<uint64_t>(
+                           keep8(a.drop, jg, static_cast<uint32_t>(qbase + 8 * t + e), bhq))
+                       << (8 * e);
+          x |= __shfl_xor_sync(0xffffffffu, x, 1);
+          x |= __shfl_xor_sync(0xffffffffu, x, 2);
+          x |= __shfl_xor_sync(0xffffffffu, x, 4);
+          // bit 8 * e' + e of x is (query 8t + e', this key); gather them
+          const uint64_t y = (x >> e) & 0x0101010101010101ull;
+          keep |= ((y * 0x0102040810204080ull) >> 56) << (8 * t);
+        }
         float pd[64];
 #pragma unroll
-        for (int q = 0; q < 64; ++q) {
-          const uint32_t bits = keep_bits(a.drop, jg, static_cast<uint32_t>(qbase + q), bhq);
-          const bool kq = (bits >> w) & 1u;
-          keep |= static_cast<uint64_t>(kq) << q;
-          pd[q] = kq ? p[q] * a.drop.rscale : 0.f;
-        }
+        for (int q = 0; q < 64; ++q) pd[q] = ((keep >> q) & 1u) ? p[q] * a.drop.rscale : 0.f;
         tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, pd);
       } else {
         tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, p);
@@ -749,11 +761,11 @@ __global__ void __launch_bounds__(320, 1)
         // dS = P o (Z o dP - Delta), Z = keep / (1 - p)
         const int64_t kbase = static_cast<int64_t>(jt) * C::BT + 64 * hf;
 #pragma unroll
-        for (int q = 0; q < 64; q += 4) {
-          const uint32_t bits = keep_bits(a.drop, static_cast<uint32_t>((kbase + q) >> 2),
-                                          static_cast<uint32_t>(qrow), static_cast<uint32_t>(bh));
+        for (int q = 0; q < 64; q += 8) {
+          const uint32_t bits = keep8(a.drop, static_cast<uint32_t>((kbase + q) >> 3),
+                                      static_cast<uint32_t>(qrow), static_cast<uint32_t>(bh));
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
+          for (int e = 0; e < 8; ++e) {
             const float z = ((bits >> e) & 1u) ? a.drop.rscale : 0.f;
             dp[q + e] = p[q + e] * fmaf(z, dp[q + e], -dl);
           }

@@ -73,9 +73,9 @@ __device__ __forceinline__ void block_coords(const FfmaArgs& a, bool heavy_last_
 // Dropout factor Z_ij of query i, key j (positions in the sequence) of flat
 // query head bhq: 1 / (1 - p) if kept, else 0.
 __device__ __forceinline__ float drop_factor(const Dropout& d, int64_t i, int64_t j, int64_t bhq) {
-  const uint32_t bits = keep_bits(d, static_cast<uint32_t>(j >> 2), static_cast<uint32_t>(i),
-                                  static_cast<uint32_t>(bhq));
-  return ((bits >> (j & 3)) & 1u) ? d.rscale : 0.f;
+  const uint32_t bits = keep8(d, static_cast<uint32_t>(j >> 3), static_cast<uint32_t>(i),
+                              static_cast<uint32_t>(bhq));
+  return ((bits >> (j & 7)) & 1u) ? d.rscale : 0.f;
 }
 
 template <typename T, int D>

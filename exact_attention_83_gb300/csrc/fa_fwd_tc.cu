@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tO = lane_base + C::COL_O0 + D * g;
     const float c = a.c;
     float m = -INFINITY, l = 0.f;
-    uint32_t keepq = 0;            // dropout: keep bits of the current group of four keys
+    uint32_t keepq = 0;            // dropout: keep bits of the current group of eight keys
     (void)keepq;
     bool ok = true;
     const int n = ntile[g];
@@ -348,12 +348,11 @@ __global__ void __launch_bounds__(320, 1)
           sum1 += p1;
           if constexpr (DROP) {
             // l sums the undropped weights; P V takes the dropped, rescaled ones
-            uint32_t bits = 0;
             const int key = j * C::BN + 64 * half + 2 * i;
-            if ((i & 1) == 0)
-              keepq = keep_bits(a.drop, static_cast<uint32_t>(key >> 2), static_cast<uint32_t>(qrow),
-                                static_cast<uint32_t>(bh));
-            bits = keepq >> (2 * (i & 1));
+            if ((i & 3) == 0)
+              keepq = keep8(a.drop, static_cast<uint32_t>(key >> 3), static_cast<uint32_t>(qrow),
+                            static_cast<uint32_t>(bh));
+            const uint32_t bits = keepq >> (2 * (i & 3));
             pk[i] = pack2<T>((bits & 1u) ? p0 * a.drop.rscale : 0.f,
                              (bits & 2u) ? p1 * a.drop.rscale : 0.f);
           } else {

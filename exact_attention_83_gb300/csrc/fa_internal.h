@@ -27,10 +27,11 @@ struct Geo {
 };
 
 // Dropout of the attention weights: weight (i, j) of query head h in sequence
-// b is kept iff word (j mod 4) of Philox4x32-10 (Salmon, Moraes, Dror and
-// Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011) at counter
-// (j / 4, i, b * Hq + h, offset) under key (key0, key1) is >= thr; kept
-// weights are multiplied by rscale = 1 / (1 - p).
+// b is kept iff 16-bit half (j mod 2) of word ((j mod 8) / 2) of Philox4x32-10
+// (Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2,
+// 3", SC 2011) at counter (j / 8, i, b * Hq + h, offset) under key
+// (key0, key1) is >= thr = floor(p * 65536); kept weights are multiplied by
+// rscale = 1 / (1 - p).  One generator call serves eight consecutive keys.
 struct Dropout {
   int on;
   uint32_t thr;
@@ -111,26 +112,36 @@ __device__ __forceinline__ void record_status(unsigned int* status, unsigned int
   atomicCAS(status, 0u, code);
 }
 
-// Philox4x32-10: ten rounds of the published round function, the key bumped
-// by the two Weyl constants between rounds.
+// Philox4x32-10: ten rounds of the published round function (each multiplies
+// counter words 0 and 2 by the round multipliers and mixes the halves of the
+// 64-bit products with words 1 and 3 and the key), the key bumped by the two
+// Weyl constants between rounds.
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    uint64_t p0, p1;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(0xD2511F53u));
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(0xCD9E8D57u));
+    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
   }
   return c;
 }
 
-// The four keep decisions for keys 4*jg .. 4*jg+3 of query row i in flat
-// head bh (= b * Hq + h), as bits 0..3.
-__device__ __forceinline__ uint32_t keep_bits(const Dropout& d, uint32_t jg, uint32_t i,
-                                              uint32_t bh) {
+// The eight keep decisions for keys 8*jg .. 8*jg+7 of query row i in flat
+// head bh (= b * Hq + h), as bits 0..7.
+__device__ __forceinline__ uint32_t keep8(const Dropout& d, uint32_t jg, uint32_t i,
+                                          uint32_t bh) {
   const uint4 r = philox4x32_10(make_uint4(jg, i, bh, d.offset), d.key0, d.key1);
-  return (r.x >= d.thr ? 1u : 0u) | (r.y >= d.thr ? 2u : 0u) | (r.z >= d.thr ? 4u : 0u) |
-         (r.w >= d.thr ? 8u : 0u);
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+  uint32_t bits = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    bits |= ((w[e] & 0xFFFFu) >= d.thr ? 1u : 0u) << (2 * e);
+    bits |= ((w[e] >> 16) >= d.thr ? 1u : 0u) << (2 * e + 1);
+  }
+  return bits;
 }
 #endif
 

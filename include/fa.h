@@ -193,12 +193,12 @@ FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, con
  *              sequence's first row (top-left aligned, as for fa_fwd)
  *   scale, dtype  as for fa_fwd
  *   dropout_p  0 <= p < 1.  With p > 0 each attention weight P_ij of query
- *              head h in sequence b is kept iff word (j mod 4) of
- *              Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
- *              Numbers: As Easy as 1, 2, 3", SC 2011) with counter
- *              (j / 4, i, b*Hq + h, offset) and key (seed mod 2^32,
- *              seed / 2^32) is >= floor(p * 2^32); i, j are positions within
- *              the sequence.  Kept weights are scaled by 1 / (1 - p):
+ *              head h in sequence b is kept iff the 16-bit half (j mod 2;
+ *              0 = low) of word ((j mod 8) / 2) of Philox4x32-10 (Salmon,
+ *              Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2,
+ *              3", SC 2011) with counter (j / 8, i, b*Hq + h, offset) and key
+ *              (seed mod 2^32, seed / 2^32) is >= floor(p * 65536); i, j are
+ *              positions within the sequence.  Kept weights are scaled by 1 / (1 - p):
  *              O = (P o Z) V with Z_ij = keep_ij / (1 - p).  L stays the
  *              log-sum-exp of the undropped scores.  fa_bwd_ex with the same
  *              seed and offset rebuilds the same mask:

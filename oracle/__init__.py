@@ -56,15 +56,15 @@ class Dropout(ctypes.Structure):
 
 def dropout_params(p: float = 0.0, seed: int = 0, offset: int = 0, bh0: int = 0):
     """The dropout description for probability p (taken as a float32 value, as
-    the library takes it): keep iff the Philox word is >= floor(p * 2^32);
-    kept weights scaled by 1 / (1 - p)."""
+    the library takes it): keep iff the 16-bit Philox half is >=
+    floor(p * 65536); kept weights scaled by 1 / (1 - p)."""
     p32 = float(np.float32(p))
     if not 0.0 <= p32 < 1.0:
         raise ValueError("dropout probability must be in [0, 1)")
     d = Dropout()
     if p32 > 0.0:
         d.on = 1
-        d.thr = min(int(np.floor(p32 * 4294967296.0)), 4294967295)
+        d.thr = min(int(np.floor(p32 * 65536.0)), 65535)
         d.rscale = 1.0 / (1.0 - p32)
         d.key0 = int(seed) & 0xFFFFFFFF
         d.key1 = (int(seed) >> 32) & 0xFFFFFFFF

@@ -40,8 +40,9 @@
 //    before the product with V (O = (P o Z) V); L stays the log-sum-exp of the
 //    undropped scores; then dV = (P o Z)^T dO and dS = P o (Z o dP - Delta),
 //    Delta = rowsum(dO o O) as before.  keep_ij is drawn from Philox4x32-10
-//    (Salmon et al., SC 2011) at counter (j / 4, i, flat head, offset); word
-//    j mod 4 is compared with floor(p * 2^32).
+//    (Salmon et al., SC 2011) at counter (j / 8, i, flat head, offset): the
+//    16-bit half j mod 2 of word (j mod 8) / 2 is compared with
+//    floor(p * 65536).
 //
 // Readings where the pages are open (each is also listed in the design notes):
 //  * masked keys are excluded exactly (weight 0, never a finite sentinel);
@@ -117,11 +118,12 @@ void philox(const uint32_t ctr[4], uint32_t k0, uint32_t k1, uint32_t out[4]) {
 extern "C" {
 
 // Dropout of the attention weights (none when on == 0): weight (i, j) of flat
-// query head bh0 + (b * Hq + h) is kept iff word (j mod 4) of Philox4x32-10 at
-// counter (j / 4, i, bh0 + b * Hq + h, offset) under key (key0, key1) is
-// >= thr; a kept weight is multiplied by rscale = 1 / (1 - p).  i and j are
-// positions within the sequence; bh0 lets a packed batch pass one sequence at
-// a time with its own head numbering.
+// query head bh0 + (b * Hq + h) is kept iff the 16-bit half (j mod 2, 0 = low)
+// of word ((j mod 8) / 2) of Philox4x32-10 at counter
+// (j / 8, i, bh0 + b * Hq + h, offset) under key (key0, key1) is >= thr
+// (= floor(p * 65536)); a kept weight is multiplied by rscale = 1 / (1 - p).
+// i and j are positions within the sequence; bh0 lets a packed batch pass one
+// sequence at a time with its own head numbering.
 typedef struct {
   int on;
   uint32_t thr;
@@ -137,11 +139,13 @@ namespace {
 // Z_ij of one weight, 1 without dropout.
 inline double zfac(const oracle_dropout* dr, int64_t i, int64_t j, int64_t bh) {
   if (dr == nullptr || !dr->on) return 1.0;
-  const uint32_t ctr[4] = {static_cast<uint32_t>(j >> 2), static_cast<uint32_t>(i),
+  const uint32_t ctr[4] = {static_cast<uint32_t>(j / 8), static_cast<uint32_t>(i),
                            static_cast<uint32_t>(dr->bh0 + bh), dr->offset};
   uint32_t w[4];
   philox(ctr, dr->key0, dr->key1, w);
-  return w[j & 3] >= dr->thr ? dr->rscale : 0.0;
+  const uint32_t word = w[(j % 8) / 2];
+  const uint32_t half = (j % 2 == 0) ? (word & 0xFFFFu) : (word >> 16);
+  return half >= dr->thr ? dr->rscale : 0.0;
 }
 
 // Forward for one query row (the plain definition).

@@ -103,16 +103,18 @@ def test_dropout_zero_is_no_dropout():
 
 def _mask(p, seed, offset, bh, Nq, Nk):
     """Z built here from the generator (pinned above) and the stated counter
-    layout: word j%4 of philox((j/4, i, bh, offset), (seed lo, seed hi))."""
-    thr = min(int(np.floor(float(np.float32(p)) * 2.0 ** 32)), 2 ** 32 - 1)
+    layout: 16-bit half j%2 of word (j%8)/2 of philox((j/8, i, bh, offset),
+    (seed lo, seed hi)) against floor(p * 65536)."""
+    thr = min(int(np.floor(float(np.float32(p)) * 65536.0)), 65535)
     z = np.zeros((Nq, Nk))
     for i in range(Nq):
-        for jg in range((Nk + 3) // 4):
+        for jg in range((Nk + 7) // 8):
             w = oracle.philox4x32_10([jg, i, bh, offset], [seed & 0xFFFFFFFF, seed >> 32])
-            for e in range(4):
-                j = 4 * jg + e
+            halves = [h for word in w for h in (word & 0xFFFF, word >> 16)]
+            for e in range(8):
+                j = 8 * jg + e
                 if j < Nk:
-                    z[i, j] = 1.0 / (1.0 - float(np.float32(p))) if w[e] >= thr else 0.0
+                    z[i, j] = 1.0 / (1.0 - float(np.float32(p))) if halves[e] >= thr else 0.0
     return z
 
 
