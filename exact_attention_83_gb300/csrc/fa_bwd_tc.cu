@@ -409,12 +409,14 @@ __global__ void __launch_bounds__(320, 1)
         for (int q = 0; q < 64; ++q)
           if (64 * hf + q < row) p[q] = 0.f;
       }
-      uint64_t keep = 0;   // dropout: bit q set iff weight (query 64*hf + q, this key) is kept
+      // Dropout keep bits: bit q set iff weight (query 64*hf + q of this
+      // tile, this key) is kept.
+      // The eight lanes of an octet hold eight consecutive keys, which one
+      // generator call covers for one query.  Lane e of the octet draws for
+      // query 8t + e, the octet exchanges the eight 8-bit results, and each
+      // lane keeps the bit of its own key for the eight queries.
+      uint64_t keep = 0;
       if constexpr (DROP) {
-        // The eight lanes of an octet hold eight consecutive keys, which one
-        // generator call covers for one query.  Lane e of the octet draws for
-        // query 8t + e, the octet exchanges the eight 8-bit results, and each
-        // lane keeps the bit of its own key for the eight queries.
         const uint32_t bhq = static_cast<uint32_t>(bseq * a.g.Hq + hk * a.g.G + it / per);
         const uint32_t jg = static_cast<uint32_t>(key >> 3);
         const int e = lane & 7;
@@ -431,6 +433,8 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t y = (x >> e) & 0x0101010101010101ull;
           keep |= ((y * 0x0102040810204080ull) >> 56) << (8 * t);
         }
+      }
+      if constexpr (DROP) {
         float pd[64];
 #pragma unroll
         for (int q = 0; q < 64; ++q) pd[q] = ((keep >> q) & 1u) ? p[q] * a.drop.rscale : 0.f;
@@ -736,6 +740,18 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_before();
     mbar_arrive(b_qt);
     for (int jt = 0; ok && jt < n; ++jt) {
+      // Dropout keep bits of this row's 64 keys (positions only), drawn before
+      // the scores arrive: bit q set iff key 64*hf + q of this tile is kept.
+      uint64_t keep = 0;
+      if constexpr (DROP) {
+        const int64_t kbase = static_cast<int64_t>(jt) * C::BT + 64 * hf;
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          keep |= static_cast<uint64_t>(keep8(a.drop, static_cast<uint32_t>((kbase >> 3) + t),
+                                              static_cast<uint32_t>(qrow),
+                                              static_cast<uint32_t>(bh)))
+                  << (8 * t);
+      }
       if (!(ok = wait_warp(b_sfull, jt & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
       float p[64];
@@ -759,16 +775,10 @@ __global__ void __launch_bounds__(320, 1)
       tmem_ld64(lane_base + C::COL_DP + 64 * hf, dp);
       if constexpr (DROP) {
         // dS = P o (Z o dP - Delta), Z = keep / (1 - p)
-        const int64_t kbase = static_cast<int64_t>(jt) * C::BT + 64 * hf;
 #pragma unroll
-        for (int q = 0; q < 64; q += 8) {
-          const uint32_t bits = keep8(a.drop, static_cast<uint32_t>((kbase + q) >> 3),
-                                      static_cast<uint32_t>(qrow), static_cast<uint32_t>(bh));
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float z = ((bits >> e) & 1u) ? a.drop.rscale : 0.f;
-            dp[q + e] = p[q + e] * fmaf(z, dp[q + e], -dl);
-          }
+        for (int q = 0; q < 64; ++q) {
+          const float z = ((keep >> q) & 1u) ? a.drop.rscale : 0.f;
+          dp[q] = p[q] * fmaf(z, dp[q], -dl);
         }
       } else {
 #pragma unroll

@@ -347,7 +347,8 @@ __global__ void __launch_bounds__(320, 1)
           sum0 += p0;
           sum1 += p1;
           if constexpr (DROP) {
-            // l sums the undropped weights; P V takes the dropped, rescaled ones
+            // l sums the undropped weights; P V takes the dropped, rescaled
+            // ones; one generator call covers eight keys
             const int key = j * C::BN + 64 * half + 2 * i;
             if ((i & 3) == 0)
               keepq = keep8(a.drop, static_cast<uint32_t>(key >> 3), static_cast<uint32_t>(qrow),
