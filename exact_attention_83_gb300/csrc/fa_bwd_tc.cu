@@ -59,6 +59,7 @@ struct BwdTcArgs {
   float c;                 // scale * log2(e)
   float scale;
   Dropout drop;
+  int split;               // dK/dV kernel: CTAs (one cluster) sharing a key tile's query heads
   unsigned int* status;
   uint64_t timeout_ns;
 };
@@ -100,6 +101,16 @@ __device__ __forceinline__ void tmem_st_packed64(uint32_t taddr, const float (&x
 // only after dK_i (two dO slots).  S^T_{i+1} overwrites P^T_i and dP^T_{i+1}
 // overwrites dS^T_i; each is read only by products issued before it.  The next
 // tile's scores are therefore ready while the elementwise warps finish dS_i.
+// Staging of a CTA's partial dV (t = 0) and dK (t = 1) for the cluster
+// reduction of the dK/dV kernel: [2][128 rows][D] fp32 over the operand
+// buffers (idle by then), 16-byte chunk c of row r stored at chunk
+// c ^ (r mod 8) so a warp's 32 rows spread over the banks.
+template <int D>
+__device__ __forceinline__ float* stage_row(uint8_t* smem, int t, int row) {
+  return reinterpret_cast<float*>(smem) + (t * 128 + row) * D;
+}
+__device__ __forceinline__ int stage_chunk(int c, int row) { return c ^ (row & 7); }
+
 template <int D>
 struct DkdvCfg : BwdShape<D> {
   using S = BwdShape<D>;
@@ -125,6 +136,7 @@ __global__ void __launch_bounds__(320, 1)
                        const BwdTcArgs a) {
   using C = DkdvCfg<D>;
   static_assert(C::SMEM <= 232448, "shared memory per block");
+  static_assert(2 * 128 * D * 4 <= C::OFF_BAR, "cluster staging fits below the barriers");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad > static_cast<uint32_t>(C::MAX_PAD)) {   // never expected: report, do nothing
@@ -151,7 +163,12 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t b_mmadone = smem_u32(&bars[18]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t id = blockIdx.x;
+  // With split S > 1, the S CTAs of a cluster share one key tile: CTA `rank`
+  // takes query heads rank*G/S .. (rank+1)*G/S - 1 of the group, and rank 0
+  // sums the partial dK, dV through distributed shared memory at the end.
+  const int split = a.split;
+  const int rank = static_cast<int>(blockIdx.x % split);
+  const int64_t id = blockIdx.x / split;
   const int64_t bhk = id % a.BH;                // b * Hkv + key/value head
   const int64_t kt = id / a.BH;                 // key tile; low tiles (most work) first
   const int64_t bseq = bhk / a.g.Hkv;
@@ -167,10 +184,13 @@ __global__ void __launch_bounds__(320, 1)
   const int nq = static_cast<int>((Nq + C::BT - 1) / C::BT);
   const int i0 = a.causal ? static_cast<int>(kt) : 0;   // first query tile
   const int per = nq > i0 ? nq - i0 : 0;                 // query tiles per query head
-  const int n = per * static_cast<int>(a.g.G);           // (query head, query tile) steps
+  const int gper = static_cast<int>(a.g.G) / split;      // query heads of this CTA
+  const int g0 = rank * gper;                            // its first head within the group
+  const int n = per * gper;                              // (query head, query tile) steps
   if (n == 0) {
-    // No query attends to these keys: dK = dV = 0.
-    if (warp < 8) {
+    // No query attends to these keys: dK = dV = 0 (every CTA of a cluster
+    // takes this branch together).
+    if (warp < 8 && rank == 0) {
       const int64_t key = kt * C::BT + (warp & 3) * 32 + lane;
       if (key < Nk) {
         const int64_t* st = (warp >> 2) ? a.s1 : a.s0;
@@ -211,6 +231,7 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  bool ew_ok = false;   // elementwise warps: main loop completed
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -237,7 +258,7 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     for (int it = 0; it < n; ++it) {
       const int64_t q0 = static_cast<int64_t>(i0 + it % per) * C::BT;     // within the sequence
-      const int32_t hq = static_cast<int32_t>(hk * a.g.G + it / per);
+      const int32_t hq = static_cast<int32_t>(hk * a.g.G + g0 + it / per);
       // Q_i
       const int qs = it % C::NQ;
       const uint32_t qr = static_cast<uint32_t>(it / C::NQ);
@@ -417,7 +438,7 @@ __global__ void __launch_bounds__(320, 1)
       // lane keeps the bit of its own key for the eight queries.
       uint64_t keep = 0;
       if constexpr (DROP) {
-        const uint32_t bhq = static_cast<uint32_t>(bseq * a.g.Hq + hk * a.g.G + it / per);
+        const uint32_t bhq = static_cast<uint32_t>(bseq * a.g.Hq + hk * a.g.G + g0 + it / per);
         const uint32_t jg = static_cast<uint32_t>(key >> 3);
         const int e = lane & 7;
         const int64_t qbase = static_cast<int64_t>(i) * C::BT + 64 * hf;
@@ -474,17 +495,84 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(b_dsready0 + 8 * hf);
     }
     if (ok) ok = wait_warp(b_accdone, 0, ctl, a.status, a.timeout_ns);
+    ew_ok = ok;
     if (ok) {
       tc_fence_after();
       const bool store = key < Nk;
-      if (hf == 0) {
-        T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hk * a.s0[1] + (sv.k0 + key) * a.s0[2];
-        store_row_cols<T>(lane_base + C::COL_DV, 1.f, out, store, a.dreal);
-      } else {
-        T* out = static_cast<T*>(a.out1) + bb * a.s1[0] + hk * a.s1[1] + (sv.k0 + key) * a.s1[2];
-        store_row_cols<T>(lane_base + C::COL_DK, a.scale, out, store, a.dreal);
+      const uint32_t acc = lane_base + (hf == 0 ? C::COL_DV : C::COL_DK);
+      if (split == 1) {
+        if (hf == 0) {
+          T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hk * a.s0[1] + (sv.k0 + key) * a.s0[2];
+          store_row_cols<T>(acc, 1.f, out, store, a.dreal);
+        } else {
+          T* out = static_cast<T*>(a.out1) + bb * a.s1[0] + hk * a.s1[1] + (sv.k0 + key) * a.s1[2];
+          store_row_cols<T>(acc, a.scale, out, store, a.dreal);
+        }
+      } else if (rank != 0) {
+        // partial sums into this CTA's shared memory for rank 0 to read
+        float* st = stage_row<D>(smem, hf, row);
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t t[32];
+          tmem_ld32(acc + 32 * cc, t);
+          tmem_wait_ld();
+          reg_fence32(t);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(st + 4 * stage_chunk(cc * 8 + u, row)) =
+                make_uint4(t[4 * u], t[4 * u + 1], t[4 * u + 2], t[4 * u + 3]);
+        }
       }
     }
+  }
+
+  if (split > 1) {
+    // Every thread of every CTA of the cluster passes both barriers, also
+    // after a timeout (outputs are then undefined but nothing waits forever).
+    cluster_sync_all();
+    if (warp < 8 && rank == 0 && ew_ok) {
+      const int hf = warp >> 2, quarter = warp & 3, row = quarter * 32 + lane;
+      const int64_t key = kt * C::BT + row;
+      const uint32_t acc = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                           (hf == 0 ? C::COL_DV : C::COL_DK);
+      const uint32_t st = smem_u32(stage_row<D>(smem, hf, row));
+      const float mul = hf == 0 ? 1.f : a.scale;
+      T* out = hf == 0
+                   ? static_cast<T*>(a.out0) + bb * a.s0[0] + hk * a.s0[1] + (sv.k0 + key) * a.s0[2]
+                   : static_cast<T*>(a.out1) + bb * a.s1[0] + hk * a.s1[1] + (sv.k0 + key) * a.s1[2];
+#pragma unroll 1
+      for (int cc = 0; cc < a.dreal / 32 + (a.dreal % 32 ? 1 : 0); ++cc) {
+        uint32_t t[32];
+        tmem_ld32(acc + 32 * cc, t);
+        tmem_wait_ld();
+        reg_fence32(t);
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(t[i]);
+        for (int r = 1; r < split; ++r) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 x = ld_cluster_f4(cluster_map(st + 16 * stage_chunk(cc * 8 + u, row),
+                                                       static_cast<uint32_t>(r)));
+            v[4 * u] += x.x; v[4 * u + 1] += x.y; v[4 * u + 2] += x.z; v[4 * u + 3] += x.w;
+          }
+        }
+        if (key < Nk) {
+          const int ncol = min(32, a.dreal - 32 * cc);   // 16 or 32
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (8 * u >= ncol) break;
+            uint4 w;
+            w.x = pack2<T>(v[8 * u] * mul, v[8 * u + 1] * mul);
+            w.y = pack2<T>(v[8 * u + 2] * mul, v[8 * u + 3] * mul);
+            w.z = pack2<T>(v[8 * u + 4] * mul, v[8 * u + 5] * mul);
+            w.w = pack2<T>(v[8 * u + 6] * mul, v[8 * u + 7] * mul);
+            *reinterpret_cast<uint4*>(out + 32 * cc + 8 * u) = w;
+          }
+        }
+      }
+    }
+    cluster_sync_all();
   }
 
   tc_fence_before();
@@ -830,9 +918,16 @@ fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
   a.status = p.status;
   a.timeout_ns = p.timeout_ns;
 
-  // dK / dV: one CTA per (b, key/value head, key tile)
+  // dK / dV: one CTA per (b, key/value head, key tile); with few key/value
+  // heads (grouped or multi-query attention) a cluster of `split` CTAs
+  // shares each key tile's query heads, so the grid fills the SMs and the
+  // heaviest key tiles no longer run alone.
   a.BH = g.B * g.Hkv; a.ntiles = (g.Nk + 127) / 128;
-  const int64_t blocks1 = a.BH * a.ntiles;
+  const int64_t base1 = a.BH * a.ntiles;
+  int split = 1;
+  while (split < 8 && g.G % (2 * split) == 0 && base1 * split < 2 * device_sm_count()) split *= 2;
+  a.split = split;
+  const int64_t blocks1 = base1 * split;
   if (blocks1 > 0x7fffffffLL) return FA_ERR_SHAPE;
   a.out0 = p.dv; a.out1 = p.dk;
   for (int i = 0; i < 4; ++i) { a.s0[i] = p.sdv[i]; a.s1[i] = p.sdk[i]; }
@@ -840,12 +935,29 @@ fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
   if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM) != cudaSuccess)
     return FA_ERR_LAUNCH;
   prof_record(p, 0, stream);
-  k1<<<dim3(static_cast<unsigned>(blocks1)), dim3(DkdvCfg<D>::THREADS), DkdvCfg<D>::SMEM, stream>>>(
-      mq, mk, mv, mdo, a);
+  if (split == 1) {
+    k1<<<dim3(static_cast<unsigned>(blocks1)), dim3(DkdvCfg<D>::THREADS), DkdvCfg<D>::SMEM,
+         stream>>>(mq, mk, mv, mdo, a);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks1));
+    cfg.blockDim = dim3(DkdvCfg<D>::THREADS);
+    cfg.dynamicSmemBytes = DkdvCfg<D>::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k1, mq, mk, mv, mdo, a) != cudaSuccess) return FA_ERR_LAUNCH;
+  }
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   prof_record(p, 1, stream);
 
   // dQ: one CTA per (b, query head, query tile)
+  a.split = 1;
   a.BH = g.B * g.Hq; a.ntiles = (g.Nq + 127) / 128;
   const int64_t blocks2 = a.BH * a.ntiles;
   if (blocks2 > 0x7fffffffLL) return FA_ERR_SHAPE;
