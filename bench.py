@@ -45,10 +45,10 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 1044.2 MB per launch measured on 16 heads,
+    # bwd_dkdv_tc_kernel<bf16,128>: 1044.8 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("dkdv", "558c14be612ebef4da9c1c4ac9f907c1327a5579e07a8d5f106ae7974d19f2ad",
-     "long-bf16-B1-H32-N16384-D128-causal"): 2088.5e6,
+    ("dkdv", "2f9a705f49a991fa19d83eae80d507ae1dad56412e29a9f6853de6e9fd1404a8",
+     "long-bf16-B1-H32-N16384-D128-causal"): 2089.5e6,
 }
 
 
