@@ -67,3 +67,41 @@ def test_noalloc_rejects_sizes_beyond_its_buffer():
                               1, 0.088, 2, None)
     assert code == 12
     assert lib.fa_status_string(12).decode().startswith("FA_ERR_SCRATCH")
+
+
+@pytest.mark.gpu
+def test_forward_and_noalloc_backward_replay_from_a_cuda_graph():
+    """The use the entry point exists for: the forward and fa_bwd_noalloc
+    captured into a CUDA graph (no allocation may happen during capture) and
+    replayed; the replay gives bit-identical results to eager calls."""
+    dev = torch.device("cuda", 0)
+    fa.load_library()
+    fa.set_path(fa.FA_PATH_AUTO)
+    w = Workload("graph-bf16-causal", 1, 4, 1000, 128, "bf16", True, seed=13)
+    q, k, v, do = (t.to(dev) for t in make_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+
+    def step():
+        fa.fwd(q, k, v, o, lse, w.causal, w.scale)
+        fa.bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale)
+
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        step()                       # first call on the device: looks up the buffer
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (o, lse, dq, dk, dv)]
+    for t in (o, lse, dq, dk, dv):
+        t.fill_(float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    for name, got, want in zip(("o", "lse", "dq", "dk", "dv"), (o, lse, dq, dk, dv), ref):
+        assert torch.equal(got, want), name
