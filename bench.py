@@ -34,9 +34,10 @@ sys.path.insert(0, ROOT)
 import torch  # noqa: E402
 
 from exact_attention_83_gb300 import shard  # noqa: E402
-from exact_attention_83_gb300.inputs import (LONG_CAUSAL, GeneralWorkload, Workload,  # noqa: E402
-                                             bf16_n1024, make_general_inputs, make_inputs,
-                                             seqlen_mix, sweep)
+from exact_attention_83_gb300.inputs import (LONG_CAUSAL, SWEEP_N, TINY_FP32,  # noqa: E402
+                                             GeneralWorkload, Workload, bf16_n1024, coverage,
+                                             make_general_inputs, make_inputs, seqlen_mix,
+                                             sweep)
 
 METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 peak"
 
@@ -76,15 +77,21 @@ GENERAL = [
 
 
 def workloads():
-    ws = {LONG_CAUSAL.name: LONG_CAUSAL, PROFILE_CASE.name: PROFILE_CASE}
+    ws = {LONG_CAUSAL.name: LONG_CAUSAL, PROFILE_CASE.name: PROFILE_CASE,
+          TINY_FP32.name: TINY_FP32}
     ws.update({g.name: g for g in GENERAL})
     for c in (False, True):
         w = bf16_n1024(c)
         ws[w.name] = w
-        for N in (1024, 4096, 16384):
+        for N in SWEEP_N:
             for dt in ("bf16", "fp16"):
                 s = sweep(N, dt, c)
                 ws[s.name] = s
+        for D in (16, 32, 64, 128):
+            for N in (1000, 3001):
+                for dt in ("fp16", "bf16", "fp32"):
+                    cv = coverage(D, N, dt, c)
+                    ws[cv.name] = cv
     return ws
 
 
@@ -207,9 +214,27 @@ def cpu_baseline(w: Workload):
     t0 = time.perf_counter()
     oracle.fwd_bwd(qn, kn, vn, dn, w.causal, w.scale)
     dt = time.perf_counter() - t0
-    return {"value": sample.fwd_bwd_flops() / dt / 1e12, "unit": "TFLOP/s",
-            "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd on 1 of {w.B * w.H} heads ({dt:.1f} s)"}
+    out = {"value": sample.fwd_bwd_flops() / dt / 1e12, "unit": "TFLOP/s",
+           "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"fp64 oracle fwd+bwd on 1 of {w.B * w.H} heads ({dt:.1f} s)"}
+    # the same on one core, on one head of a quarter of the length (the
+    # oracle's work per flop does not depend on N)
+    small = Workload(w.name + "-one-head-quarter", 1, 1, max(w.N // 4, 1), w.D, w.dtype,
+                     w.causal, w.layout, w.qkv_scale, w.seed)
+    q, k, v, do = make_inputs(small)
+    qn, kn, vn, dn = (t.float().double().numpy() for t in (q, k, v, do))
+    threads = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.fwd_bwd(qn, kn, vn, dn, w.causal, w.scale)
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(threads)
+    out["single_core"] = {"value": small.fwd_bwd_flops() / dt1 / 1e12, "unit": "TFLOP/s",
+                          "cores": 1,
+                          "sample": f"one head, N={small.N} ({dt1:.1f} s)"}
+    return out
 
 
 def main():
@@ -277,6 +302,13 @@ def main():
     if fa.device_status() != 0:
         raise RuntimeError("device status not OK after warm-up")
 
+    # Inputs smaller than twice the L2 are flushed from it before every timed
+    # step (a 2 x L2 write, outside the events), and steps are timed one by one.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    in_bytes = 4 * B * H * N * D * q.element_size()
+    flush_buf = (torch.empty(2 * l2, dtype=torch.uint8, device=dev) if in_bytes < 2 * l2
+                 else None)
+
     # ---- forward + backward step, with per-kernel events on the stream
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     for e in ev:        # create the events (torch creates them lazily on first record)
@@ -288,6 +320,8 @@ def main():
         start.record(stream)
         for i in range(args.steps):
             e = ev[i]
+            if flush_buf is not None:
+                flush_buf.zero_()
             e[0].record(stream)
             fa.fwd(q, k, v, o, lse, w.causal, w.scale)
             e[1].record(stream)
@@ -297,8 +331,10 @@ def main():
         end.record(stream)
         barrier()
     fa.set_profile_events(None)
-    total_ms = max_over_ranks(start.elapsed_time(end))
-    ms_step = total_ms / args.steps
+    if flush_buf is None:
+        ms_step = max_over_ranks(start.elapsed_time(end)) / args.steps
+    else:
+        ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[4]) for e in ev))
     fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     pre_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
@@ -308,13 +344,24 @@ def main():
 
     # ---- forward alone
     barrier()
-    fs, fe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    fs.record(stream)
-    for _ in range(args.steps):
-        fa.fwd(q, k, v, o, lse, w.causal, w.scale)
-    fe.record(stream)
-    barrier()
-    fwd_only_ms = max_over_ranks(fs.elapsed_time(fe)) / args.steps
+    if flush_buf is None:
+        fs, fe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fs.record(stream)
+        for _ in range(args.steps):
+            fa.fwd(q, k, v, o, lse, w.causal, w.scale)
+        fe.record(stream)
+        barrier()
+        fwd_only_ms = max_over_ranks(fs.elapsed_time(fe)) / args.steps
+    else:
+        fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a_, b_ in fev:
+            flush_buf.zero_()
+            a_.record(stream)
+            fa.fwd(q, k, v, o, lse, w.causal, w.scale)
+            b_.record(stream)
+        barrier()
+        fwd_only_ms = max_over_ranks(statistics.mean(a_.elapsed_time(b_) for a_, b_ in fev))
 
     flops_fwd = w.fwd_flops()
     flops_step = w.fwd_bwd_flops()
@@ -350,7 +397,10 @@ def main():
             "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D,
                        "causal": w.causal, "parallelism": f"replicas{world}",
-                       "l2": "inputs 4 x %d MiB > L2, no flush" % (B * H * N * D * 2 >> 20)},
+                       "l2": ("inputs 4 x %d MiB > L2, no flush" % (B * H * N * D * q.element_size() >> 20)
+                              if flush_buf is None else
+                              "L2 flushed (%d MiB write) before each step; steps timed one by one"
+                              % (2 * l2 >> 20))},
             "fwd_tflops": world * flops_fwd / (fwd_only_ms * 1e-3) / 1e12,
             "fwd_ms": fwd_only_ms,
             "fwd_frac_of_peak": flops_fwd / (fwd_only_ms * 1e-3) / 1e12 / peak_dense,
