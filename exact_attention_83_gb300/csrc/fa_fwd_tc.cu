@@ -58,6 +58,11 @@ struct FwdCfg {
   static constexpr uint32_t COL_S0 = 0, COL_O0 = 256;
 };
 
+// Ring position of each K / V tile when tiles are loaded in consumption order
+// K_0, K_1, V_0, K_2, V_1, ...: K_j at 2j - 1 (K_0 at 0), V_j at 2j + 2.
+__device__ __forceinline__ int unit_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int unit_v(int j) { return 2 * j + 2; }
+
 struct FwdTcArgs {
   void* o;
   float* lse;
@@ -400,6 +405,350 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
+// ============================================================================
+// D <= 64: one query tile per CTA, two CTAs per SM
+// ============================================================================
+// At D = 64 one query tile needs S (128 columns), O (64) and P (64, two
+// input-type values per column) of tensor memory: 256 columns, half an SM's,
+// and its operands fit in under half the shared memory.  So two CTAs share an
+// SM; each one's softmax overlaps the other's products, and a CTA's start-up
+// and epilogue overlap the other's main loop.  With P in its own columns the
+// softmax warps release S as soon as they have read it: per key tile j the MMA
+// issuer runs S_{j+1} (once S_j has been read) and then P_j V_j (once P_j is
+// written); the softmax warps write P_{j+1} only after P_j V_j has completed,
+// which also makes O stable for a rescale.  K and V tiles share one ring,
+// filled in consumption order K_0, K_1, V_0, K_2, V_1, ...
+struct Fwd1Cfg {
+  static constexpr int D = 64;
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int TILE = BM * 128;           // one 128 x 64 tile of 16-bit values
+  static constexpr int NS = 5;                    // K/V ring slots
+  static constexpr int OFF_RING = TILE;
+  static constexpr int OFF_BAR = OFF_RING + NS * TILE;
+  static constexpr int SMEM = OFF_BAR + 1024 + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr uint32_t TMEM_COLS = 256;
+  static constexpr uint32_t COL_S = 0, COL_O = 128, COL_P = 192;
+};
+
+template <typename T, bool DROP>
+__global__ void __launch_bounds__(192, 2)
+    fwd_tc_1t_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const FwdTcArgs a) {
+  using C = Fwd1Cfg;
+  constexpr int D = C::D;
+  static_assert(2 * C::SMEM <= 227 * 1024, "two CTAs per SM");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + C::OFF_RING;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  Ctl* ctl = reinterpret_cast<Ctl*>(bars + 40);
+  const uint32_t b_q = smem_u32(&bars[0]);
+  const uint32_t b_full0 = smem_u32(&bars[1]);                   // + 8 * slot
+  const uint32_t b_empty0 = smem_u32(&bars[1 + C::NS]);          // + 8 * slot
+  const uint32_t b_sfull = smem_u32(&bars[1 + 2 * C::NS]);       // S ready
+  const uint32_t b_sfree = smem_u32(&bars[2 + 2 * C::NS]);       // S read
+  const uint32_t b_pready = smem_u32(&bars[3 + 2 * C::NS]);      // P written
+  const uint32_t b_pvdone = smem_u32(&bars[4 + 2 * C::NS]);      // P V done
+  const uint32_t b_mmadone = smem_u32(&bars[5 + 2 * C::NS]);
+  static_assert(6 + 2 * C::NS <= 40, "barriers below the control block");
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t id = blockIdx.x;
+  const int64_t bh = id % a.BH;                 // b * Hq + h
+  const int64_t qt = a.causal ? (a.npairs - 1 - id / a.BH) : (id / a.BH);   // query tile
+  const int64_t h = bh % a.g.Hq;
+  const SeqView sv = seq_view(a.g, bh / a.g.Hq);
+  if (!sv.ok) {
+    if (threadIdx.x == 0) record_status(a.status, FA_ERR_SEQLENS);
+    return;
+  }
+  const int64_t Nq = sv.nq, Nk = sv.nk;
+  if (qt * C::BM >= Nq) return;                 // this query tile lies past the sequence
+  const int32_t hq = static_cast<int32_t>(h), hk = static_cast<int32_t>(h / a.g.G);
+  const int32_t bb = static_cast<int32_t>(sv.b);
+  const int nk = static_cast<int>((Nk + C::BN - 1) / C::BN);
+  const int n = a.causal ? min(static_cast<int>(qt) + 1, nk) : nk;   // key tiles to visit
+  if (n == 0) {
+    // No key at all (an empty key sequence): O = 0 and L = -inf.
+    if (warp < 4) {
+      const int64_t qrow = qt * C::BM + warp * 32 + lane;
+      if (qrow < Nq) {
+        T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qrow) * a.so[2];
+        for (int d = 0; d < a.dreal; ++d) orow[d] = Elem<T>::from_f32(0.f);
+        a.lse[lse_index(a.g, sv, h, qrow)] = -INFINITY;
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(b_full0 + 8 * s, 1);
+      mbar_init(b_empty0 + 8 * s, 1);
+    }
+    mbar_init(b_sfull, 1);
+    mbar_init(b_sfree, 128);
+    mbar_init(b_pready, 128);
+    mbar_init(b_pvdone, 1);
+    mbar_init(b_mmadone, 1);
+    ctl->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      uint32_t issued[C::NS];
+#pragma unroll
+      for (int s = 0; s < C::NS; ++s) issued[s] = 0;
+      mbar_arrive_expect_tx(b_q, C::TILE);
+      tma_load_4d(smem_u32(sQ), &tmq, b_q, 0, static_cast<int32_t>(sv.q0 + qt * C::BM), hq, bb);
+      bool ok = true;
+      // units in consumption order; unit 2*n - 1 would be K_n (absent)
+      for (int u = 0; ok && u <= 2 * n; ++u) {
+        int j, kv;
+        if (u == 0) { j = 0; kv = 0; }
+        else if (u & 1) { j = (u + 1) / 2; kv = 0; }
+        else { j = (u - 2) / 2; kv = 1; }
+        if (j >= n) continue;
+        const int s = u % C::NS;
+        const uint32_t r = static_cast<uint32_t>(u / C::NS);
+        if (r > 0 && !(ok = wait_bounded(b_empty0 + 8 * s, (r - 1) & 1, ctl, a.status,
+                                         a.timeout_ns)))
+          break;
+        mbar_arrive_expect_tx(b_full0 + 8 * s, C::TILE);
+        tma_load_4d(smem_u32(sRing + s * C::TILE), kv ? &tmv : &tmk, b_full0 + 8 * s, 0,
+                    static_cast<int32_t>(sv.k0 + j * C::BN), hk, bb);
+        issued[s] = r + 1;
+      }
+      // Drain: every copy issued has landed before the CTA may exit.
+      wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns, false);
+      for (int s = 0; s < C::NS; ++s)
+        if (issued[s]) wait_bounded(b_full0 + 8 * s, (issued[s] - 1) & 1, ctl, a.status,
+                                    a.timeout_ns, false);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_f16<T>(128, C::BN, false, false);
+      const uint32_t idO = idesc_f16<T>(128, D, false, true);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sRing), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sRing), C::TILE, 1024);
+      auto slot_of = [](int u) { return u % C::NS; };
+      auto parity_of = [](int u) { return static_cast<uint32_t>((u / C::NS) & 1); };
+      auto issue_S = [&](int slot) {   // S = Q K^T
+        const uint64_t kb = dK0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::COL_S, dQ0 + ((kk * 32) >> 4), kb + ((kk * 32) >> 4), idS,
+                 kk > 0 ? 1u : 0u);
+      };
+      auto issue_PV = [&](int slot, bool acc) {   // O += P V, P from tensor memory
+        const uint64_t vb = dV0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ts(tmem + C::COL_O, tmem + C::COL_P + 8 * kk,
+                 vb + static_cast<uint64_t>((kk * 2048) >> 4), idO, (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns) &&
+                wait_bounded(b_full0 + 8 * slot_of(unit_k(0)), parity_of(unit_k(0)), ctl,
+                             a.status, a.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        issue_S(slot_of(unit_k(0)));
+        // A test can withhold this arrival in CTA 0 to make the softmax warps'
+        // bounded wait run out (the timeout path, without a fault).
+        if (!(a.withhold_arrival && blockIdx.x == 0)) mma_commit(b_sfull);
+        mma_commit(b_empty0 + 8 * slot_of(unit_k(0)));
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) {
+          // S_{j+1} once S_j has been read out of TMEM
+          const int uk = unit_k(j + 1);
+          if (!(ok = wait_bounded(b_full0 + 8 * slot_of(uk), parity_of(uk), ctl, a.status,
+                                  a.timeout_ns)))
+            break;
+          if (!(ok = wait_bounded(b_sfree, j & 1, ctl, a.status, a.timeout_ns))) break;
+          tc_fence_after();
+          issue_S(slot_of(uk));
+          mma_commit(b_sfull);
+          mma_commit(b_empty0 + 8 * slot_of(uk));
+        }
+        // P_j V_j once P_j is in TMEM
+        const int uv = unit_v(j);
+        if (!(ok = wait_bounded(b_full0 + 8 * slot_of(uv), parity_of(uv), ctl, a.status,
+                                a.timeout_ns)))
+          break;
+        if (!(ok = wait_bounded(b_pready, j & 1, ctl, a.status, a.timeout_ns))) break;
+        tc_fence_after();
+        issue_PV(slot_of(uv), j > 0);
+        mma_commit(b_pvdone);
+        mma_commit(b_empty0 + 8 * slot_of(uv));
+      }
+      // Drain: every MMA (and every commit arrival) of this thread is complete.
+      mma_commit(b_mmadone);
+      wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int r = warp * 32 + lane;                          // row in the query tile
+    const int64_t qrow = qt * C::BM + r;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t tS = lane_base + C::COL_S;
+    const uint32_t tO = lane_base + C::COL_O;
+    const uint32_t tP = lane_base + C::COL_P;
+    const float c = a.c;
+    float m = -INFINITY, l = 0.f;
+    uint32_t keepq = 0;            // dropout: keep bits of the current group of eight keys
+    (void)keepq;
+    bool ok = true;
+    // last valid key column of the last key tile
+    const int lim_last = static_cast<int>(Nk - 1 - static_cast<int64_t>(nk - 1) * C::BN);
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = wait_warp(b_sfull, j & 1, ctl, a.status, a.timeout_ns))) break;
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tS + 0, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tmem_wait_ld();
+        reg_fence32(r0); reg_fence32(r1); reg_fence32(r2); reg_fence32(r3);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(r0[i]);
+          s[32 + i] = __uint_as_float(r1[i]);
+          s[64 + i] = __uint_as_float(r2[i]);
+          s[96 + i] = __uint_as_float(r3[i]);
+        }
+      }
+      // S is in registers: the tensor cores may overwrite it with S_{j+1}.
+      tc_fence_before();
+      mbar_arrive(b_sfree);
+      // Exclude keys past the sequence (last key tile) and keys after the
+      // query (the diagonal tile, the only one a causal row can straddle).
+      int lim = C::BN - 1;
+      if (a.causal && j == qt) lim = r;
+      if (j == nk - 1) lim = min(lim, lim_last);
+      if (lim < C::BN - 1) {
+#pragma unroll
+        for (int kk = 0; kk < C::BN; ++kk)
+          if (kk > lim) s[kk] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int kk = 4; kk < C::BN; kk += 4) {
+        mx0 = fmaxf(mx0, s[kk]);
+        mx1 = fmaxf(mx1, s[kk + 1]);
+        mx2 = fmaxf(mx2, s[kk + 2]);
+        mx3 = fmaxf(mx3, s[kk + 3]);
+      }
+      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
+      // Lazy rescale decision (warp-uniform for the TMEM access below).
+      bool rescale = false;
+      float alpha = 1.f;
+      if (j == 0) {
+        m = m_new;
+      } else {
+        const bool need = m_new > m + 8.f;
+        rescale = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ex2(m - m_new);
+          l *= alpha;
+          m = m_new;
+        }
+      }
+      const float negm = -m;
+      float sum0 = 0.f, sum1 = 0.f;
+      // P in two halves of 64 keys (32 columns each); the first half waits
+      // (in registers) until P_{j-1} V has finished reading the P columns,
+      // which also makes O stable for a rescale.
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(s[64 * half + 2 * i], c, negm));
+          const float p1 = ex2(fmaf(s[64 * half + 2 * i + 1], c, negm));
+          sum0 += p0;
+          sum1 += p1;
+          if constexpr (DROP) {
+            // l sums the undropped weights; P V takes the dropped, rescaled
+            // ones; one generator call covers eight keys
+            const int key = j * C::BN + 64 * half + 2 * i;
+            if ((i & 3) == 0)
+              keepq = keep8(a.drop, static_cast<uint32_t>(key >> 3), static_cast<uint32_t>(qrow),
+                            static_cast<uint32_t>(bh));
+            const uint32_t bits = keepq >> (2 * (i & 3));
+            pk[i] = pack2<T>((bits & 1u) ? p0 * a.drop.rscale : 0.f,
+                             (bits & 2u) ? p1 * a.drop.rscale : 0.f);
+          } else {
+            pk[i] = pack2<T>(p0, p1);
+          }
+        }
+        if (half == 0 && j > 0) {
+          if (!(ok = wait_warp(b_pvdone, (j - 1) & 1, ctl, a.status, a.timeout_ns))) break;
+          tc_fence_after();
+          if (rescale) {
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t t[32];
+              tmem_ld32(tO + 32 * cc, t);
+              tmem_wait_ld();
+              reg_fence32(t);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+              tmem_st32(tO + 32 * cc, t);
+            }
+          }
+        }
+        tmem_st32(tP + 32 * half, pk);
+      }
+      if (!ok) break;
+      l += sum0 + sum1;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(b_pready);
+    }
+    if (ok) ok = wait_warp(b_pvdone, (n - 1) & 1, ctl, a.status, a.timeout_ns);
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool store = qrow < Nq;
+      T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qrow) * a.so[2];
+      store_row_cols<T>(tO, inv, orow, store, a.dreal);
+      if (store) a.lse[lse_index(a.g, sv, h, qrow)] = (m + log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 template <typename T, int D>
 fa_status run_fwd_tc(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
@@ -425,11 +774,24 @@ fa_status run_fwd_tc(const FwdParams& p, cudaStream_t stream) {
   a.withhold_arrival = p.withhold_arrival;
   const int64_t blocks = a.BH * a.npairs;
   if (blocks > 0x7fffffffLL) return FA_ERR_SHAPE;
-  auto kern = p.drop.on ? fwd_tc_kernel<T, D, true> : fwd_tc_kernel<T, D, false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
-      cudaSuccess)
-    return FA_ERR_LAUNCH;
-  kern<<<dim3(static_cast<unsigned>(blocks)), dim3(C::THREADS), C::SMEM, stream>>>(mq, mk, mv, a);
+  if constexpr (D == 64) {
+    // one query tile per CTA (npairs counts query tiles here), two CTAs per SM
+    a.npairs = (g.Nq + 127) / 128;
+    const int64_t blocks1 = a.BH * a.npairs;
+    if (blocks1 > 0x7fffffffLL) return FA_ERR_SHAPE;
+    auto kern = p.drop.on ? fwd_tc_1t_kernel<T, true> : fwd_tc_1t_kernel<T, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Fwd1Cfg::SMEM) !=
+        cudaSuccess)
+      return FA_ERR_LAUNCH;
+    kern<<<dim3(static_cast<unsigned>(blocks1)), dim3(Fwd1Cfg::THREADS), Fwd1Cfg::SMEM, stream>>>(
+        mq, mk, mv, a);
+  } else {
+    auto kern = p.drop.on ? fwd_tc_kernel<T, D, true> : fwd_tc_kernel<T, D, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+        cudaSuccess)
+      return FA_ERR_LAUNCH;
+    kern<<<dim3(static_cast<unsigned>(blocks)), dim3(C::THREADS), C::SMEM, stream>>>(mq, mk, mv, a);
+  }
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
