@@ -205,3 +205,37 @@ def test_autograd_general():
     assert torch.equal(o, o2)
     for a, b in zip((qa.grad, ka.grad, va.grad), grads):
         assert torch.equal(a, b)
+
+
+def _random_general(seed: int) -> GeneralWorkload:
+    """A seeded random general problem: any combination of grouped heads,
+    packed or fixed lengths (empty sequences included), Nq != Nk, causal,
+    dropout, head dimension and dtype, at sizes the oracle runs in well under a
+    second."""
+    r = np.random.default_rng(seed)
+    D = int(r.choice([16, 32, 64, 128]))
+    dtype = str(r.choice(["bf16", "fp16", "fp32"]))
+    Hkv = int(r.choice([1, 2]))
+    Hq = Hkv * int(r.choice([1, 2, 4]))
+    B = int(r.integers(1, 4))
+    causal = bool(r.integers(0, 2))
+    p = float(r.choice([0.0, 0.0, 0.25]))
+    if r.integers(0, 2):
+        lq = tuple(int(x) for x in r.integers(0, 300, size=B))
+        lk = tuple(int(x) for x in r.integers(0, 300, size=B))
+        if sum(lq) == 0:
+            lq = (1,) + lq[1:]
+        if sum(lk) == 0:
+            lk = (1,) + lk[1:]
+        return GeneralWorkload(f"fuzz{seed}", B, Hq, Hkv, max(max(lq), 1), max(max(lk), 1), D,
+                               dtype, causal, seqlens_q=lq, seqlens_k=lk, dropout_p=p,
+                               seed=seed, drop_seed=seed * 7919, drop_offset=seed)
+    Nq, Nk = int(r.integers(1, 400)), int(r.integers(1, 400))
+    return GeneralWorkload(f"fuzz{seed}", B, Hq, Hkv, Nq, Nk, D, dtype, causal, dropout_p=p,
+                           seed=seed, drop_seed=seed * 7919, drop_offset=seed)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_general_problems(seed):
+    w = _random_general(seed)
+    compare(w, *run_general(w))
