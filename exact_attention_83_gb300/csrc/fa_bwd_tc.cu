@@ -1,5 +1,7 @@
 // Tensor-core backward: TMA + tcgen05 + TMEM, warp-specialised, for fp16/bf16
-// with D in {64, 128}.
+// with D in {64, 128} (16 and 32 run through D = 64 with the head dimension
+// zero-filled by the TMA loads), over the general geometry of fa_internal.h
+// (sequence views, grouped key/value heads) and, as a template flag, dropout.
 //
 // The FlashAttention-2 split of "Triton FlashAttention" (project summary): a
 // dK/dV kernel that, for each 128-key tile, loops over the query tiles that
@@ -24,6 +26,11 @@
 // its rounded P^T / dS into the TMEM columns it alone reads, so the two never
 // race, and the MMAs that consume them are issued per half as soon as that
 // half is ready.
+//
+// With grouped heads the dK/dV kernel of a key/value head loops over every
+// query head that reads it; when that leaves too few CTAs for the GPU, a
+// cluster of CTAs splits the query heads of one key tile and sums its partial
+// dK, dV through distributed shared memory (see the kernel).
 //
 // Every mbarrier wait is bounded (tc_common.cuh); on a timeout the CTA drains
 // its copies and MMAs in flight, frees its tensor memory and exits.

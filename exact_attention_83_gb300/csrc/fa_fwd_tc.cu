@@ -1,5 +1,9 @@
 // Tensor-core forward: TMA + tcgen05 + TMEM, warp-specialised, for fp16/bf16
-// with D in {64, 128}.
+// with D in {64, 128} (16 and 32 run through D = 64 with the head dimension
+// zero-filled by the TMA loads).  D = 128 uses fwd_tc_kernel below (two query
+// tiles per CTA); D <= 64 uses fwd_tc_1t_kernel further down (one query tile
+// per CTA, two CTAs per SM).  Both handle the general geometry of fa_internal.h
+// (sequence views, grouped key/value heads) and, as a template flag, dropout.
 //
 // Algorithm ("FlashAttention-2 from PyTorch to Triton", the running quantities
 // m, l, O and the store of L = m + log l; "Triton FlashAttention", the online
@@ -7,7 +11,8 @@
 // rescaled when the max moves, and causal key tiles above the diagonal never
 // visited): for each 128-row query tile, loop over 128-key tiles,
 //   S = Q K_j^T (tensor cores, fp32 in TMEM),
-//   mask keys past N (last tile) and keys after the query (diagonal tile only),
+//   mask keys past the sequence (last tile) and keys after the query
+//   (diagonal tile only),
 //   m_new = max(m, c * rowmax S) with c = scale * log2(e),
 //   P = exp2(c * S - m) rounded to the input type (FIX 1 of the Triton page),
 //   l += rowsum P,  O += P V_j (tensor cores, fp32 in TMEM),
@@ -20,7 +25,8 @@
 // denominator share the one max used for that row, and the final division
 // cancels it.
 //
-// CTA = two query tiles (256 rows) of one head sharing every K/V tile load.
+// fwd_tc_kernel: CTA = two query tiles (256 rows) of one head sharing every
+// K/V tile load.
 // Warps 0-3: softmax + epilogue of query tile 0 (one TMEM lane = one row per
 // thread); warps 4-7: the same for query tile 1; warp 8: TMA producer (lane 0)
 // and TMEM allocation; warp 9: MMA issuer (lane 0).  TMEM columns: S0 [0,128),
