@@ -9,7 +9,11 @@ in HBM.  The inputs (4 x 128 MiB) are larger than the 129 MB L2, so L2 is not
 flushed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--bwd split|fused]
+
+`--bwd fused` times the single-pass backward (fa_bwd_fused: one kernel per key
+tile, dQ summed by fp32 bulk reductions into a workspace, then converted)
+instead of the split one.
 
 Under torchrun each rank runs its own copy of the workload (independent heads,
 no collective on the data path; weak scaling) and rank 0 prints the line.
@@ -246,6 +250,7 @@ def main():
     ap.add_argument("--workload", default=LONG_CAUSAL.name)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--bwd", default="split", choices=["split", "fused"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -282,11 +287,20 @@ def main():
     delta = torch.empty_like(lse)
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
     stream = torch.cuda.current_stream(dev)
+    fused = args.bwd == "fused"
+    ws = (torch.empty(fa.workspace_bytes(q, k, w.causal, w.scale) // 4, dtype=torch.float32,
+                      device=dev) if fused else None)
+
+    def bwd():
+        if fused:
+            fa.bwd_fused(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale, workspace=ws)
+        else:
+            fa.bwd(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale)
 
     def step():
         fa.fwd(q, k, v, o, lse, w.causal, w.scale)
         fa.bwd_preprocess(o, do, delta)
-        fa.bwd(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale)
+        bwd()
 
     def barrier():
         if world > 1:
@@ -327,7 +341,7 @@ def main():
             e[1].record(stream)
             fa.bwd_preprocess(o, do, delta)
             fa.set_profile_events(e[2:5])
-            fa.bwd(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale)
+            bwd()
         end.record(stream)
         barrier()
     fa.set_profile_events(None)
@@ -374,16 +388,17 @@ def main():
     peak_sustained = pk["bf16_tflops_sustained"]
 
     # dominant kernel: the dK/dV kernel (4 of the 7 N x N x D products of the
-    # split backward); its algorithmic flops are 4 products of 2*N^2*D per
-    # head, halved when causal.
-    dkdv_flops = 4 * 2.0 * B * H * N * N * D * (0.5 if w.causal else 1.0)
+    # split backward), or the single-pass kernel (5 products); algorithmic
+    # flops are 2*N^2*D per product and head, halved when causal.
+    nprod = 5 if fused else 4
+    dkdv_flops = nprod * 2.0 * B * H * N * N * D * (0.5 if w.causal else 1.0)
     achieved = dkdv_flops / (dkdv_ms * 1e-3) / 1e12
-    sha = kernel_source_sha("fa_bwd_tc.cu")
-    traffic = MEASURED_TRAFFIC.get(("dkdv", sha, w.name))
+    sha = kernel_source_sha("fa_bwd_fused.cu" if fused else "fa_bwd_tc.cu")
+    traffic = MEASURED_TRAFFIC.get(("fused" if fused else "dkdv", sha, w.name))
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(args, w, dev, fa)
+        e2e = measure_e2e(args, w, dev, fa, fused)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -397,6 +412,7 @@ def main():
             "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "N": N, "D": D,
                        "causal": w.causal, "parallelism": f"replicas{world}",
+                       "backward": BWD_NAMES[args.bwd],
                        "l2": ("inputs 4 x %d MiB > L2, no flush" % (B * H * N * D * q.element_size() >> 20)
                               if flush_buf is None else
                               "L2 flushed (%d MiB write) before each step; steps timed one by one"
@@ -407,11 +423,10 @@ def main():
             "fwd_bwd_frac_of_peak": value / world / peak_dense,
             "fwd_bwd_frac_of_sustained_peak": value / world / peak_sustained,
             "peak_tflops": peak_dense, "peak_source": pk["source"] + " burst bf16 (cuBLAS)",
-            "kernel_ms": {"fwd": fwd_ms, "preprocess": pre_ms, "bwd_dkdv": dkdv_ms,
-                          "bwd_dq": dq_ms},
-            "roofline": {"kernel": "bwd_dkdv", "bound": "tensor", "achieved": achieved,
-                         "peak": peak_dense, "unit": "TFLOP/s", "frac": achieved / peak_dense,
-                         "traffic": traffic},
+            "kernel_ms": kernel_ms(fused, fwd_ms, pre_ms, dkdv_ms, dq_ms),
+            "roofline": {"kernel": "bwd_fused" if fused else "bwd_dkdv", "bound": "tensor",
+                         "achieved": achieved, "peak": peak_dense, "unit": "TFLOP/s",
+                         "frac": achieved / peak_dense, "traffic": traffic},
             "clocks": clocks.summary(),
             "gpu_launches": 4 * args.steps,
             "e2e": e2e,
@@ -420,6 +435,17 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+BWD_NAMES = {"split": "split: dK/dV kernel + dQ kernel (deterministic)",
+             "fused": "single pass: dQ by fp32 bulk reduce-add + convert"}
+
+
+def kernel_ms(fused, fwd_ms, pre_ms, k1_ms, k2_ms):
+    if fused:
+        return {"fwd": fwd_ms, "preprocess+workspace_zero": pre_ms, "bwd_fused": k1_ms,
+                "dq_convert": k2_ms}
+    return {"fwd": fwd_ms, "preprocess": pre_ms, "bwd_dkdv": k1_ms, "bwd_dq": k2_ms}
 
 
 def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
@@ -444,6 +470,16 @@ def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     o4, do4 = fa._as4(o, w.packed), fa._as4(do, w.packed)
     stream = torch.cuda.current_stream(dev)
+    fused = args.bwd == "fused"
+    ws = (torch.empty(fa.workspace_bytes(q, k, w.causal, w.scale, **kw) // 4,
+                      dtype=torch.float32, device=dev) if fused else None)
+
+    def bwd():
+        if fused:
+            fa.bwd_fused(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale, workspace=ws,
+                         **kw)
+        else:
+            fa.bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale, **kw)
 
     def barrier():
         if world > 1:
@@ -453,7 +489,7 @@ def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
     for _ in range(args.warmup):
         fa.fwd_ex(q, k, v, o, lse, w.causal, w.scale, **kw)
         fa.bwd_preprocess(o4, do4, delta)
-        fa.bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale, **kw)
+        bwd()
     barrier()
     if fa.device_status() != 0:
         raise RuntimeError("device status not OK after warm-up")
@@ -472,7 +508,7 @@ def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
             e[1].record(stream)
             fa.bwd_preprocess(o4, do4, delta)
             fa.set_profile_events(e[2:5])
-            fa.bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale, **kw)
+            bwd()
         end.record(stream)
         barrier()
     fa.set_profile_events(None)
@@ -486,7 +522,7 @@ def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
     value = world * w.fwd_bwd_flops() / (ms_step * 1e-3) / 1e12
     pk = peaks()
     peak = pk["bf16_tflops"]
-    dkdv_flops = 4 * 2.0 * w.D * w.Hq * w.pairs()
+    dkdv_flops = (5 if fused else 4) * 2.0 * w.D * w.Hq * w.pairs()
     achieved = dkdv_flops / (dkdv_ms * 1e-3) / 1e12
     if rank == 0:
         line = {
@@ -497,16 +533,16 @@ def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq,
                        "Nk": w.Nk, "D": w.D, "causal": w.causal, "packed": w.packed,
                        "dropout_p": w.dropout_p, "parallelism": f"replicas{world}",
+                       "backward": BWD_NAMES[args.bwd],
                        "flops": "4*D*Hq*(attended pairs), backward credited 2.5x"},
             "fwd_tflops": w.fwd_flops() / (fwd_ms * 1e-3) / 1e12, "fwd_ms": fwd_ms,
             "fwd_frac_of_peak": w.fwd_flops() / (fwd_ms * 1e-3) / 1e12 / peak,
             "fwd_bwd_frac_of_peak": value / world / peak,
             "peak_tflops": peak, "peak_source": pk["source"] + " burst bf16 (cuBLAS)",
-            "kernel_ms": {"fwd": fwd_ms, "preprocess": pre_ms, "bwd_dkdv": dkdv_ms,
-                          "bwd_dq": dq_ms},
-            "roofline": {"kernel": "bwd_dkdv", "bound": "tensor", "achieved": achieved,
-                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                         "traffic": None},
+            "kernel_ms": kernel_ms(fused, fwd_ms, pre_ms, dkdv_ms, dq_ms),
+            "roofline": {"kernel": "bwd_fused" if fused else "bwd_dkdv", "bound": "tensor",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None},
             "clocks": clocks.summary(),
             "gpu_launches": 4 * args.steps,
             "e2e": None,
@@ -517,7 +553,7 @@ def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
         torch.distributed.destroy_process_group()
 
 
-def measure_e2e(args, w, dev, fa):
+def measure_e2e(args, w, dev, fa, fused=False):
     """Same metric through the public API with host buffers.  Every step copies
     Q, K, V, dO from pinned host memory to the device, runs the forward and
     the backward, and copies O, dQ, dK, dV back to pinned host memory.  The
@@ -531,6 +567,8 @@ def measure_e2e(args, w, dev, fa):
     dout = [[torch.empty(hq.shape, dtype=hq.dtype, device=dev) for _ in range(4)] for _ in range(2)]
     lse = [torch.empty(hq.shape[:3], dtype=torch.float32, device=dev) for _ in range(2)]
     delta = [torch.empty(hq.shape[:3], dtype=torch.float32, device=dev) for _ in range(2)]
+    ws = ([torch.empty(fa.workspace_bytes(din[b][0], din[b][1], w.causal, w.scale) // 4,
+                       dtype=torch.float32, device=dev) for b in range(2)] if fused else None)
     s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     ev = lambda: torch.cuda.Event()
     in_ready, comp_done, out_done = {}, {}, {}
@@ -551,7 +589,11 @@ def measure_e2e(args, w, dev, fa):
             o, dq, dk, dv = dout[b]
             fa.fwd(q, k, v, o, lse[b], w.causal, w.scale)
             fa.bwd_preprocess(o, do, delta[b])
-            fa.bwd(q, k, v, do, lse[b], delta[b], dq, dk, dv, w.causal, w.scale)
+            if fused:
+                fa.bwd_fused(q, k, v, do, lse[b], delta[b], dq, dk, dv, w.causal, w.scale,
+                             workspace=ws[b])
+            else:
+                fa.bwd(q, k, v, do, lse[b], delta[b], dq, dk, dv, w.causal, w.scale)
             comp_done[i] = ev(); comp_done[i].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[i])

@@ -201,12 +201,14 @@ fa_status run_fwd(const Problem& pb, const void* q, const int64_t* sq, const voi
   return launch_fwd_ffma(p, stream);
 }
 
-fa_status run_bwd(const Problem& pb, const void* q, const int64_t* sq, const void* k,
-                  const int64_t* sk, const void* v, const int64_t* sv, const void* dout,
-                  const int64_t* sdo, const float* lse, const float* delta, void* dq,
-                  const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
-                  const int64_t* sdv, cudaStream_t stream) {
-  BwdParams p{};
+// Validates the backward's tensors and fills p (everything but the path).
+fa_status prepare_bwd(const Problem& pb, const void* q, const int64_t* sq, const void* k,
+                      const int64_t* sk, const void* v, const int64_t* sv, const void* dout,
+                      const int64_t* sdo, const float* lse, const float* delta, void* dq,
+                      const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
+                      const int64_t* sdv, BwdParams* out) {
+  BwdParams& p = *out;
+  p = BwdParams{};
   const Geo& g = pb.g;
   FA_TRY(check_tensor(q, sq, g.Bt, g.Hq, g.rows_q, pb.dtype, p.sq));
   FA_TRY(check_tensor(k, sk, g.Bt, g.Hkv, g.rows_k, pb.dtype, p.sk));
@@ -225,6 +227,17 @@ fa_status run_bwd(const Problem& pb, const void* q, const int64_t* sq, const voi
   p.causal = pb.causal; p.scale = pb.scale; p.dtype = pb.dtype; p.drop = pb.drop;
   p.status = dev->status; p.timeout_ns = g_timeout_ns.load();
   p.prof = g_prof_on.load() ? g_prof_events : nullptr;
+  return FA_OK;
+}
+
+fa_status run_bwd(const Problem& pb, const void* q, const int64_t* sq, const void* k,
+                  const int64_t* sk, const void* v, const int64_t* sv, const void* dout,
+                  const int64_t* sdo, const float* lse, const float* delta, void* dq,
+                  const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
+                  const int64_t* sdv, cudaStream_t stream) {
+  BwdParams p;
+  FA_TRY(prepare_bwd(pb, q, sq, k, sk, v, sv, dout, sdo, lse, delta, dq, sdq, dk, sdk, dv, sdv,
+                     &p));
   if (use_tc(pb.dtype) && have_bwd_tc(pb.D, pb.dtype)) return launch_bwd_tc(p, stream);
   return launch_bwd_ffma(p, stream);
 }
@@ -317,6 +330,31 @@ fa_status fa_bwd_ex(const fa_problem* prob, const void* q, const int64_t* sq, co
                  stream);
 }
 
+size_t fa_bwd_fused_workspace_bytes(const fa_problem* prob) {
+  Problem pb{};
+  if (check_problem(prob, &pb) != FA_OK) return 0;
+  return bwd_fused_workspace_floats(pb.g, pb.D) * sizeof(float);
+}
+
+fa_status fa_bwd_fused(const fa_problem* prob, const void* q, const int64_t* sq, const void* k,
+                       const int64_t* sk, const void* v, const int64_t* sv, const void* dout,
+                       const int64_t* sdo, const float* lse, const float* delta, void* dq,
+                       const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
+                       const int64_t* sdv, float* dq_accum, size_t workspace_bytes,
+                       cudaStream_t stream) {
+  Problem pb{};
+  FA_TRY(check_problem(prob, &pb));
+  if (pb.dtype == FA_F32) return FA_ERR_DTYPE;
+  if (!dq_accum) return FA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(dq_accum) % 16 != 0) return FA_ERR_ALIGN;
+  if (workspace_bytes < bwd_fused_workspace_floats(pb.g, pb.D) * sizeof(float))
+    return FA_ERR_SCRATCH;
+  BwdParams p;
+  FA_TRY(prepare_bwd(pb, q, sq, k, sk, v, sv, dout, sdo, lse, delta, dq, sdq, dk, sdk, dv, sdv,
+                     &p));
+  return launch_bwd_fused(p, dq_accum, stream);
+}
+
 fa_status fa_get_device_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_LAUNCH;
   DeviceInfo* dev = nullptr;
@@ -346,7 +384,8 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_ARCH: return "FA_ERR_ARCH: the current device is not sm_103";
     case FA_ERR_SCALE: return "FA_ERR_SCALE: scale must be finite and > 0";
     case FA_ERR_ARG: return "FA_ERR_ARG: invalid argument";
-    case FA_ERR_SCRATCH: return "FA_ERR_SCRATCH: B*H*N exceeds FA_NOALLOC_MAX_ROWS";
+    case FA_ERR_SCRATCH:
+      return "FA_ERR_SCRATCH: B*H*N exceeds FA_NOALLOC_MAX_ROWS, or the workspace is too small";
     case FA_ERR_SEQLENS: return "FA_ERR_SEQLENS: packed sequence offsets are inconsistent";
   }
   return "unknown fa_status";

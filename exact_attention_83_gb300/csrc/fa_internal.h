@@ -159,12 +159,21 @@ fa_status launch_fwd_tc(const FwdParams& p, cudaStream_t s);
 fa_status launch_bwd_tc(const BwdParams& p, cudaStream_t s);
 bool have_fwd_tc(int64_t D, fa_dtype dt);
 bool have_bwd_tc(int64_t D, fa_dtype dt);
+// Single-pass backward (fp16/bf16): dK, dV and dQ through the fp32 workspace
+// `ws` of bwd_fused_workspace_floats(g, D) floats, 16-byte aligned.
+fa_status launch_bwd_fused(const BwdParams& p, float* ws, cudaStream_t s);
+size_t bwd_fused_workspace_floats(const Geo& g, int64_t D);
 
 // Encodes a 4-D tiled TMA map (d, n, h, b) over a strided [B,H,N,D] fp16/bf16
 // tensor with 128-byte swizzle and a box of box_cols x box_rows elements.
 bool encode_tile_map(CUtensorMap* map, const void* base, fa_dtype dt, int64_t B, int64_t H,
                      int64_t N, int64_t D, const int64_t* strides, uint32_t box_rows,
                      uint32_t box_cols);
+
+// Encodes a 3-D tiled TMA map over `planes` contiguous blocks of `rows` fp32
+// rows of `cols` elements, 128-byte swizzle, box of box_cols x box_rows.
+bool encode_f32_rows_map(CUtensorMap* map, const float* base, int64_t cols, int64_t rows,
+                         int64_t planes, uint32_t box_cols, uint32_t box_rows);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

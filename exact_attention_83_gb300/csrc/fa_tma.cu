@@ -1,8 +1,10 @@
-// Host side of the TMA loads: encodes 4-D tiled tensor maps over the caller's
+// Host side of the TMA copies: encodes 4-D tiled tensor maps over the caller's
 // strided [B, H, N, D] tensors (dimensions innermost first: d, n, h, b), so a
 // permuted view needs no copy and the zero fill past N stops at the end of
-// each head.  cuTensorMapEncodeTiled is reached through the runtime's driver
-// entry point, so libfa needs no link against libcuda.
+// each head, and 3-D maps over contiguous fp32 row blocks (the dQ workspace
+// of the single-pass backward, target of bulk reductions).
+// cuTensorMapEncodeTiled is reached through the runtime's driver entry
+// point, so libfa needs no link against libcuda.
 #include "fa_internal.h"
 
 #include <cudaTypedefs.h>
@@ -49,6 +51,23 @@ bool encode_tile_map(CUtensorMap* map, const void* base, fa_dtype dt, int64_t B,
   const CUresult r = fn(map, type, 4, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_f32_rows_map(CUtensorMap* map, const float* base, int64_t cols, int64_t rows,
+                         int64_t planes, uint32_t box_cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 4,
+                           static_cast<cuuint64_t>(cols) * 4 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

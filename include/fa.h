@@ -56,6 +56,7 @@
 #ifndef FA_H_
 #define FA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -84,7 +85,8 @@ typedef enum {
   FA_ERR_ARCH = 9,     /* the current device is not sm_103                      */
   FA_ERR_SCALE = 10,   /* scale is not finite and > 0                          */
   FA_ERR_ARG = 11,     /* another invalid argument (e.g. an unknown option)    */
-  FA_ERR_SCRATCH = 12, /* fa_bwd_noalloc: B*H*N exceeds FA_NOALLOC_MAX_ROWS    */
+  FA_ERR_SCRATCH = 12, /* B*H*N above FA_NOALLOC_MAX_ROWS (fa_bwd_noalloc) or */
+                       /* a workspace too small (fa_bwd_fused)              */
   FA_ERR_SEQLENS = 13  /* device-reported: packed offsets inconsistent (below) */
 } fa_status;
 
@@ -244,6 +246,36 @@ FA_API fa_status fa_bwd_ex(const fa_problem* prob, const void* q, const int64_t*
                            const float* lse, const float* delta, void* dq,
                            const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
                            const int64_t* sdv, cudaStream_t stream);
+
+/*
+ * Single-pass backward for a general problem (fp16 / bf16 only): the same
+ * inputs, outputs and validation as fa_bwd_ex, computed by one kernel per key
+ * tile that also produces each tile's share of dQ ("FlashAttention-2 from
+ * PyTorch to Triton", defect 5: dQ accumulated by atomics instead of a second
+ * pass).  The shares are summed by fp32 bulk reductions into `dq_accum`, a
+ * caller-owned DEVICE buffer of at least fa_bwd_fused_workspace_bytes(prob)
+ * bytes, 16-byte aligned, which the call zeroes on `stream` and then converts
+ * into dq (scaled, rounded to the input type).  The buffer may be reused once
+ * the call's work on `stream` has finished; the call allocates nothing.
+ *
+ * dK and dV are bitwise reproducible; dQ is not, because the order in which
+ * key tiles add into a row is not fixed (results differ from run to run by
+ * fp32 rounding).  Query rows that belong to no sequence (packed rows past
+ * cu_seqlens_q[B] or before cu_seqlens_q[0]) are left untouched, as by
+ * fa_bwd_ex.
+ *
+ * Errors: those of fa_bwd_ex; FA_ERR_DTYPE for FA_F32; FA_ERR_NULL for a NULL
+ * dq_accum; FA_ERR_ALIGN for a dq_accum not 16-byte aligned; FA_ERR_SCRATCH
+ * when workspace_bytes is below fa_bwd_fused_workspace_bytes(prob).
+ */
+FA_API size_t fa_bwd_fused_workspace_bytes(const fa_problem* prob);
+FA_API fa_status fa_bwd_fused(const fa_problem* prob, const void* q, const int64_t* sq,
+                              const void* k, const int64_t* sk, const void* v,
+                              const int64_t* sv, const void* dout, const int64_t* sdo,
+                              const float* lse, const float* delta, void* dq,
+                              const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
+                              const int64_t* sdv, float* dq_accum, size_t workspace_bytes,
+                              cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the

@@ -65,9 +65,10 @@ def tolerance(w: Workload, key: str, ref: np.ndarray, mag: np.ndarray | None = N
     return atol, 0.0
 
 
-def run_gpu(w: Workload, inputs=None, backward: bool = True):
-    """Runs fa_fwd (+ fa_bwd_preprocess + fa_bwd) on cuda:0 with NaN-filled
-    outputs; returns (inputs on CPU, dict of CPU float64 numpy outputs)."""
+def run_gpu(w: Workload, inputs=None, backward: bool = True, fused: bool = False):
+    """Runs fa_fwd (+ fa_bwd_preprocess + fa_bwd, or fa_bwd_fused when `fused`)
+    on cuda:0 with NaN-filled outputs; returns (inputs on CPU, dict of CPU
+    float64 numpy outputs)."""
     if inputs is None:
         inputs = make_inputs(w, "cpu", with_grad_out=backward)
     q, k, v, do = inputs
@@ -93,7 +94,13 @@ def run_gpu(w: Workload, inputs=None, backward: bool = True):
         dq = torch.full((B, H, N, D), float("nan"), dtype=dt, device=dev)
         dk = torch.full_like(dq, float("nan"))
         dv = torch.full_like(dq, float("nan"))
-        fa.bwd(qd, kd, vd, dod, lse, delta, dq, dk, dv, w.causal, w.scale)
+        if fused:
+            nbytes = fa.workspace_bytes(qd, kd, w.causal, w.scale)
+            ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device=dev)
+            fa.bwd_fused(qd, kd, vd, dod, lse, delta, dq, dk, dv, w.causal, w.scale,
+                         workspace=ws)
+        else:
+            fa.bwd(qd, kd, vd, dod, lse, delta, dq, dk, dv, w.causal, w.scale)
         out.update(delta=delta, dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     status = fa.device_status()

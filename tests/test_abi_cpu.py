@@ -99,3 +99,36 @@ def test_preprocess_and_bwd_validation(lib):
                       st, st, st, st, st, st, bad, 1, 0.125, 2, None) == 5
     assert lib.fa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, 1, 2, 64, 64,
                       st, st, st, st, st, st, st, 1, 0.125, 2, None) == 1
+
+
+def _problem(B=2, Hq=4, Hkv=2, Nq=300, Nk=200, D=64, dtype=2):
+    pr = fa.Problem()
+    pr.B, pr.Hq, pr.Hkv, pr.Nq, pr.Nk, pr.D = B, Hq, Hkv, Nq, Nk, D
+    pr.scale, pr.dtype = 0.125, dtype
+    return pr
+
+
+def test_fused_workspace_size_and_validation(lib):
+    """fa_bwd_fused_workspace_bytes: fp32 rows of 64 (D <= 64) or 128 floats
+    per query row of every query head; 0 for an invalid problem.  fa_bwd_fused
+    rejects fp32 inputs, a NULL / unaligned / short workspace before any
+    device work."""
+    pr = _problem()
+    assert lib.fa_bwd_fused_workspace_bytes(ctypes.byref(pr)) == 2 * 4 * 300 * 64 * 4
+    for D, w in ((16, 64), (32, 64), (64, 64), (128, 128)):
+        pr = _problem(D=D)
+        assert lib.fa_bwd_fused_workspace_bytes(ctypes.byref(pr)) == 2 * 4 * 300 * w * 4
+    pr = _problem(Hkv=3)                                  # Hq % Hkv != 0
+    assert lib.fa_bwd_fused_workspace_bytes(ctypes.byref(pr)) == 0
+    assert lib.fa_bwd_fused_workspace_bytes(None) == 0
+
+    def call(pr, ws=FAKE, nbytes=1 << 30):
+        st = S(0, 0, 64, 1)
+        return lib.fa_bwd_fused(ctypes.byref(pr), FAKE, st, FAKE, st, FAKE, st, FAKE, st,
+                                FAKE, FAKE, FAKE, st, FAKE, st, FAKE, st, ws, nbytes, None)
+
+    assert call(_problem(dtype=0)) == 4                   # FA_ERR_DTYPE: fp32
+    assert call(_problem(), ws=None) == 1                 # FA_ERR_NULL
+    assert call(_problem(), ws=FAKE + 4) == 6             # FA_ERR_ALIGN
+    need = 2 * 4 * 300 * 64 * 4
+    assert call(_problem(), nbytes=need - 16) == 12       # FA_ERR_SCRATCH

@@ -35,9 +35,10 @@ def _kw(w: GeneralWorkload, cu_q, cu_k):
     return kw
 
 
-def run_general(w: GeneralWorkload):
-    """Forward, preprocess and backward through the C ABI; outputs start as NaN
-    so any element left unwritten fails the comparison."""
+def run_general(w: GeneralWorkload, fused: bool = False):
+    """Forward, preprocess and backward (fa_bwd_ex, or fa_bwd_fused when
+    `fused`) through the C ABI; outputs start as NaN so any element left
+    unwritten fails the comparison."""
     q, k, v, do, cu_q, cu_k = make_general_inputs(w)
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
     cq = cu_q.to(DEV) if cu_q is not None else None
@@ -52,7 +53,13 @@ def run_general(w: GeneralWorkload):
     dq = torch.full_like(qd, float("nan"))
     dk = torch.full_like(kd, float("nan"))
     dv = torch.full_like(vd, float("nan"))
-    fa.bwd_ex(qd, kd, vd, dod, lse, delta, dq, dk, dv, w.causal, w.scale, **kw)
+    if fused:
+        nbytes = fa.workspace_bytes(qd, kd, w.causal, w.scale, **kw)
+        ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device=DEV)
+        fa.bwd_fused(qd, kd, vd, dod, lse, delta, dq, dk, dv, w.causal, w.scale, workspace=ws,
+                     **kw)
+    else:
+        fa.bwd_ex(qd, kd, vd, dod, lse, delta, dq, dk, dv, w.causal, w.scale, **kw)
     torch.cuda.synchronize()
     status = fa.device_status()
     assert status == 0, fa.STATUS_NAMES.get(status, status)
@@ -61,22 +68,32 @@ def run_general(w: GeneralWorkload):
     return (q, k, v, do, cu_q, cu_k), got
 
 
-def reference(w: GeneralWorkload, inputs):
+def reference(w: GeneralWorkload, inputs, magnitudes: bool = False):
     q, k, v, do, cu_q, cu_k = inputs
     if w.packed:
         return oracle.varlen_fwd_bwd(q, k, v, do, cu_q.numpy(), cu_k.numpy(), w.causal, w.scale,
-                                     p=w.dropout_p, seed=w.drop_seed, offset=w.drop_offset)
+                                     p=w.dropout_p, seed=w.drop_seed, offset=w.drop_offset,
+                                     magnitudes_too=magnitudes)
     dr = oracle.dropout_params(w.dropout_p, w.drop_seed, w.drop_offset)
-    return oracle.fwd_bwd(q, k, v, do, w.causal, w.scale, dr)
+    ref = oracle.fwd_bwd(q, k, v, do, w.causal, w.scale, dr)
+    if magnitudes:
+        m = oracle.magnitudes(q, k, v, do, w.causal, w.scale, dr)
+        ref.update({key + "_abs": val for key, val in m.items()})
+    return ref
 
 
 def compare(w: GeneralWorkload, inputs, got):
     """Max-abs tolerance of the unit-normal workloads, plus the final rounding
     of each output to the input type (half an ulp: u * |ref|).  A sum over many
     rows (e.g. dV of a key that every query attends to with weight 1) grows
-    past 1, where that rounding alone exceeds the absolute term."""
-    ref = reference(w, inputs)
-    tol = (TOL[w.dtype], UNIT_ROUNDOFF.get(w.dtype, 0.0))
+    past 1, where that rounding alone exceeds the absolute term.  For fp16 and
+    bf16 each element also gets u * m, m the oracle's magnitude sum of the
+    terms of its product (the componentwise bound for rounding P or dS to the
+    input type before the product): a key attended by hundreds of
+    (query, head) pairs, as with multi-query heads, sums that many rounded
+    terms."""
+    u = UNIT_ROUNDOFF.get(w.dtype, 0.0)
+    ref = reference(w, inputs, magnitudes=u > 0)
     for key in ("o", "lse", "dq", "dk", "dv"):
         g, r = got[key], ref[key]
         if key == "lse":
@@ -86,7 +103,8 @@ def compare(w: GeneralWorkload, inputs, got):
             g, r = np.where(inf, 0.0, g), np.where(inf, 0.0, r)
             check(f"{w.name}:{key}", g, r, TOL[w.dtype])
             continue
-        check(f"{w.name}:{key}", g, r, tol)
+        atol = TOL[w.dtype] + u * ref[key + "_abs"] if u > 0 else TOL[w.dtype]
+        check(f"{w.name}:{key}", g, r, (atol, u))
 
 
 # --------------------------------------------------------------- Nq != Nk
