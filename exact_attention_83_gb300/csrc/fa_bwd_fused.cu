@@ -22,20 +22,30 @@
 // The elementwise warps write each rounded dS^T row twice: into TMEM (the A
 // operand of dK) and into a 128 x 128 shared-memory tile (key rows, query
 // columns, 128-byte swizzle), which the dQ product reads as an MN-major A
-// operand with the key tile K_j as an MN-major B operand.  dQ_i lands in TMEM
-// (at D = 128 in the dP^T columns, which are free once dK_i has read dS^T;
-// the next dP^T waits until the elementwise warps have read dQ_i out); each
-// warpgroup copies its half of the columns, 32 at a time, into its half of the
-// dS tile (fp32, rows of 128 bytes, swizzled) and one thread issues the TMA
-// reduction of that 128 x 32 box into the workspace.
+// operand with the key tile K_j as an MN-major B operand.  At D = 128 that
+// tile is the dO_i slot, whose last reader, dV_i, has completed by then: the
+// Q ring keeps three slots.  dQ_i lands in TMEM (at D = 128 in the dP^T
+// columns, free once dK_i has read dS^T); each warpgroup copies its half of
+// the columns, 32 at a time, into free shared memory (fp32 rows of 128 bytes,
+// swizzled; at D = 128 the dO_i and Q_i slots, whose last readers dQ_i and
+// dK_i have completed) and one thread issues the TMA reduction of that
+// 128 x 32 box.  That thread releases the slots to the producer once the
+// reductions have read them.
+//
+// Schedule per step i (MMA issue order and elementwise order):
+//   MMA:          dK_i, dQ_i, dV_{i+1}, dP^T_{i+1}, S^T_{i+2}
+//   elementwise:  dS_i, P_{i+1}, dQ_i out of TMEM and into the workspace
+// so P_{i+1} is formed while dK_i and dQ_i run, dV_{i+1} follows dQ_i without
+// waiting for the dQ read-out, and at D = 128 only dP^T_{i+1} (which reuses
+// the dQ columns) waits for it.
 //
 // The workspace is fp32 [B, Hq, Nq, Dw] (packed: [Hq, total_q, Dw]), Dw = 64
 // for head dimensions up to 64 and 128 otherwise; the caller's buffer is
-// zeroed on the stream first.  Rows past a sequence's last query receive
-// exact zeros (their probabilities are 0), keys past its last key are masked.
+// zeroed on the stream first.  Query rows past a sequence's end receive exact
+// zeros (their probabilities are 0) and keys past its end are masked.
 //
 // Every mbarrier wait is bounded (tc_common.cuh); the elementwise warpgroups
-// hand their staging tile to the TMA thread through mbarriers as well, so a
+// hand their staging boxes to the TMA thread through mbarriers as well, so a
 // timeout anywhere ends every role.  Before exit the issuing threads wait for
 // their reductions to complete.
 
@@ -54,14 +64,18 @@ struct FusedCfg {
   static constexpr int TILE = DC * CHUNK;        // bytes of one 128 x D tile
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int NQ = D == 128 ? 2 : 3;    // Q ring slots
+  static constexpr int NQ = 3;                   // Q ring slots
   static constexpr int ND = 2;                   // dO (+ L, Delta) ring slots
   static constexpr int DSLOT = TILE + 1024;      // dO | L*log2e | Delta
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_Q = 2 * TILE;
   static constexpr int OFF_DO = OFF_Q + NQ * TILE;
-  static constexpr int OFF_DS = OFF_DO + ND * DSLOT;   // dS^T tile: one chunk per warpgroup
-  static constexpr int OFF_BAR = OFF_DS + 2 * CHUNK;
+  // D = 128: dS lives in the dO slot and dQ is staged in the dO and Q slots.
+  // D = 64: a dS tile and a staging area of their own (two chunks each).
+  static constexpr bool IN_SLOTS = D == 128;
+  static constexpr int OFF_DS = OFF_DO + ND * DSLOT;
+  static constexpr int OFF_ST = OFF_DS + (IN_SLOTS ? 0 : 2 * CHUNK);
+  static constexpr int OFF_BAR = OFF_ST + (IN_SLOTS ? 0 : 2 * CHUNK);
   static constexpr int BAR_BYTES = 256;
   static constexpr int MAX_PAD = D == 128 ? 768 : 1024;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + MAX_PAD;
@@ -69,6 +83,9 @@ struct FusedCfg {
   static constexpr uint32_t COL_DQ = D == 128 ? COL_DPT : 384;
   static constexpr int DW = D;                   // workspace row width (floats)
   static constexpr int ROUNDS = D / 64;          // 32-column boxes per warpgroup and tile
+  // arrivals that release a Q or dO slot: the MMA commit, plus at D = 128 the
+  // two threads whose reductions read dQ out of it
+  static constexpr uint32_t RELEASE = IN_SLOTS ? 3 : 1;
 };
 
 struct FusedArgs {
@@ -156,6 +173,77 @@ __device__ __forceinline__ float* stage_row(uint8_t* smem, int t, int row) {
 }
 __device__ __forceinline__ int stage_chunk(int c, int row) { return c ^ (row & 7); }
 
+// What the elementwise threads need to form P for one step.
+struct ProbStep {
+  const float* L2s;       // L * log2(e) of this half's 64 queries
+  bool diag;              // causal diagonal tile
+  uint32_t bhq;           // flat query head (dropout numbering)
+  int64_t qbase;          // first query (within the sequence) of this half
+};
+
+// P^T for this thread's key and its half's 64 queries: exp2(c*S - L*log2 e),
+// masked (keys past the sequence, causal diagonal), dropout keep bits into
+// `keep` (bit q: query qbase + q kept), and the rounded (dropped, rescaled)
+// P^T stored back over the scores for dV.
+template <typename T, bool DROP>
+__device__ __forceinline__ void form_probs(float (&p)[64], uint64_t& keep, uint32_t taddr,
+                                           const ProbStep& s, float c, bool key_in, int hf, int row,
+                                           int lane, int64_t key, const Dropout& drop) {
+  tmem_ld64f(taddr, p);
+#pragma unroll
+  for (int q = 0; q < 64; q += 4) {
+    const float4 l4 = *reinterpret_cast<const float4*>(s.L2s + q);
+    p[q] = ex2(fmaf(p[q], c, -l4.x));
+    p[q + 1] = ex2(fmaf(p[q + 1], c, -l4.y));
+    p[q + 2] = ex2(fmaf(p[q + 2], c, -l4.z));
+    p[q + 3] = ex2(fmaf(p[q + 3], c, -l4.w));
+  }
+  if (!key_in) {
+    // a key past the sequence (packed rows of the next one): no weight
+#pragma unroll
+    for (int q = 0; q < 64; ++q) p[q] = 0.f;
+  }
+  if (s.diag) {
+    // query (64*hf + q) attends to this key only if it is not earlier
+#pragma unroll
+    for (int q = 0; q < 64; ++q)
+      if (64 * hf + q < row) p[q] = 0.f;
+  }
+  keep = 0;
+  if constexpr (DROP) {
+    // The eight lanes of an octet hold eight consecutive keys, which one
+    // generator call covers for one query: lane e of the octet draws for
+    // query 8t + e, the octet exchanges the eight 8-bit results, and each
+    // lane keeps the bit of its own key.
+    const uint32_t jg = static_cast<uint32_t>(key >> 3);
+    const int e = lane & 7;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      uint64_t x = static_cast<uint64_t>(
+                       keep8(drop, jg, static_cast<uint32_t>(s.qbase + 8 * t + e), s.bhq))
+                   << (8 * e);
+      x |= __shfl_xor_sync(0xffffffffu, x, 1);
+      x |= __shfl_xor_sync(0xffffffffu, x, 2);
+      x |= __shfl_xor_sync(0xffffffffu, x, 4);
+      const uint64_t y = (x >> e) & 0x0101010101010101ull;
+      keep |= ((y * 0x0102040810204080ull) >> 56) << (8 * t);
+    }
+  }
+  uint32_t w[32];
+#pragma unroll
+  for (int q = 0; q < 32; ++q) {
+    if constexpr (DROP) {
+      const float z0 = ((keep >> (2 * q)) & 1u) ? drop.rscale : 0.f;
+      const float z1 = ((keep >> (2 * q + 1)) & 1u) ? drop.rscale : 0.f;
+      w[q] = pack2<T>(p[2 * q] * z0, p[2 * q + 1] * z1);
+    } else {
+      w[q] = pack2<T>(p[2 * q], p[2 * q + 1]);
+    }
+  }
+  tmem_st32(taddr, w);
+  tmem_wait_st();
+}
+
 template <typename T, int D, bool DROP>
 __global__ void __launch_bounds__(320, 1)
     bwd_fused_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -163,7 +251,7 @@ __global__ void __launch_bounds__(320, 1)
                         const __grid_constant__ CUtensorMap tmdq, const FusedArgs a) {
   using C = FusedCfg<D>;
   static_assert(C::SMEM <= 232448, "shared memory per block");
-  static_assert(2 * 128 * D * 4 <= C::OFF_DS, "cluster staging fits below the dS tile");
+  static_assert(2 * 128 * D * 4 <= C::OFF_DO, "cluster staging fits below the dO slots");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad > static_cast<uint32_t>(C::MAX_PAD)) {   // never expected: report, do nothing
@@ -174,12 +262,13 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sQ = smem + C::OFF_Q;            // slot s: Q tile
-  uint8_t* sD = smem + C::OFF_DO;           // slot s: dO tile | L2 (128 f32) | Delta (128 f32)
-  uint8_t* sDS = smem + C::OFF_DS;          // dS^T (16-bit) / dQ staging (fp32), chunk per warpgroup
+  uint8_t* sD = smem + C::OFF_DO;           // slot s: dO tile (then dS at D = 128) | L2 | Delta
+  uint8_t* sDS = smem + C::OFF_DS;          // D = 64: dS tile
+  uint8_t* sST = smem + C::OFF_ST;          // D = 64: dQ staging boxes
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   Ctl* ctl = reinterpret_cast<Ctl*>(bars + 28);
   const uint32_t b_kv = smem_u32(&bars[0]);
-  const uint32_t b_qfull0 = smem_u32(&bars[1]);                  // + 8 * Q slot (<= 3)
+  const uint32_t b_qfull0 = smem_u32(&bars[1]);                  // + 8 * Q slot (3)
   const uint32_t b_qempty0 = smem_u32(&bars[4]);                 // + 8 * Q slot
   const uint32_t b_dfull0 = smem_u32(&bars[7]);                  // + 8 * dO slot (2)
   const uint32_t b_dempty0 = smem_u32(&bars[9]);                 // + 8 * dO slot
@@ -190,9 +279,12 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t b_accdone = smem_u32(&bars[17]);
   const uint32_t b_mmadone = smem_u32(&bars[18]);
   const uint32_t b_dqfull = smem_u32(&bars[19]);                 // dQ_i is in TMEM
-  const uint32_t b_dqread = smem_u32(&bars[20]);                 // dQ_i has been read out (D = 128)
-  const uint32_t b_staged0 = smem_u32(&bars[21]);                // + 8 * half: staging box written
-  const uint32_t b_stfree0 = smem_u32(&bars[23]);                // + 8 * half: staging box read by TMA
+  const uint32_t b_dqread = smem_u32(&bars[20]);                 // dQ_i read out (D = 128)
+  const uint32_t b_dvdone = smem_u32(&bars[21]);                 // dV_i has completed
+  // + 8 * (2 * half + round): box written.  One barrier per round, so a warp
+  // that is already writing the next round's box cannot complete this one.
+  const uint32_t b_staged0 = smem_u32(&bars[22]);
+  const uint32_t b_stfree0 = smem_u32(&bars[26]);                // + 8 * half (D = 64): box read
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = a.split;
@@ -234,24 +326,26 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(b_kv, 1);
     for (int s = 0; s < C::NQ; ++s) {
       mbar_init(b_qfull0 + 8 * s, 1);
-      mbar_init(b_qempty0 + 8 * s, 1);
+      mbar_init(b_qempty0 + 8 * s, C::RELEASE);
     }
     for (int s = 0; s < C::ND; ++s) {
       mbar_init(b_dfull0 + 8 * s, 32);
-      mbar_init(b_dempty0 + 8 * s, 1);
+      mbar_init(b_dempty0 + 8 * s, C::RELEASE);
     }
     mbar_init(b_sfull, 1);
     mbar_init(b_dpfull, 1);
     for (int h = 0; h < 2; ++h) {
       mbar_init(b_pready0 + 8 * h, 128);
       mbar_init(b_dsready0 + 8 * h, 128);
-      mbar_init(b_staged0 + 8 * h, 128);
+      mbar_init(b_staged0 + 8 * (2 * h), 128);
+      mbar_init(b_staged0 + 8 * (2 * h + 1), 128);
       mbar_init(b_stfree0 + 8 * h, 1);
     }
     mbar_init(b_accdone, 1);
     mbar_init(b_mmadone, 1);
     mbar_init(b_dqfull, 1);
     mbar_init(b_dqread, 256);
+    mbar_init(b_dvdone, 1);
     ctl->abort = 0;
     mbar_fence_init();
   }
@@ -269,8 +363,9 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ producer
     // Lane 0 issues the TMA copies: K and V once, then per step Q into its Q
     // slot and dO into its dO slot, where all 32 lanes also stage L * log2(e)
-    // and Delta (4 rows per lane; rows past the sequence get L = +inf, so
-    // their probabilities are exactly 0, and Delta = 0).
+    // and Delta (4 rows per lane, read from global memory before the slot is
+    // free; rows past the sequence get L = +inf, so their probabilities are
+    // exactly 0, and Delta = 0).
     if (lane == 0) {
       tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
@@ -306,6 +401,14 @@ __global__ void __launch_bounds__(320, 1)
       }
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
+      float lv[4], dv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int64_t q = q0 + lane * 4 + t;
+        const int64_t li = lse_index(a.g, sv, hq, q);
+        lv[t] = q < Nq ? a.lse[li] * kLog2e : INFINITY;
+        dv[t] = q < Nq ? a.delta[li] : 0.f;
+      }
       const int ds = it % C::ND;
       const uint32_t dr = static_cast<uint32_t>(it / C::ND);
       if (dr > 0 && !(ok = wait_warp(b_dempty0 + 8 * ds, (dr - 1) & 1, ctl, a.status, a.timeout_ns)))
@@ -315,10 +418,8 @@ __global__ void __launch_bounds__(320, 1)
       float* Ds = L2s + 128;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const int64_t q = q0 + lane * 4 + t;
-        const int64_t li = lse_index(a.g, sv, hq, q);
-        L2s[lane * 4 + t] = q < Nq ? a.lse[li] * kLog2e : INFINITY;
-        Ds[lane * 4 + t] = q < Nq ? a.delta[li] : 0.f;
+        L2s[lane * 4 + t] = lv[t];
+        Ds[lane * 4 + t] = dv[t];
       }
       if (lane == 0) {
         mbar_arrive_expect_tx(b_dfull0 + 8 * ds, C::TILE);
@@ -343,11 +444,6 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // Per step: dV_i (per half), S^T_{i+1}, dK_i (per half), dQ_i, then
-    // dP^T_{i+1}.  At D = 128 dQ_i occupies the dP^T columns, so dP^T_{i+1}
-    // waits until the elementwise warps have read dQ_i; at D = 64 dQ has
-    // columns of its own, and the dS_{i+1} arrivals already imply that dQ_i
-    // was read (each elementwise thread reads dQ_i before it computes dS_{i+1}).
     if (lane == 0) {
       const uint32_t idS = idesc_f16<T>(128, C::BT, false, false);
       const uint32_t idG = idesc_f16<T>(128, D, false, true);
@@ -359,7 +455,7 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t dQm = sdesc_sw128(smem_u32(sQ), C::CHUNK, 1024);    // MN-major views
       const uint64_t dDm = sdesc_sw128(smem_u32(sD), C::CHUNK, 1024);
       const uint64_t dKm = sdesc_sw128(smem_u32(sK), C::CHUNK, 1024);
-      const uint64_t dSm = sdesc_sw128(smem_u32(sDS), C::CHUNK, 1024);
+      const uint64_t dSm = sdesc_sw128(smem_u32(C::IN_SLOTS ? sD : sDS), C::CHUNK, 1024);
       auto issue_ST = [&](int qs) {   // S^T = K Q^T
         const uint64_t q = dQk + static_cast<uint64_t>((qs * C::TILE) >> 4);
 #pragma unroll
@@ -378,6 +474,21 @@ __global__ void __launch_bounds__(320, 1)
         }
         mma_commit(b_dpfull);
       };
+      // dV += P^T_j dO_j (per half as P^T is ready; B: dO read MN-major, N = d)
+      auto issue_DV = [&](int j) -> bool {
+        const uint64_t mdo = dDm + static_cast<uint64_t>(((j % C::ND) * C::DSLOT) >> 4);
+        for (int h = 0; h < 2; ++h) {
+          if (!wait_bounded(b_pready0 + 8 * h, j & 1, ctl, a.status, a.timeout_ns)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + C::COL_DV, tmem + C::COL_ST + 64 * h + 8 * kk,
+                   mdo + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
+                   (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(b_dvdone);
+        return true;
+      };
       bool ok = wait_bounded(b_kv, 0, ctl, a.status, a.timeout_ns) &&
                 wait_bounded(b_qfull0, 0, ctl, a.status, a.timeout_ns) &&
                 wait_bounded(b_dfull0, 0, ctl, a.status, a.timeout_ns);
@@ -385,30 +496,16 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         issue_ST(0);
         issue_DPT(0);
+        ok = issue_DV(0);
+      }
+      if (ok && n > 1) {
+        if ((ok = wait_bounded(b_qfull0 + 8, 0, ctl, a.status, a.timeout_ns))) {
+          tc_fence_after();
+          issue_ST(1);
+        }
       }
       for (int it = 0; ok && it < n; ++it) {
         const int qs = it % C::NQ, ds = it % C::ND;
-        const bool next = it + 1 < n;
-        const int qs1 = (it + 1) % C::NQ, ds1 = (it + 1) % C::ND;
-        // dV += P^T dO (B: this tile's dO read MN-major, N = d)
-        const uint64_t mdo = dDm + static_cast<uint64_t>((ds * C::DSLOT) >> 4);
-        for (int h = 0; ok && h < 2; ++h) {
-          if (!(ok = wait_bounded(b_pready0 + 8 * h, it & 1, ctl, a.status, a.timeout_ns))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + C::COL_DV, tmem + C::COL_ST + 64 * h + 8 * kk,
-                   mdo + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
-                   (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
-        }
-        if (!ok) break;
-        if (next) {
-          if (!(ok = wait_bounded(b_qfull0 + 8 * qs1, ((it + 1) / C::NQ) & 1, ctl, a.status,
-                                  a.timeout_ns)))
-            break;
-          tc_fence_after();
-          issue_ST(qs1);
-        }
         // dK += dS^T Q (B: this tile's Q read MN-major)
         const uint64_t mq = dQm + static_cast<uint64_t>((qs * C::TILE) >> 4);
         for (int h = 0; ok && h < 2; ++h) {
@@ -421,25 +518,39 @@ __global__ void __launch_bounds__(320, 1)
                    (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        mma_commit(b_qempty0 + 8 * qs);   // Q_i and dO_i have no reader after dK_i
-        mma_commit(b_dempty0 + 8 * ds);
-        // dQ_i = dS_i K: A = dS from the shared tile (M = query, MN-major),
+        mma_commit(b_qempty0 + 8 * qs);   // Q_i has no reader after dK_i
+        // dQ_i = dS_i K: A = dS from shared memory (M = query, MN-major),
         // B = K (N = d, MN-major); 16 keys per product.
+        const uint64_t dsm =
+            dSm + (C::IN_SLOTS ? static_cast<uint64_t>((ds * C::DSLOT) >> 4) : 0ull);
 #pragma unroll
         for (int kk = 0; kk < C::BT / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>((kk * 16 * 128) >> 4);
-          mma_ss(tmem + C::COL_DQ, dSm + off, dKm + off, idQ, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::COL_DQ, dsm + off, dKm + off, idQ, kk > 0 ? 1u : 0u);
         }
         mma_commit(b_dqfull);
-        if (next) {
-          if constexpr (C::COL_DQ == C::COL_DPT) {
-            if (!(ok = wait_bounded(b_dqread, it & 1, ctl, a.status, a.timeout_ns))) break;
-          }
+        mma_commit(b_dempty0 + 8 * ds);   // dO_i / dS_i have no reader after dQ_i
+        if (it + 1 < n) {
+          const int ds1 = (it + 1) % C::ND;
           if (!(ok = wait_bounded(b_dfull0 + 8 * ds1, ((it + 1) / C::ND) & 1, ctl, a.status,
                                   a.timeout_ns)))
             break;
           tc_fence_after();
+          if (!(ok = issue_DV(it + 1))) break;
+          if constexpr (C::COL_DQ == C::COL_DPT) {
+            // dQ_i occupies the dP^T columns until the elementwise warps read it
+            if (!(ok = wait_bounded(b_dqread, it & 1, ctl, a.status, a.timeout_ns))) break;
+            tc_fence_after();
+          }
           issue_DPT(ds1);
+          if (it + 2 < n) {
+            const int qs2 = (it + 2) % C::NQ;
+            if (!(ok = wait_bounded(b_qfull0 + 8 * qs2, ((it + 2) / C::NQ) & 1, ctl, a.status,
+                                    a.timeout_ns)))
+              break;
+            tc_fence_after();
+            issue_ST(qs2);                // P^T_{i+1} was read by dV_{i+1}, issued before
+          }
         }
       }
       if (ok) mma_commit(b_accdone);
@@ -455,133 +566,93 @@ __global__ void __launch_bounds__(320, 1)
     const bool key_in = key < Nk;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const bool elected = quarter == 0 && lane == 0;   // issues this warpgroup's reductions
-    const uint32_t chunk = smem_u32(sDS + hf * C::CHUNK);
-    const uint32_t b_staged = b_staged0 + 8 * hf, b_stfree = b_stfree0 + 8 * hf;
+    const uint32_t b_staged = b_staged0 + 16 * hf, b_stfree = b_stfree0 + 8 * hf;
     const float c = a.c;
-    uint32_t nst = 0, nfree = 0;   // reductions issued from / known to have read the chunk
-    // Makes the chunk writable: the reduction issued last has read it.
-    auto chunk_free = [&]() -> bool {
-      if (nfree == nst) return true;
-      if (elected) {
-        bulk_wait_read_all();
-        mbar_arrive(b_stfree);
-      }
-      nfree = nst;
-      return wait_warp(b_stfree, (nst - 1) & 1, ctl, a.status, a.timeout_ns);
+    auto prob_step = [&](int it) {
+      ProbStep s;
+      const int ds = it % C::ND;
+      s.L2s = reinterpret_cast<const float*>(sD + ds * C::DSLOT + C::TILE) + 64 * hf;
+      const int i = i0 + it % per;
+      s.diag = a.causal && i == kt;
+      s.bhq = static_cast<uint32_t>(bseq * a.g.Hq + hk * a.g.G + g0 + it / per);
+      s.qbase = static_cast<int64_t>(i) * C::BT + 64 * hf;
+      return s;
     };
-    bool ok = true;
-    for (int it = 0; it < n; ++it) {
-      const int i = i0 + it % per, ds = it % C::ND;
-      const int32_t hq = static_cast<int32_t>(hk * a.g.G + g0 + it / per);
-      if (!(ok = wait_warp(b_sfull, it & 1, ctl, a.status, a.timeout_ns))) break;
+    float p[64];
+    uint64_t keep = 0;
+    bool ok = wait_warp(b_sfull, 0, ctl, a.status, a.timeout_ns) &&
+              wait_warp(b_dfull0, 0, ctl, a.status, a.timeout_ns);
+    if (ok) {
       // the dO slot's arrival also publishes the staged L and Delta
-      if (!(ok = wait_warp(b_dfull0 + 8 * ds, (it / C::ND) & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
-      const float* L2s = reinterpret_cast<const float*>(sD + ds * C::DSLOT + C::TILE) + 64 * hf;
-      const float* Ds = L2s + 128;
-      float p[64];
-      tmem_ld64f(lane_base + C::COL_ST + 64 * hf, p);
-#pragma unroll
-      for (int q = 0; q < 64; q += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(L2s + q);
-        p[q] = ex2(fmaf(p[q], c, -l4.x));
-        p[q + 1] = ex2(fmaf(p[q + 1], c, -l4.y));
-        p[q + 2] = ex2(fmaf(p[q + 2], c, -l4.z));
-        p[q + 3] = ex2(fmaf(p[q + 3], c, -l4.w));
-      }
-      if (!key_in) {
-        // a key past the sequence (packed rows of the next one): no weight
-#pragma unroll
-        for (int q = 0; q < 64; ++q) p[q] = 0.f;
-      }
-      if (a.causal && i == kt) {
-        // diagonal tile: query (64*hf + q) attends to this key only if it is not earlier
-#pragma unroll
-        for (int q = 0; q < 64; ++q)
-          if (64 * hf + q < row) p[q] = 0.f;
-      }
-      // Dropout keep bits: bit q set iff weight (query 64*hf + q of this
-      // tile, this key) is kept.  The eight lanes of an octet hold eight
-      // consecutive keys, which one generator call covers for one query: lane
-      // e of the octet draws for query 8t + e, the octet exchanges the eight
-      // 8-bit results, and each lane keeps the bit of its own key.
-      uint64_t keep = 0;
-      if constexpr (DROP) {
-        const uint32_t bhq = static_cast<uint32_t>(bseq * a.g.Hq + hq);
-        const uint32_t jg = static_cast<uint32_t>(key >> 3);
-        const int e = lane & 7;
-        const int64_t qbase = static_cast<int64_t>(i) * C::BT + 64 * hf;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          uint64_t x = static_cast<uint64_t>(
-                           keep8(a.drop, jg, static_cast<uint32_t>(qbase + 8 * t + e), bhq))
-                       << (8 * e);
-          x |= __shfl_xor_sync(0xffffffffu, x, 1);
-          x |= __shfl_xor_sync(0xffffffffu, x, 2);
-          x |= __shfl_xor_sync(0xffffffffu, x, 4);
-          const uint64_t y = (x >> e) & 0x0101010101010101ull;
-          keep |= ((y * 0x0102040810204080ull) >> 56) << (8 * t);
-        }
-      }
-      {
-        uint32_t w[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          if constexpr (DROP) {
-            const float z0 = ((keep >> (2 * q)) & 1u) ? a.drop.rscale : 0.f;
-            const float z1 = ((keep >> (2 * q + 1)) & 1u) ? a.drop.rscale : 0.f;
-            w[q] = pack2<T>(p[2 * q] * z0, p[2 * q + 1] * z1);
-          } else {
-            w[q] = pack2<T>(p[2 * q], p[2 * q + 1]);
-          }
-        }
-        tmem_st32(lane_base + C::COL_ST + 64 * hf, w);
-      }
-      tmem_wait_st();
+      form_probs<T, DROP>(p, keep, lane_base + C::COL_ST + 64 * hf, prob_step(0), c, key_in, hf,
+                          row, lane, key, a.drop);
       tc_fence_before();
       mbar_arrive(b_pready0 + 8 * hf);
-
+    }
+    for (int it = 0; ok && it < n; ++it) {
+      const int i = i0 + it % per, ds = it % C::ND, qs = it % C::NQ;
+      const int32_t hq = static_cast<int32_t>(hk * a.g.G + g0 + it / per);
+      // ---- dS_i (at D = 128 written over dO_i below, so dV_i must be done)
       if (!(ok = wait_warp(b_dpfull, it & 1, ctl, a.status, a.timeout_ns))) break;
-      tc_fence_after();
-      float dp[64];
-      tmem_ld64f(lane_base + C::COL_DPT + 64 * hf, dp);
-      if constexpr (DROP) {
-        // dS = P o (Z o dP - Delta), Z = keep / (1 - p)
-#pragma unroll
-        for (int q = 0; q < 64; ++q) {
-          const float z = ((keep >> q) & 1u) ? a.drop.rscale : 0.f;
-          dp[q] = p[q] * fmaf(z, dp[q], -Ds[q]);
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 64; q += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(Ds + q);
-          dp[q] = p[q] * (dp[q] - d4.x);
-          dp[q + 1] = p[q + 1] * (dp[q + 1] - d4.y);
-          dp[q + 2] = p[q + 2] * (dp[q + 2] - d4.z);
-          dp[q + 3] = p[q + 3] * (dp[q + 3] - d4.w);
-        }
+      if constexpr (C::IN_SLOTS) {
+        if (!(ok = wait_warp(b_dvdone, it & 1, ctl, a.status, a.timeout_ns))) break;
       }
-      uint32_t w[32];
+      tc_fence_after();
+      {
+        const float* Ds = reinterpret_cast<const float*>(sD + ds * C::DSLOT + C::TILE) + 128 +
+                          64 * hf;
+        float dp[64];
+        tmem_ld64f(lane_base + C::COL_DPT + 64 * hf, dp);
+        if constexpr (DROP) {
+          // dS = P o (Z o dP - Delta), Z = keep / (1 - p)
 #pragma unroll
-      for (int q = 0; q < 32; ++q) w[q] = pack2<T>(dp[2 * q], dp[2 * q + 1]);
-      if (!(ok = chunk_free())) break;
-      tmem_st32(lane_base + C::COL_DPT + 64 * hf, w);   // dS^T, A operand of dK
-      // the same row into the shared tile, A operand of dQ (key row `row`,
-      // this warpgroup's 64 queries)
-      st_row_sw128(chunk, row, w);
-      fence_async_smem();
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(b_dsready0 + 8 * hf);
-
-      // dQ_i: this thread holds query row `row` of the tile; warpgroup hf
-      // reduces columns (D/2)*hf .. (D/2)*hf + D/2 - 1, 32 per box.
+          for (int q = 0; q < 64; ++q) {
+            const float z = ((keep >> q) & 1u) ? a.drop.rscale : 0.f;
+            dp[q] = p[q] * fmaf(z, dp[q], -Ds[q]);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 64; q += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(Ds + q);
+            dp[q] = p[q] * (dp[q] - d4.x);
+            dp[q + 1] = p[q + 1] * (dp[q + 1] - d4.y);
+            dp[q + 2] = p[q + 2] * (dp[q + 2] - d4.z);
+            dp[q + 3] = p[q + 3] * (dp[q + 3] - d4.w);
+          }
+        }
+        uint32_t w[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) w[q] = pack2<T>(dp[2 * q], dp[2 * q + 1]);
+        tmem_st32(lane_base + C::COL_DPT + 64 * hf, w);   // dS^T, A operand of dK
+        // the same row into shared memory, A operand of dQ (key row `row`,
+        // this warpgroup's 64 queries)
+        st_row_sw128(smem_u32((C::IN_SLOTS ? sD + ds * C::DSLOT : sDS) + hf * C::CHUNK), row, w);
+        fence_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(b_dsready0 + 8 * hf);
+      }
+      // ---- P_{i+1}, while the tensor cores run dK_i and dQ_i
+      if (it + 1 < n) {
+        if (!(ok = wait_warp(b_sfull, (it + 1) & 1, ctl, a.status, a.timeout_ns))) break;
+        if (!(ok = wait_warp(b_dfull0 + 8 * ((it + 1) % C::ND), ((it + 1) / C::ND) & 1, ctl,
+                             a.status, a.timeout_ns)))
+          break;
+        tc_fence_after();
+        form_probs<T, DROP>(p, keep, lane_base + C::COL_ST + 64 * hf, prob_step(it + 1), c, key_in,
+                            hf, row, lane, key, a.drop);
+        tc_fence_before();
+        mbar_arrive(b_pready0 + 8 * hf);
+      }
+      // ---- dQ_i: this thread holds query row `row` of the tile; warpgroup
+      // hf reduces columns (D/2)*hf .. (D/2)*hf + D/2 - 1, 32 per box
       if (!(ok = wait_warp(b_dqfull, it & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
       uint32_t x[C::ROUNDS][32];
 #pragma unroll
-      for (int r = 0; r < C::ROUNDS; ++r) tmem_ld32(lane_base + C::COL_DQ + (D / 2) * hf + 32 * r, x[r]);
+      for (int r = 0; r < C::ROUNDS; ++r)
+        tmem_ld32(lane_base + C::COL_DQ + (D / 2) * hf + 32 * r, x[r]);
       tmem_wait_ld();
 #pragma unroll
       for (int r = 0; r < C::ROUNDS; ++r) reg_fence32(x[r]);
@@ -589,26 +660,50 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_before();
         mbar_arrive(b_dqread);            // the dP^T columns may be overwritten
       }
+      if constexpr (!C::IN_SLOTS) {
+        // the staging box of the previous step has been read
+        if (it > 0 && !(ok = wait_warp(b_stfree, (it - 1) & 1, ctl, a.status, a.timeout_ns))) break;
+      }
       const int32_t qrow0 = static_cast<int32_t>(sv.q0 + static_cast<int64_t>(i) * C::BT);
       const int32_t plane = static_cast<int32_t>(sv.b * a.g.Hq + hq);
 #pragma unroll
       for (int r = 0; r < C::ROUNDS; ++r) {
-        if (!(ok = chunk_free())) break;
-        st_row_sw128(chunk, row, x[r]);
+        // box r: D = 128: the dO_i / dS_i slot (r = 0) and the Q_i slot
+        // (r = 1), whose readers dQ_i and dK_i have completed; D = 64: the
+        // warpgroup's own staging box
+        uint8_t* box = C::IN_SLOTS ? (r == 0 ? sD + ds * C::DSLOT : sQ + qs * C::TILE) : sST;
+        const uint32_t bx = smem_u32(box + hf * C::CHUNK);
+        st_row_sw128(bx, row, x[r]);
         fence_async_smem();
-        mbar_arrive(b_staged);
+        mbar_arrive(b_staged + 8 * r);
         if (elected) {
-          if (wait_bounded(b_staged, nst & 1, ctl, a.status, a.timeout_ns)) {
+          if (wait_bounded(b_staged + 8 * r, it & 1, ctl, a.status, a.timeout_ns)) {
             const int col = (D / 2) * hf + 32 * r;
-            if (col < a.dreal) tma_reduce_add_3d(&tmdq, chunk, col, qrow0, plane);
+            if (col < a.dreal) tma_reduce_add_3d(&tmdq, bx, col, qrow0, plane);
             bulk_commit();
           }
         }
         __syncwarp();
-        ++nst;
       }
-      if (!ok) break;
+      if (elected) {
+        // release what the reductions read (the other warps of this
+        // warpgroup go on to the next step meanwhile)
+        bulk_wait_read_all();
+        if constexpr (C::IN_SLOTS) {
+          mbar_arrive(b_dempty0 + 8 * ds);
+          mbar_arrive(b_qempty0 + 8 * qs);
+        } else {
+          mbar_arrive(b_stfree);
+        }
+      }
+      __syncwarp();
     }
+    // Every reduction of both warpgroups has completed before any thread
+    // goes on: the cluster epilogue below stages partial sums over the Q
+    // slots, which the last reductions read.  All 256 elementwise threads
+    // reach this barrier (nothing above returns early or waits unbounded).
+    if (elected) bulk_wait_all();
+    asm volatile("bar.sync 1, 256;" ::: "memory");
     if (ok) ok = wait_warp(b_accdone, 0, ctl, a.status, a.timeout_ns);
     ew_ok = ok;
     if (ok) {
@@ -639,9 +734,6 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-    // every reduction issued from this warpgroup's chunk has completed
-    if (elected) bulk_wait_all();
-    __syncwarp();
   }
 
   if (split > 1) {
