@@ -50,10 +50,14 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 1044.8 MB per launch measured on 16 heads,
+    # bwd_dkdv_tc_kernel<bf16,128>: 1043.9 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("dkdv", "2f9a705f49a991fa19d83eae80d507ae1dad56412e29a9f6853de6e9fd1404a8",
-     "long-bf16-B1-H32-N16384-D128-causal"): 2089.5e6,
+    ("dkdv", "45eb81210e5197d9c83406ea153af7a910b22baec831810e6a887713bfbe9fdc",
+     "long-bf16-B1-H32-N16384-D128-causal"): 2087.7e6,
+    # bwd_fused_tc_kernel<bf16,128>: 2927.0 MB per launch measured on 16 heads,
+    # scaled by heads to the 32-head launch
+    ("fused", "3cb1c44daeb804ad2082491ed29352de741ccfbe73df2370d7afb922057d122f",
+     "long-bf16-B1-H32-N16384-D128-causal"): 5854.0e6,
 }
 
 

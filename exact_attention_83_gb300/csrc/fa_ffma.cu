@@ -20,6 +20,13 @@
 // are never visited).  The backward follows the FlashAttention-2 split of
 // "Triton FlashAttention": one kernel per key tile for dK/dV looping over query
 // tiles, one kernel per query tile for dQ, both rebuilding P = exp(S - L).
+//
+// The kernels take the general geometry of fa_internal.h: each CTA resolves
+// its sequence view (packed offsets, lengths Nq != Nk), query head h reads
+// key/value head h / (Hq / Hkv), the dK/dV kernel of a key/value head loops
+// over every query head of its group, and sequences without keys give dQ = 0
+// (and keys nobody attends dK = dV = 0).  With dropout each weight's keep
+// decision comes from the shared Philox mask (keep8), scaled by 1 / (1 - p).
 
 #include "fa_internal.h"
 
