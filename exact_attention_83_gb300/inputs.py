@@ -85,6 +85,26 @@ def make_inputs(w: Workload, device="cpu", with_grad_out: bool = True):
     return tuple(out)
 
 
+def make_inputs_device(w: Workload, device):
+    """(q, k, v, do) for workload ``w`` generated on ``device`` by torch's
+    seeded CUDA generator (i.i.d. N(0,1) in fp32, then cast): for sizes whose
+    host generation would take minutes.  Callers compare against the oracle on
+    slices copied back to the host, so both sides see the same values."""
+    if w.layout != "bhnd":
+        raise ValueError("device generation takes [B, H, N, D] workloads")
+    g = torch.Generator(device)
+    g.manual_seed(w.seed)
+    dt = DTYPES[w.dtype]
+    out = []
+    for name in ("q", "k", "v", "do"):
+        x = torch.randn((w.B, w.H, w.N, w.D), generator=g, dtype=torch.float32, device=device)
+        if name != "do" and w.qkv_scale != 1.0:
+            x.mul_(w.qkv_scale)
+        out.append(x.to(dt))
+        del x
+    return tuple(out)
+
+
 # The workloads the tests and the benchmark run.
 TINY_FP32 = Workload("tiny-fp32-B1-H2-N128-D64", 1, 2, 128, 64, "fp32", False)
 

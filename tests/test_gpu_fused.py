@@ -323,3 +323,14 @@ def test_fused_rejects_fp32_and_short_workspace():
         fa.bwd_fused(qb, qb, qb, qb, lse, lse, qb, qb, qb, False, workspace=ws[1:])
     assert e.value.code == 6
     assert fa.device_status() == 0
+
+
+def test_offsets_beyond_2_31_elements_fused():
+    """The single-pass backward and its workspace (8.6 GB) on tensors of more
+    than 2^31 elements; sampled rows of the last head, wholly past element
+    2^31."""
+    from test_gpu_parity import HUGE, check_huge_heads, run_huge
+    inputs, out = run_huge(HUGE, fused=True)
+    check_huge_heads(HUGE, inputs, out, heads=[(0, 255)])
+    del inputs, out
+    torch.cuda.empty_cache()
