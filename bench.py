@@ -50,10 +50,10 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 1043.9 MB per launch measured on 16 heads,
+    # bwd_dkdv_tc_kernel<bf16,128>: 1044.9 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("dkdv", "45eb81210e5197d9c83406ea153af7a910b22baec831810e6a887713bfbe9fdc",
-     "long-bf16-B1-H32-N16384-D128-causal"): 2087.7e6,
+    ("dkdv", "d60b946c34462a1bd95446af68b9777c0f02575e116286417db2a3dc0e979567",
+     "long-bf16-B1-H32-N16384-D128-causal"): 2089.7e6,
     # bwd_fused_tc_kernel<bf16,128>: 2927.0 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
     ("fused", "3cb1c44daeb804ad2082491ed29352de741ccfbe73df2370d7afb922057d122f",

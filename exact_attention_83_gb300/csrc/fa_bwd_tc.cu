@@ -244,8 +244,9 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ producer
     // Lane 0 issues the TMA copies.  For each query tile: Q into its Q slot,
     // then dO into its dO slot, where all 32 lanes also stage L * log2(e) and
-    // Delta (4 rows per lane).  Rows past N get L = +inf, so their
-    // probabilities are exactly 0, and Delta = 0.
+    // Delta (4 rows per lane, read from global memory before the slot is
+    // free, so their latency overlaps the wait).  Rows past N get L = +inf,
+    // so their probabilities are exactly 0, and Delta = 0.
     if (lane == 0) {
       tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
@@ -283,6 +284,14 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       // dO_i, L, Delta
+      float lv[4], dv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int64_t q = q0 + lane * 4 + t;
+        const int64_t li = lse_index(a.g, sv, hq, q);
+        lv[t] = q < Nq ? a.lse[li] * kLog2e : INFINITY;
+        dv[t] = q < Nq ? a.delta[li] : 0.f;
+      }
       const int ds = it % C::ND;
       const uint32_t dr = static_cast<uint32_t>(it / C::ND);
       if (dr > 0 && !(ok = wait_warp(b_dempty0 + 8 * ds, (dr - 1) & 1, ctl, a.status, a.timeout_ns)))
@@ -292,10 +301,8 @@ __global__ void __launch_bounds__(320, 1)
       float* Ds = L2s + 128;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const int64_t q = q0 + lane * 4 + t;
-        const int64_t li = lse_index(a.g, sv, hq, q);
-        L2s[lane * 4 + t] = q < Nq ? a.lse[li] * kLog2e : INFINITY;
-        Ds[lane * 4 + t] = q < Nq ? a.delta[li] : 0.f;
+        L2s[lane * 4 + t] = lv[t];
+        Ds[lane * 4 + t] = dv[t];
       }
       if (lane == 0) {
         mbar_arrive_expect_tx(b_dfull0 + 8 * ds, C::TILE);
