@@ -50,14 +50,14 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 1044.9 MB per launch measured on 16 heads,
+    # bwd_dkdv_tc_kernel<bf16,128>: 1044.4 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("dkdv", "d60b946c34462a1bd95446af68b9777c0f02575e116286417db2a3dc0e979567",
-     "long-bf16-B1-H32-N16384-D128-causal"): 2089.7e6,
-    # bwd_fused_tc_kernel<bf16,128>: 2927.0 MB per launch measured on 16 heads,
+    ("dkdv", "b0ea44ade0ac72e28681384579b0a7ea7b7feb98e06e3419274f8130a4a2e383",
+     "long-bf16-B1-H32-N16384-D128-causal"): 2088.7e6,
+    # bwd_fused_tc_kernel<bf16,128>: 2929.8 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("fused", "3cb1c44daeb804ad2082491ed29352de741ccfbe73df2370d7afb922057d122f",
-     "long-bf16-B1-H32-N16384-D128-causal"): 5854.0e6,
+    ("fused", "8bd94daf83592095649752ef0129c8c5d4defa8e025d739f5262e886cfec1de2",
+     "long-bf16-B1-H32-N16384-D128-causal"): 5859.6e6,
 }
 
 

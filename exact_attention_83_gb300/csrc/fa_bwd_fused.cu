@@ -49,7 +49,7 @@
 // timeout anywhere ends every role.  Before exit the issuing threads wait for
 // their reductions to complete.
 
-#include "tc_common.cuh"
+#include "bwd_common.cuh"
 
 namespace fa {
 namespace {
@@ -139,21 +139,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t
                : "memory");
 }
 
-// Loads 64 consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld64f(uint32_t taddr, float (&x)[64]) {
-  uint32_t a[32], b[32];
-  tmem_ld32(taddr, a);
-  tmem_ld32(taddr + 32, b);
-  tmem_wait_ld();
-  reg_fence32(a);
-  reg_fence32(b);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    x[i] = __uint_as_float(a[i]);
-    x[32 + i] = __uint_as_float(b[i]);
-  }
-}
-
 // Writes one 128-byte row (8 16-byte units) of a 128-byte-swizzled tile:
 // unit u of row r goes to unit u ^ (r mod 8).
 __device__ __forceinline__ void st_row_sw128(uint32_t tile, int row, const uint32_t* w) {
@@ -163,15 +148,6 @@ __device__ __forceinline__ void st_row_sw128(uint32_t tile, int row, const uint3
     st_shared_v4(base + ((static_cast<uint32_t>(u ^ (row & 7))) << 4), w[4 * u], w[4 * u + 1],
                  w[4 * u + 2], w[4 * u + 3]);
 }
-
-// Staging of a CTA's partial dV (t = 0) and dK (t = 1) for the cluster
-// reduction: [2][128 rows][D] fp32 over the operand buffers (idle by then),
-// 16-byte chunk c of row r stored at chunk c ^ (r mod 8).
-template <int D>
-__device__ __forceinline__ float* stage_row(uint8_t* smem, int t, int row) {
-  return reinterpret_cast<float*>(smem) + (t * 128 + row) * D;
-}
-__device__ __forceinline__ int stage_chunk(int c, int row) { return c ^ (row & 7); }
 
 // What the elementwise threads need to form P for one step.
 struct ProbStep {
@@ -189,7 +165,7 @@ template <typename T, bool DROP>
 __device__ __forceinline__ void form_probs(float (&p)[64], uint64_t& keep, uint32_t taddr,
                                            const ProbStep& s, float c, bool key_in, int hf, int row,
                                            int lane, int64_t key, const Dropout& drop) {
-  tmem_ld64f(taddr, p);
+  tmem_ld64(taddr, p);
 #pragma unroll
   for (int q = 0; q < 64; q += 4) {
     const float4 l4 = *reinterpret_cast<const float4*>(s.L2s + q);
@@ -210,25 +186,7 @@ __device__ __forceinline__ void form_probs(float (&p)[64], uint64_t& keep, uint3
       if (64 * hf + q < row) p[q] = 0.f;
   }
   keep = 0;
-  if constexpr (DROP) {
-    // The eight lanes of an octet hold eight consecutive keys, which one
-    // generator call covers for one query: lane e of the octet draws for
-    // query 8t + e, the octet exchanges the eight 8-bit results, and each
-    // lane keeps the bit of its own key.
-    const uint32_t jg = static_cast<uint32_t>(key >> 3);
-    const int e = lane & 7;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      uint64_t x = static_cast<uint64_t>(
-                       keep8(drop, jg, static_cast<uint32_t>(s.qbase + 8 * t + e), s.bhq))
-                   << (8 * e);
-      x |= __shfl_xor_sync(0xffffffffu, x, 1);
-      x |= __shfl_xor_sync(0xffffffffu, x, 2);
-      x |= __shfl_xor_sync(0xffffffffu, x, 4);
-      const uint64_t y = (x >> e) & 0x0101010101010101ull;
-      keep |= ((y * 0x0102040810204080ull) >> 56) << (8 * t);
-    }
-  }
+  if constexpr (DROP) keep = octet_keep_bits(drop, static_cast<uint32_t>(key >> 3), s.qbase, s.bhq, lane);
   uint32_t w[32];
 #pragma unroll
   for (int q = 0; q < 32; ++q) {
@@ -603,7 +561,7 @@ __global__ void __launch_bounds__(320, 1)
         const float* Ds = reinterpret_cast<const float*>(sD + ds * C::DSLOT + C::TILE) + 128 +
                           64 * hf;
         float dp[64];
-        tmem_ld64f(lane_base + C::COL_DPT + 64 * hf, dp);
+        tmem_ld64(lane_base + C::COL_DPT + 64 * hf, dp);
         if constexpr (DROP) {
           // dS = P o (Z o dP - Delta), Z = keep / (1 - p)
 #pragma unroll
@@ -720,18 +678,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       } else if (rank != 0) {
         // partial sums into this CTA's shared memory for rank 0 to read
-        float* st = stage_row<D>(smem, hf, row);
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t t[32];
-          tmem_ld32(acc + 32 * cc, t);
-          tmem_wait_ld();
-          reg_fence32(t);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(st + 4 * stage_chunk(cc * 8 + u, row)) =
-                make_uint4(t[4 * u], t[4 * u + 1], t[4 * u + 2], t[4 * u + 3]);
-        }
+        stage_partial<D>(smem, hf, row, acc);
       }
     }
   }
@@ -745,42 +692,11 @@ __global__ void __launch_bounds__(320, 1)
       const int64_t key = kt * C::BT + row;
       const uint32_t acc = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                            (hf == 0 ? C::COL_DV : C::COL_DK);
-      const uint32_t st = smem_u32(stage_row<D>(smem, hf, row));
-      const float mul = hf == 0 ? 1.f : a.scale;
       T* out = hf == 0
                    ? static_cast<T*>(a.dv) + bb * a.sdv[0] + hk * a.sdv[1] + (sv.k0 + key) * a.sdv[2]
                    : static_cast<T*>(a.dk) + bb * a.sdk[0] + hk * a.sdk[1] + (sv.k0 + key) * a.sdk[2];
-#pragma unroll 1
-      for (int cc = 0; cc < a.dreal / 32 + (a.dreal % 32 ? 1 : 0); ++cc) {
-        uint32_t t[32];
-        tmem_ld32(acc + 32 * cc, t);
-        tmem_wait_ld();
-        reg_fence32(t);
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(t[i]);
-        for (int r = 1; r < split; ++r) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const float4 x = ld_cluster_f4(cluster_map(st + 16 * stage_chunk(cc * 8 + u, row),
-                                                       static_cast<uint32_t>(r)));
-            v[4 * u] += x.x; v[4 * u + 1] += x.y; v[4 * u + 2] += x.z; v[4 * u + 3] += x.w;
-          }
-        }
-        if (key < Nk) {
-          const int ncol = min(32, a.dreal - 32 * cc);   // 16 or 32
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            if (8 * u >= ncol) break;
-            uint4 w;
-            w.x = pack2<T>(v[8 * u] * mul, v[8 * u + 1] * mul);
-            w.y = pack2<T>(v[8 * u + 2] * mul, v[8 * u + 3] * mul);
-            w.z = pack2<T>(v[8 * u + 4] * mul, v[8 * u + 5] * mul);
-            w.w = pack2<T>(v[8 * u + 6] * mul, v[8 * u + 7] * mul);
-            *reinterpret_cast<uint4*>(out + 32 * cc + 8 * u) = w;
-          }
-        }
-      }
+      cluster_reduce_store<T, D>(smem, hf, row, acc, split, hf == 0 ? 1.f : a.scale, out,
+                                 key < Nk, a.dreal);
     }
     cluster_sync_all();
   }

@@ -35,7 +35,7 @@
 // Every mbarrier wait is bounded (tc_common.cuh); on a timeout the CTA drains
 // its copies and MMAs in flight, frees its tensor memory and exits.
 
-#include "tc_common.cuh"
+#include "bwd_common.cuh"
 
 namespace fa {
 namespace {
@@ -71,30 +71,6 @@ struct BwdTcArgs {
   uint64_t timeout_ns;
 };
 
-// Loads 64 consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
-  uint32_t a[32], b[32];
-  tmem_ld32(taddr, a);
-  tmem_ld32(taddr + 32, b);
-  tmem_wait_ld();
-  reg_fence32(a);
-  reg_fence32(b);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    x[i] = __uint_as_float(a[i]);
-    x[32 + i] = __uint_as_float(b[i]);
-  }
-}
-
-// Rounds 64 floats to T, packs two per column and stores 32 TMEM columns.
-template <typename T>
-__device__ __forceinline__ void tmem_st_packed64(uint32_t taddr, const float (&x)[64]) {
-  uint32_t w[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) w[i] = pack2<T>(x[2 * i], x[2 * i + 1]);
-  tmem_st32(taddr, w);
-}
-
 // ============================================================================
 // dK / dV
 // ============================================================================
@@ -108,15 +84,8 @@ __device__ __forceinline__ void tmem_st_packed64(uint32_t taddr, const float (&x
 // only after dK_i (two dO slots).  S^T_{i+1} overwrites P^T_i and dP^T_{i+1}
 // overwrites dS^T_i; each is read only by products issued before it.  The next
 // tile's scores are therefore ready while the elementwise warps finish dS_i.
-// Staging of a CTA's partial dV (t = 0) and dK (t = 1) for the cluster
-// reduction of the dK/dV kernel: [2][128 rows][D] fp32 over the operand
-// buffers (idle by then), 16-byte chunk c of row r stored at chunk
-// c ^ (r mod 8) so a warp's 32 rows spread over the banks.
-template <int D>
-__device__ __forceinline__ float* stage_row(uint8_t* smem, int t, int row) {
-  return reinterpret_cast<float*>(smem) + (t * 128 + row) * D;
-}
-__device__ __forceinline__ int stage_chunk(int c, int row) { return c ^ (row & 7); }
+// The cluster reduction stages partial sums with stage_row / stage_chunk
+// (bwd_common.cuh).
 
 template <int D>
 struct DkdvCfg : BwdShape<D> {
