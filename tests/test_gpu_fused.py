@@ -22,8 +22,8 @@ import torch
 from exact_attention_83_gb300 import fa
 from exact_attention_83_gb300.inputs import (LONG_CAUSAL, SWEEP_N, GeneralWorkload, Workload,
                                              bf16_n1024, coverage, make_inputs, sweep)
-from parity import compare_full, compare_sampled, run_gpu
-from test_gpu_general import PAGE_SHAPES, _random_general, compare, run_general
+from parity import HUGE, check_huge_heads, compare_full, compare_sampled, run_gpu, run_huge
+from general import PAGE_SHAPES, compare, random_general, run_general
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -285,7 +285,7 @@ def test_dropout_packed_fused():
 
 @pytest.mark.parametrize("seed", range(40))
 def test_random_general_problems_fused(seed):
-    w = _random_general(seed)
+    w = random_general(seed)
     if w.dtype == "fp32":           # the single-pass backward takes 16-bit inputs only
         w = dataclasses.replace(w, dtype="bf16")
     compare(w, *run_general(w, fused=True))
@@ -329,7 +329,6 @@ def test_offsets_beyond_2_31_elements_fused():
     """The single-pass backward and its workspace (8.6 GB) on tensors of more
     than 2^31 elements; sampled rows of the last head, wholly past element
     2^31."""
-    from test_gpu_parity import HUGE, check_huge_heads, run_huge
     inputs, out = run_huge(HUGE, fused=True)
     check_huge_heads(HUGE, inputs, out, heads=[(0, 255)])
     del inputs, out

@@ -16,7 +16,7 @@ import torch
 from exact_attention_83_gb300 import fa
 from exact_attention_83_gb300.inputs import (LONG_CAUSAL, SWEEP_N, TINY_FP32, Workload,
                                              bf16_n1024, coverage, make_inputs, sweep)
-from parity import compare_full, compare_sampled, run_gpu
+from parity import HUGE, check_huge_heads, compare_full, compare_sampled, run_gpu, run_huge
 
 pytestmark = pytest.mark.gpu
 
@@ -176,45 +176,6 @@ def test_invalid_arguments_return_codes_without_launch():
         fa.fwd(qs, qs, qs, o[..., ::2], lse, False, 0.1)
     assert e.value.code == 5
     assert fa.device_status() == 0
-
-
-def run_huge(w, fused: bool):
-    """Forward and backward of a workload whose tensors hold more than 2^31
-    elements, inputs generated on the device; returns the device tensors."""
-    from exact_attention_83_gb300.inputs import make_inputs_device
-    dev = torch.device("cuda", 0)
-    q, k, v, do = make_inputs_device(w, dev)
-    o = torch.full_like(q, float("nan"))
-    lse = torch.full((w.B, w.H, w.N), float("nan"), dtype=torch.float32, device=dev)
-    delta = torch.full_like(lse, float("nan"))
-    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
-    fa.fwd(q, k, v, o, lse, w.causal, w.scale)
-    fa.bwd_preprocess(o, do, delta)
-    if fused:
-        ws = torch.empty(fa.workspace_bytes(q, k, w.causal, w.scale) // 4, dtype=torch.float32,
-                         device=dev)
-        fa.bwd_fused(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale, workspace=ws)
-        del ws
-    else:
-        fa.bwd(q, k, v, do, lse, delta, dq, dk, dv, w.causal, w.scale)
-    torch.cuda.synchronize()
-    assert fa.device_status() == 0
-    return (q, k, v, do), dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
-
-
-def check_huge_heads(w, inputs, out, heads):
-    """Sampled rows of the given heads against the oracle, one head at a time
-    (the head's inputs copied to the host)."""
-    one = Workload(w.name + "-head", 1, 1, w.N, w.D, w.dtype, w.causal, seed=w.seed)
-    for b, h in heads:
-        sub = tuple(t[b:b + 1, h:h + 1].cpu() for t in inputs)
-        got = {key: t[b:b + 1, h:h + 1].float().cpu().double().numpy() for key, t in out.items()}
-        compare_sampled(one, sub, got, q_heads=[(0, 0)], k_heads=[(0, 0)])
-
-
-# B=1, H=256, N=65793 (a ragged tail), D=128: 2.16e9 elements per tensor, so
-# element offsets pass 2^31 in the last heads; ~35 GB on the device.
-HUGE = Workload("huge-bf16-B1-H256-N65793-D128-causal", 1, 256, 65793, 128, "bf16", True, seed=3)
 
 
 def test_offsets_beyond_2_31_elements():
