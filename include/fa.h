@@ -296,6 +296,7 @@ FA_API const char* fa_status_string(fa_status status);
  *   FA_PATH_AUTO: tensor-core kernels for fp16/bf16 where compiled, FFMA
  *                 kernels otherwise (always for fp32).
  *   FA_PATH_FFMA: the FFMA kernels for every dtype.
+ * fa_bwd_fused has tensor-core kernels only and ignores this setting.
  * Returns FA_ERR_ARG for an unknown value.
  */
 typedef enum { FA_PATH_AUTO = 0, FA_PATH_FFMA = 1 } fa_path;
