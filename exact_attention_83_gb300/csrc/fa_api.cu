@@ -172,6 +172,10 @@ fa_status check_problem(const fa_problem* pr, Problem* out) {
     d.key0 = static_cast<uint32_t>(pr->seed & 0xffffffffu);
     d.key1 = static_cast<uint32_t>(pr->seed >> 32);
     d.offset = pr->offset;
+    for (int r = 0; r < 10; ++r) {   // Philox4x32 key schedule (Weyl increments)
+      d.rk0[r] = d.key0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
+      d.rk1[r] = d.key1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
+    }
   }
   out->g = g; out->D = D; out->causal = pr->causal ? 1 : 0; out->scale = pr->scale;
   out->dtype = dt; out->drop = d;

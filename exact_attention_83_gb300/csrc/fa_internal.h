@@ -32,11 +32,15 @@ struct Geo {
 // 3", SC 2011) at counter (j / 8, i, b * Hq + h, offset) under key
 // (key0, key1) is >= thr = floor(p * 65536); kept weights are multiplied by
 // rscale = 1 / (1 - p).  One generator call serves eight consecutive keys.
+// The key of round r (key0 and key1 bumped r times by the two Weyl
+// constants) is computed on the host: as a kernel parameter it is read from
+// the constant bank and takes no register.
 struct Dropout {
   int on;
   uint32_t thr;
   float rscale;
   uint32_t key0, key1, offset;
+  uint32_t rk0[10], rk1[10];   // round keys
 };
 
 // Parameters of one forward call.
@@ -114,17 +118,17 @@ __device__ __forceinline__ void record_status(unsigned int* status, unsigned int
 
 // Philox4x32-10: ten rounds of the published round function (each multiplies
 // counter words 0 and 2 by the round multipliers and mixes the halves of the
-// 64-bit products with words 1 and 3 and the key), the key bumped by the two
-// Weyl constants between rounds.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// 64-bit products with words 1 and 3 and the round's key); the round keys are
+// the key bumped by the two Weyl constants once per round (Dropout::rk0/rk1).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const uint32_t (&rk0)[10],
+                                               const uint32_t (&rk1)[10]) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
     uint64_t p0, p1;
     asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(0xD2511F53u));
     asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(0xCD9E8D57u));
-    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
-                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
+    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ rk0[r], static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ rk1[r], static_cast<uint32_t>(p0));
   }
   return c;
 }
@@ -133,7 +137,7 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 // head bh (= b * Hq + h), as bits 0..7.
 __device__ __forceinline__ uint32_t keep8(const Dropout& d, uint32_t jg, uint32_t i,
                                           uint32_t bh) {
-  const uint4 r = philox4x32_10(make_uint4(jg, i, bh, d.offset), d.key0, d.key1);
+  const uint4 r = philox4x32_10(make_uint4(jg, i, bh, d.offset), d.rk0, d.rk1);
   const uint32_t w[4] = {r.x, r.y, r.z, r.w};
   uint32_t bits = 0;
 #pragma unroll
