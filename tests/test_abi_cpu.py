@@ -132,3 +132,44 @@ def test_fused_workspace_size_and_validation(lib):
     assert call(_problem(), ws=FAKE + 4) == 6             # FA_ERR_ALIGN
     need = 2 * 4 * 300 * 64 * 4
     assert call(_problem(), nbytes=need - 16) == 12       # FA_ERR_SCRATCH
+
+
+def test_general_problem_validation_codes(lib):
+    """fa_fwd_ex / fa_bwd_ex reject invalid problems before any device work."""
+    st = S(0, 300 * 64, 64, 1)        # [1, H, N, D] strides, B = 1
+
+    def fwd(pr, strides=None):
+        s4 = strides or st
+        return lib.fa_fwd_ex(ctypes.byref(pr) if pr is not None else None, FAKE, s4, FAKE, s4,
+                             FAKE, s4, FAKE, s4, FAKE, None)
+
+    def bwd(pr, delta=FAKE):
+        return lib.fa_bwd_ex(ctypes.byref(pr), FAKE, st, FAKE, st, FAKE, st, FAKE, st, FAKE,
+                             delta, FAKE, st, FAKE, st, FAKE, st, None)
+
+    assert fwd(None) == 1                                        # FA_ERR_NULL
+    assert fwd(_problem(B=1, dtype=7)) == 4                      # FA_ERR_DTYPE
+    assert fwd(_problem(B=0)) == 2                               # FA_ERR_SHAPE
+    assert fwd(_problem(B=1, Hq=4, Hkv=3)) == 2                  # Hq % Hkv
+    assert fwd(_problem(B=1, D=48)) == 3                         # FA_ERR_HEADDIM
+    pr = _problem(B=1)
+    pr.scale = 0.0
+    assert fwd(pr) == 10                                         # FA_ERR_SCALE
+    for p in (1.0, -0.1, float("nan")):
+        pr = _problem(B=1)
+        pr.dropout_p = p
+        assert fwd(pr) == 11, p                                  # FA_ERR_ARG
+    pr = _problem(B=1)
+    pr.cu_seqlens_q = FAKE                                        # only one offset array
+    assert fwd(pr) == 2
+    pr = _problem(B=1)
+    pr.cu_seqlens_q = pr.cu_seqlens_k = FAKE
+    pr.total_q, pr.total_k = 0, 100                               # packed totals >= 1
+    assert fwd(pr) == 2
+    pr.total_q = 100
+    pr.cu_seqlens_k = FAKE + 2                                    # int32 offsets, 4-byte aligned
+    assert fwd(pr) == 6
+    pr = _problem(B=1, Nq=(1 << 31) - 1000, Nk=10)                # TMA rows are int32
+    assert fwd(pr) == 2
+    assert fwd(_problem(B=1), strides=S(0, 300 * 64, 64, 2)) == 5     # FA_ERR_STRIDE
+    assert bwd(_problem(B=1), delta=None) == 1
