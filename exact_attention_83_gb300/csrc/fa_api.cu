@@ -356,6 +356,7 @@ fa_status fa_bwd_fused(const fa_problem* prob, const void* q, const int64_t* sq,
   BwdParams p;
   FA_TRY(prepare_bwd(pb, q, sq, k, sk, v, sv, dout, sdo, lse, delta, dq, sdq, dk, sdk, dv, sdv,
                      &p));
+  p.withhold_arrival = g_withhold_next.exchange(0);
   return launch_bwd_fused(p, dq_accum, stream);
 }
 

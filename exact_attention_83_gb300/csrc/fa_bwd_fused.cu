@@ -104,6 +104,7 @@ struct FusedArgs {
   int split;               // CTAs (one cluster) sharing a key tile's query heads
   unsigned int* status;
   uint64_t timeout_ns;
+  int withhold_arrival;    // test-only: CTA 0 withholds one arrival of its first P^T
 };
 
 // ---------------------------------------------------------------- local PTX
@@ -546,7 +547,10 @@ __global__ void __launch_bounds__(320, 1)
       form_probs<T, DROP>(p, keep, lane_base + C::COL_ST + 64 * hf, prob_step(0), c, key_in, hf,
                           row, lane, key, a.drop);
       tc_fence_before();
-      mbar_arrive(b_pready0 + 8 * hf);
+      // A test can withhold this arrival in CTA 0 to make the MMA warp's
+      // bounded wait run out (the timeout path, without a fault).
+      if (!(a.withhold_arrival && blockIdx.x == 0 && threadIdx.x == 0))
+        mbar_arrive(b_pready0 + 8 * hf);
     }
     for (int it = 0; ok && it < n; ++it) {
       const int i = i0 + it % per, ds = it % C::ND, qs = it % C::NQ;
@@ -769,6 +773,7 @@ fa_status run_bwd_fused(const BwdParams& p, float* ws, cudaStream_t stream) {
   a.drop = p.drop;
   a.status = p.status;
   a.timeout_ns = p.timeout_ns;
+  a.withhold_arrival = p.withhold_arrival;
   // one CTA per (b, key/value head, key tile); a cluster of `split` CTAs
   // shares a key tile's query heads while the grid is short of two waves
   const int64_t base = a.BH * ((g.Nk + 127) / 128);

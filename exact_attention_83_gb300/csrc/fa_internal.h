@@ -80,6 +80,7 @@ struct BwdParams {
   unsigned int* status;
   uint64_t timeout_ns;
   const cudaEvent_t* prof;   // 3 events to record around the two kernels, or null
+  int withhold_arrival;      // test-only (single-pass backward): see fa.h
 };
 
 #ifdef __CUDACC__

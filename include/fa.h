@@ -321,14 +321,15 @@ FA_API void fa_set_wait_timeout_ns(uint64_t ns);
 FA_API void fa_set_profile_events(const cudaEvent_t* events);
 
 /*
- * Test hook for the device-side failure path.  The next fa_fwd call that runs
- * the tensor-core forward kernel launches it with one mbarrier arrival
- * withheld in its first CTA, so that CTA's softmax warps wait until the
- * bounded wait (fa_set_wait_timeout_ns) runs out: the kernel then records
- * FA_ERR_TIMEOUT, drains its copies and MMAs in flight, frees its tensor
- * memory and returns; fa_get_device_status reports FA_ERR_TIMEOUT and the
- * context stays usable.  That call's outputs are undefined.  One-shot: later
- * calls run normally.  Set a short wait bound first (e.g. 50 ms).
+ * Test hook for the device-side failure path.  The next call that runs the
+ * tensor-core forward kernel (fa_fwd, fa_fwd_ex) or the single-pass backward
+ * (fa_bwd_fused) launches it with one mbarrier arrival withheld in its first
+ * CTA, so that CTA's waiting warps wait until the bounded wait
+ * (fa_set_wait_timeout_ns) runs out: the kernel then records FA_ERR_TIMEOUT,
+ * drains its copies, MMAs and reductions in flight, frees its tensor memory
+ * and returns; fa_get_device_status reports FA_ERR_TIMEOUT and the context
+ * stays usable.  That call's outputs are undefined.  One-shot: later calls
+ * run normally.  Set a short wait bound first (e.g. 50 ms).
  */
 FA_API void fa_test_withhold_next_arrival(void);
 
