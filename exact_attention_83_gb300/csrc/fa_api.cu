@@ -257,6 +257,24 @@ fa_problem square_problem(int64_t B, int64_t H, int64_t N, int64_t D, int causal
 
 }  // namespace
 
+fa_status validate_square_bwd(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, const void* dq,
+                              const void* dk, const void* dv, int64_t B, int64_t H, int64_t N,
+                              int64_t D, const int64_t* sq, const int64_t* sk,
+                              const int64_t* sv, const int64_t* so, const int64_t* sdo,
+                              const int64_t* sdq, const int64_t* sdk, const int64_t* sdv,
+                              int causal, float scale, fa_dtype dtype) {
+  FA_TRY(check_shape(B, H, N, D, dtype));
+  const fa_problem pr = square_problem(B, H, N, D, causal, scale, dtype);
+  Problem pb{};
+  FA_TRY(check_problem(&pr, &pb));
+  int64_t st[4];
+  const void* tensors[8] = {q, k, v, o, dout, dq, dk, dv};
+  const int64_t* strides[8] = {sq, sk, sv, so, sdo, sdq, sdk, sdv};
+  for (int i = 0; i < 8; ++i) FA_TRY(check_tensor(tensors[i], strides[i], B, H, N, dtype, st));
+  return check_f32_vec(lse);
+}
+
 int device_sm_count() {
   int dev = 0;
   cudaGetDevice(&dev);

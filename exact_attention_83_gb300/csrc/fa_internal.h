@@ -183,6 +183,18 @@ bool encode_f32_rows_map(CUtensorMap* map, const float* base, int64_t cols, int6
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Every argument check of fa_bwd_preprocess followed by fa_bwd on a square
+// problem (shape, dtype, scale, each tensor's pointer, alignment and strides,
+// lse), except the delta pointer, which the caller supplies itself.  Touches
+// no device: no context is created and nothing is launched.
+fa_status validate_square_bwd(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, const void* dq,
+                              const void* dk, const void* dv, int64_t B, int64_t H, int64_t N,
+                              int64_t D, const int64_t* sq, const int64_t* sk,
+                              const int64_t* sv, const int64_t* so, const int64_t* sdo,
+                              const int64_t* sdq, const int64_t* sdk, const int64_t* sdv,
+                              int causal, float scale, fa_dtype dtype);
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

@@ -47,10 +47,17 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                                     const int64_t* so, const int64_t* sdo, const int64_t* sdq,
                                     const int64_t* sdk, const int64_t* sdv, int causal,
                                     float scale, fa_dtype dtype, cudaStream_t stream) {
+  // Every check comes before any device work: an invalid call neither creates
+  // a context, nor looks up the array, nor launches anything (so it leaves no
+  // stray node in a graph being captured and never writes the shared array).
   if (B < 1 || H < 1 || N < 1) return FA_ERR_SHAPE;
   int64_t bh = 0, rows = 0;
   if (__builtin_mul_overflow(B, H, &bh) || __builtin_mul_overflow(bh, N, &rows)) return FA_ERR_SHAPE;
   if (rows > kMaxRows) return FA_ERR_SCRATCH;
+  const fa_status valid = fa::validate_square_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, D,
+                                                  sq, sk, sv, so, sdo, sdq, sdk, sdv, causal,
+                                                  scale, dtype);
+  if (valid != FA_OK) return valid;
   float* delta = nullptr;
   const fa_status st = scratch_delta(&delta);
   if (st != FA_OK) return st;

@@ -141,8 +141,10 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
  * process exits.  O is the forward output (strides so).  The call allocates
  * nothing (no cudaMalloc, no cudaFree).
  *
- * Limit: B * H * N <= FA_NOALLOC_MAX_ROWS, else FA_ERR_SCRATCH and nothing is
- * launched.
+ * Limit: B * H * N <= FA_NOALLOC_MAX_ROWS, else FA_ERR_SCRATCH.
+ * Errors: the size limit and every argument check of fa_bwd_preprocess and
+ * fa_bwd run before any device work, so an invalid call returns its code
+ * without creating a context, looking up the buffer or launching anything.
  * Set-up: the first call on a device (with that device current) looks up the
  * buffer's device address once; make that first call before any stream
  * capture begins.
