@@ -38,10 +38,9 @@ sys.path.insert(0, ROOT)
 import torch  # noqa: E402
 
 from exact_attention_83_gb300 import shard  # noqa: E402
-from exact_attention_83_gb300.inputs import (LONG_CAUSAL, SWEEP_N, TINY_FP32,  # noqa: E402
-                                             GeneralWorkload, Workload, bf16_n1024, coverage,
-                                             make_general_inputs, make_inputs, seqlen_mix,
-                                             sweep)
+from exact_attention_83_gb300.inputs import (BENCH_GENERAL, LONG_CAUSAL, SWEEP_N,  # noqa: E402
+                                             TINY_FP32, GeneralWorkload, Workload, bf16_n1024,
+                                             coverage, make_general_inputs, make_inputs, sweep)
 
 METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 peak"
 
@@ -66,28 +65,10 @@ MEASURED_TRAFFIC = {
 PROFILE_CASE = Workload("long-bf16-B1-H16-N16384-D128-causal", 1, 16, 16384, 128, "bf16", True)
 
 
-# General problems at the size of the long causal shape (32 query heads of
-# 16384 rows, D = 128, bf16): grouped and multi-query heads, packed sequences,
-# dropout, and cross-attention-like lengths.
-_MIX = seqlen_mix(65536, 512, 8192, seed=1)
-GENERAL = [
-    GeneralWorkload("gqa-bf16-B1-Hq32-Hkv8-N16384-D128-causal", 1, 32, 8, 16384, 16384, 128,
-                    "bf16", True),
-    GeneralWorkload("mqa-bf16-B1-Hq32-Hkv1-N16384-D128-causal", 1, 32, 1, 16384, 16384, 128,
-                    "bf16", True),
-    GeneralWorkload("dropout0.1-bf16-B1-H32-N16384-D128-causal", 1, 32, 32, 16384, 16384, 128,
-                    "bf16", True, dropout_p=0.1),
-    GeneralWorkload("varlen-bf16-64k-tokens-len512-8192-Hq32-Hkv8-D128-causal", len(_MIX), 32, 8,
-                    max(_MIX), max(_MIX), 128, "bf16", True, seqlens_q=_MIX, seqlens_k=_MIX),
-    GeneralWorkload("cross-bf16-B4-H32-Nq4096-Nk16384-D128-full", 4, 32, 32, 4096, 16384, 128,
-                    "bf16", False),
-]
-
-
 def workloads():
     ws = {LONG_CAUSAL.name: LONG_CAUSAL, PROFILE_CASE.name: PROFILE_CASE,
           TINY_FP32.name: TINY_FP32}
-    ws.update({g.name: g for g in GENERAL})
+    ws.update({g.name: g for g in BENCH_GENERAL})
     for c in (False, True):
         w = bf16_n1024(c)
         ws[w.name] = w
@@ -254,6 +235,8 @@ def main():
     ap.add_argument("--workload", default=LONG_CAUSAL.name)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the sequence-length sweep record of the default run")
     ap.add_argument("--bwd", default="split", choices=["split", "fused"])
     args = ap.parse_args()
     if args.warmup < 3:
@@ -352,10 +335,10 @@ def main():
     if flush_buf is None:
         ms_step = max_over_ranks(start.elapsed_time(end)) / args.steps
     else:
-        ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[4]) for e in ev))
+        ms_step = max_over_ranks(statistics.median(e[0].elapsed_time(e[4]) for e in ev))
     fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     pre_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
-    dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    dkdv_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
     dq_ms = statistics.median(e[3].elapsed_time(e[4]) for e in ev)
     if fa.device_status() != 0:
         raise RuntimeError("device status not OK after the timed region")
@@ -379,7 +362,7 @@ def main():
             fa.fwd(q, k, v, o, lse, w.causal, w.scale)
             b_.record(stream)
         barrier()
-        fwd_only_ms = max_over_ranks(statistics.mean(a_.elapsed_time(b_) for a_, b_ in fev))
+        fwd_only_ms = max_over_ranks(statistics.median(a_.elapsed_time(b_) for a_, b_ in fev))
 
     flops_fwd = w.fwd_flops()
     flops_step = w.fwd_bwd_flops()
@@ -403,6 +386,10 @@ def main():
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(args, w, dev, fa, fused)
+
+    sweep_rec = None
+    if not args.no_sweep and w.name == LONG_CAUSAL.name and world == 1:
+        sweep_rec = run_sweep(fa, dev, stream, args.steps, args.warmup, pk["bf16_tflops"])
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -436,6 +423,8 @@ def main():
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if sweep_rec is not None:
+            line["sweep"] = sweep_rec
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -521,7 +510,7 @@ def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
     ms_step = shard.max_over_ranks(start.elapsed_time(end), dev) / args.steps
     fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     pre_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
-    dkdv_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    dkdv_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
     dq_ms = statistics.median(e[3].elapsed_time(e[4]) for e in ev)
     value = world * w.fwd_bwd_flops() / (ms_step * 1e-3) / 1e12
     pk = peaks()
@@ -555,6 +544,66 @@ def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_sweep(fa, dev, stream, steps: int, warmup: int, peak: float):
+    """The sequence-length sweep over the metric's range: D = 64, H = 16,
+    B*N = 16384, N = 512 .. 16384, bf16 and fp16, causal and full.  Inputs
+    (4 x 32 MiB) are smaller than twice the L2, so L2 is flushed (2 x L2
+    write) before every timed step and steps are timed one by one; each point
+    reports the median forward and forward+backward TFLOP/s (forward 4*B*H*N^2*D
+    halved when causal, backward credited 2.5x) and their fractions of the
+    burst bf16 peak."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    points = []
+    with ClockSampler(dev.index) as clocks:
+        for dt in ("bf16", "fp16"):
+            for N in SWEEP_N:
+                # causal and full share the seed, hence the inputs
+                q, k, v, do = (t.to(dev) for t in make_inputs(sweep(N, dt, False)))
+                o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+                lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+                delta = torch.empty_like(lse)
+                for causal in (True, False):
+                    w = sweep(N, dt, causal)
+
+                    def step(ev=None):
+                        if ev is not None:
+                            ev[0].record(stream)
+                        fa.fwd(q, k, v, o, lse, causal, w.scale)
+                        if ev is not None:
+                            ev[1].record(stream)
+                        fa.bwd_preprocess(o, do, delta)
+                        fa.bwd(q, k, v, do, lse, delta, dq, dk, dv, causal, w.scale)
+                        if ev is not None:
+                            ev[2].record(stream)
+
+                    for _ in range(warmup):
+                        step()
+                    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                          for _ in range(steps)]
+                    for e in ev:
+                        flush.zero_()
+                        step(e)
+                    torch.cuda.synchronize(dev)
+                    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+                    step_ms = statistics.median(e[0].elapsed_time(e[2]) for e in ev)
+                    f = w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
+                    fb = w.fwd_bwd_flops() / (step_ms * 1e-3) / 1e12
+                    points.append({"N": N, "B": w.B, "dtype": dt, "causal": causal,
+                                   "fwd_tflops": f, "fwd_bwd_tflops": fb,
+                                   "fwd_frac": f / peak, "fwd_bwd_frac": fb / peak,
+                                   "fwd_ms": fwd_ms, "fwd_bwd_ms": step_ms})
+                del q, k, v, do, o, dq, dk, dv, lse, delta
+    if fa.device_status() != 0:
+        raise RuntimeError("device status not OK after the sweep")
+    return {"workload": "D=64 H=16 B*N=16384 (B*H*N=262144), N 512..16384, bf16 and fp16, "
+                        "causal and full; inputs i.i.d. N(0,1) seed 0",
+            "l2": "flushed (%d MiB write) before each timed step; median of %d steps"
+                  % (2 * l2 >> 20, steps),
+            "unit": "TFLOP/s", "peak_tflops": peak, "points": points,
+            "clocks": clocks.summary()}
 
 
 def measure_e2e(args, w, dev, fa, fused=False):
@@ -609,6 +658,38 @@ def measure_e2e(args, w, dev, fa, fused=False):
         step(i)
     torch.cuda.synchronize(dev)
     in_ready.clear(); comp_done.clear(); out_done.clear()
+
+    # The link alone: one step's host->device and device->host copies on the
+    # same pinned buffers, nothing else running (median of five).
+    def copy_ms(stream, pairs):
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        with torch.cuda.stream(stream):
+            for dst, src in pairs:
+                dst.copy_(src, non_blocking=True)
+        b_.record(stream)
+        torch.cuda.synchronize(dev)
+        return a_.elapsed_time(b_)
+
+    h2d_ms = statistics.median(copy_ms(s_in, list(zip(din[0], hin))) for _ in range(5))
+    d2h_ms = statistics.median(copy_ms(s_out, list(zip(hout[0], dout[0]))) for _ in range(5))
+    # The compute alone on the same device buffers (no copy in flight).
+    ca, cb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ca.record(s_comp)
+    with torch.cuda.stream(s_comp):
+        for _ in range(args.steps):
+            q, k, v, do = din[0]
+            o, dq, dk, dv = dout[0]
+            fa.fwd(q, k, v, o, lse[0], w.causal, w.scale)
+            fa.bwd_preprocess(o, do, delta[0])
+            if fused:
+                fa.bwd_fused(q, k, v, do, lse[0], delta[0], dq, dk, dv, w.causal, w.scale,
+                             workspace=ws[0])
+            else:
+                fa.bwd(q, k, v, do, lse[0], delta[0], dq, dk, dv, w.causal, w.scale)
+    cb.record(s_comp)
+    torch.cuda.synchronize(dev)
+    comp_ms = ca.elapsed_time(cb) / args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(s_in)
     for i in range(args.steps):
@@ -622,7 +703,15 @@ def measure_e2e(args, w, dev, fa, fused=False):
     nbytes = hq.numel() * hq.element_size()
     return {"value": world * w.fwd_bwd_flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "ms_per_step": ms, "h2d_bytes_per_step": 4 * nbytes, "d2h_bytes_per_step": 4 * nbytes,
-            "overlap": "copies on separate streams, double-buffered"}
+            "overlap": "copies on separate streams, double-buffered",
+            "link": {"h2d_ms": h2d_ms, "d2h_ms": d2h_ms,
+                     "h2d_gbs": 4 * nbytes / (h2d_ms * 1e-3) / 1e9,
+                     "d2h_gbs": 4 * nbytes / (d2h_ms * 1e-3) / 1e9,
+                     "compute_alone_ms": comp_ms,
+                     "bound_ms": max(comp_ms, h2d_ms, d2h_ms),
+                     "note": "each direction's copies alone on the step's pinned buffers; "
+                             "compute alone on the same device buffers; with full overlap "
+                             "a step takes max of the three"}}
 
 
 if __name__ == "__main__":

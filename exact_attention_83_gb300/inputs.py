@@ -225,3 +225,22 @@ def seqlen_mix(total: int, lo: int, hi: int, seed: int) -> tuple:
         lens.append(n)
         acc += n
     return tuple(lens)
+
+
+# General problems at the size of the long causal shape (32 query heads of
+# 16384 rows, D = 128, bf16): grouped and multi-query heads, packed sequences,
+# dropout, and cross-attention-like lengths.  The benchmark times them and the
+# GPU tests check sampled rows of each against the oracle at this size.
+_MIX = seqlen_mix(65536, 512, 8192, seed=1)
+BENCH_GENERAL = [
+    GeneralWorkload("gqa-bf16-B1-Hq32-Hkv8-N16384-D128-causal", 1, 32, 8, 16384, 16384, 128,
+                    "bf16", True),
+    GeneralWorkload("mqa-bf16-B1-Hq32-Hkv1-N16384-D128-causal", 1, 32, 1, 16384, 16384, 128,
+                    "bf16", True),
+    GeneralWorkload("dropout0.1-bf16-B1-H32-N16384-D128-causal", 1, 32, 32, 16384, 16384, 128,
+                    "bf16", True, dropout_p=0.1),
+    GeneralWorkload("varlen-bf16-64k-tokens-len512-8192-Hq32-Hkv8-D128-causal", len(_MIX), 32, 8,
+                    max(_MIX), max(_MIX), 128, "bf16", True, seqlens_q=_MIX, seqlens_k=_MIX),
+    GeneralWorkload("cross-bf16-B4-H32-Nq4096-Nk16384-D128-full", 4, 32, 32, 4096, 16384, 128,
+                    "bf16", False),
+]

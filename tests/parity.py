@@ -3,34 +3,27 @@ seeded inputs and compare with the fp64 oracle.
 
 Tolerances (stated in the attention spec this library follows): max-abs error
 1e-4 for fp32 and 2e-2 for fp16/bf16, for O, L, dQ, dK and dV at unit-normal
-inputs.
+inputs.  Those workloads use them exactly as stated.
 
-For inputs scaled by 4 the spec states no tolerance; it is derived here.
-Every intermediate grows with the inputs: raw scores q.k reach ~16*sqrt(D)
-standard deviations (exponents ~80 in log2 units), O grows to ~4 and dQ, dK
-to tens.  A correct implementation's absolute error then scales with the
-largest magnitudes, not with the RMS:
-  * fp32: the fp32 dot products behind S carry ~1e-7 * |q||k| * sqrt(D) of
-    rounding, i.e. a relative error of ~1e-4 in P, which multiplies
-    dP - Delta (~|dO||V| sqrt(D));
-  * fp16/bf16: Delta = rowsum(dO o O) is formed from the stored O (as in
-    FlashAttention-2), whose rounding (|O| * 2^-9 for bf16) enters every
-    dS_ij = P_ij (dP_ij - Delta_i).
-Measured on the FFMA kernels, these give max errors of 2-10x the spec
-tolerance times RMS(ref).  The bound used for these cases is therefore
-    max |got - ref| <= tol * max(1, max |ref|)      per tensor,
-which still fails on any structural mistake (those give errors of the order
-of max |ref| itself).
+For inputs scaled by 4 the spec states no tolerance, and its unit-normal one
+does not carry over: every intermediate grows with the inputs (scores reach
+~80 in natural-log units, O ~17, dQ and dK ~70, Delta ~140), and so does the
+rounding error of any correct implementation.  The bound is therefore measured
+on the same inputs, not chosen: ``emulate.py`` computes the same outputs in
+the library's documented precision (IEEE fp32 products and sums; for
+fp16/bf16 P and dS rounded to the input type before their products, Delta from
+the stored O, outputs rounded), independently of the kernels and of the
+oracle, and its max-abs error against the oracle over exactly the elements a
+comparison checks is e_ind.  The kernels must then meet
 
-The 16-bit tensor-core kernels also round P (before P V) and dS (before
-dS K and dS^T Q) to the input type, as FlashAttention-2 does for its second
-GEMM of each pair.  A sum of products with one factor rounded to relative
-precision u is off by at most u times the sum of the products' magnitudes
-(the standard componentwise bound), so for x4 inputs in fp16/bf16 each
-element of O, dQ, dK, dV gets, on top of the per-tensor term above,
-    u * (sum P|V|, scale sum |dS||K|, scale sum |dS||Q|, sum P|dO|)
-with u = 2^-8 (bf16) or 2^-11 (fp16), the sums computed by the oracle.  At
-unit-normal inputs the spec's tolerance is used as stated.
+    max |got - ref| <= max(tol, C_EMU * e_ind)      per tensor and case,
+
+with C_EMU = 4 fixed before any kernel was measured against it: a kernel that
+does the same arithmetic in another order lands within a small factor of
+e_ind, while a dropped term, a wrong index or a mis-rounded product gives
+errors of the order of the values themselves.  Every comparison of these
+cases is recorded in REPORT (error, bound, ratio, and whether the plain spec
+tolerance alone would pass) and printed at the end of the test session.
 """
 
 from __future__ import annotations
@@ -39,30 +32,44 @@ import numpy as np
 import torch
 
 import oracle
+from emulate import emulate
 from exact_attention_83_gb300 import fa
 from exact_attention_83_gb300.inputs import Workload, make_inputs, make_inputs_device
 
 TOL = {"fp32": 1e-4, "fp16": 2e-2, "bf16": 2e-2}
 UNIT_ROUNDOFF = {"fp16": 2.0 ** -11, "bf16": 2.0 ** -8}
 KEYS = ("o", "lse", "dq", "dk", "dv")
-MAG_KEYS = ("o", "dq", "dk", "dv")
+C_EMU = 4.0
+
+# (case, tensor, max error, bound, error / bound, passes the plain spec tolerance)
+REPORT: list[tuple[str, str, float, float, float, bool]] = []
 
 
-def wants_magnitudes(w: Workload) -> bool:
-    return w.qkv_scale != 1.0 and w.dtype in UNIT_ROUNDOFF
+def derived(w: Workload) -> bool:
+    """True for the workloads whose bound is derived from the emulation."""
+    return w.qkv_scale != 1.0
 
 
-def tolerance(w: Workload, key: str, ref: np.ndarray, mag: np.ndarray | None = None):
-    """(atol, rtol) for tensor `key` of workload `w`; atol is an array when
-    the componentwise term applies (mag: the oracle's magnitude sums)."""
+def tolerance(w: Workload, key: str, e_ind: float | None = None) -> float:
+    """Max-abs bound for tensor `key` of workload `w`.  e_ind is the
+    emulation's error over the compared elements; it sizes the bound of the
+    derived workloads, and of Delta (an intermediate, not one of the five
+    outputs the spec's tolerances cover) everywhere."""
     t = TOL[w.dtype]
-    if w.qkv_scale == 1.0:
-        return t, 0.0
-    peak = float(np.abs(ref).max()) if ref.size else 0.0
-    atol = t * max(1.0, peak)
-    if mag is not None and wants_magnitudes(w):
-        atol = atol + UNIT_ROUNDOFF[w.dtype] * mag
-    return atol, 0.0
+    if not derived(w) and key != "delta":
+        return t
+    assert e_ind is not None, "derived bound needs the emulation's error"
+    return max(t, C_EMU * e_ind)
+
+
+def _compare(w: Workload, key: str, got: np.ndarray, ref: np.ndarray, emu: np.ndarray | None):
+    e_ind = float(np.abs(emu - ref).max()) if (emu is not None and ref.size) else 0.0
+    bound = tolerance(w, key, e_ind if emu is not None else None)
+    err = check(f"{w.name}:{key}", got, ref, bound)
+    if derived(w):
+        REPORT.append((w.name, key, err, bound, err / bound if bound else 0.0,
+                       err <= TOL[w.dtype]))
+    return err
 
 
 def run_gpu(w: Workload, inputs=None, backward: bool = True, fused: bool = False):
@@ -130,41 +137,23 @@ def compare_full(w: Workload, inputs, got, heads=None):
     when None) with the oracle run on those heads alone."""
     q, k, v, do = inputs
     if heads is None:
-        sel = (slice(None), slice(None))
-        ref = oracle.fwd_bwd(q, k, v, do, w.causal, w.scale) if do is not None else None
-        if ref is not None and wants_magnitudes(w):
-            m = oracle.magnitudes(q, k, v, do, w.causal, w.scale)
-            ref.update({key + "_abs": m[key] for key in MAG_KEYS})
-        if ref is None:
-            o, L = oracle.fwd(q, k, v, w.causal, w.scale)
-            ref = {"o": o, "lse": L}
-        pairs = [(ref, sel)]
-    else:
-        pairs = []
-        for b, h in heads:
-            sl = (slice(b, b + 1), slice(h, h + 1))
-            qs, ks, vs = q[sl], k[sl], v[sl]
-            if do is not None:
-                r = oracle.fwd_bwd(qs, ks, vs, do[sl], w.causal, w.scale)
-                if wants_magnitudes(w):
-                    m = oracle.magnitudes(qs, ks, vs, do[sl], w.causal, w.scale)
-                    r.update({key + "_abs": m[key] for key in MAG_KEYS})
-            else:
-                o, L = oracle.fwd(qs, ks, vs, w.causal, w.scale)
-                r = {"o": o, "lse": L}
-            pairs.append((r, sl))
+        heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    need_emu = derived(w) or (do is not None and "delta" in got)
+    emu = emulate(q, k, v, do, w.causal, w.scale, heads) if need_emu else None
     errs = {}
-    for ref, sl in pairs:
+    for b, h in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        qs, ks, vs = q[sl], k[sl], v[sl]
+        if do is not None:
+            ref = oracle.fwd_bwd(qs, ks, vs, do[sl], w.causal, w.scale)
+        else:
+            o, L = oracle.fwd(qs, ks, vs, w.causal, w.scale)
+            ref = {"o": o, "lse": L}
         for key in KEYS + ("delta",):
             if key not in ref or key not in got:
                 continue
-            g = got[key][sl]
-            tol = tolerance(w, key, ref[key], ref.get(key + "_abs"))
-            if key == "delta":
-                # Delta is a D-term sum of dO * O, O read back in the input type
-                atol_o, r_o = tolerance(w, "o", ref["o"])
-                tol = (atol_o * max(1.0, float(np.abs(ref[key]).max())), r_o)
-            errs[key] = max(errs.get(key, 0.0), check(f"{w.name}:{key}", g, ref[key], tol))
+            e = emu[(b, h)][key][None, None] if emu is not None else None
+            errs[key] = max(errs.get(key, 0.0), _compare(w, key, got[key][sl], ref[key], e))
     return errs
 
 
@@ -188,23 +177,25 @@ def compare_sampled(w: Workload, inputs, got, q_heads, k_heads):
     (dK, dV) over k_heads, against the oracle's row entry points."""
     q, k, v, do = inputs
     errs = {}
+    emu = None
+    if derived(w):
+        emu = emulate(q, k, v, do, w.causal, w.scale, sorted(set(q_heads) | set(k_heads)))
     qrows = sample_rows(w, q_heads)
-    mags = wants_magnitudes(w)
-    ref = oracle.query_rows(q, k, v, do, w.causal, qrows, w.scale, magnitudes=mags)
+    ref = oracle.query_rows(q, k, v, do, w.causal, qrows, w.scale)
     bh, i = qrows[:, 0], qrows[:, 1]
     b, h = bh // w.H, bh % w.H
     for key in ("o", "lse", "dq"):
-        g = got[key][b, h, i]
-        tol = tolerance(w, key, ref[key], ref.get(key + "_abs"))
-        errs[key] = check(f"{w.name}:{key}", g, ref[key], tol)
+        e = (np.stack([emu[(int(bb), int(hh))][key][int(ii)] for bb, hh, ii in zip(b, h, i)])
+             if emu is not None else None)
+        errs[key] = _compare(w, key, got[key][b, h, i], ref[key], e)
     krows = sample_rows(w, k_heads, seed=2)
-    ref = oracle.key_rows(q, k, v, do, w.causal, krows, w.scale, magnitudes=mags)
+    ref = oracle.key_rows(q, k, v, do, w.causal, krows, w.scale)
     bh, j = krows[:, 0], krows[:, 1]
     b, h = bh // w.H, bh % w.H
     for key in ("dk", "dv"):
-        g = got[key][b, h, j]
-        tol = tolerance(w, key, ref[key], ref.get(key + "_abs"))
-        errs[key] = check(f"{w.name}:{key}", g, ref[key], tol)
+        e = (np.stack([emu[(int(bb), int(hh))][key][int(jj)] for bb, hh, jj in zip(b, h, j)])
+             if emu is not None else None)
+        errs[key] = _compare(w, key, got[key][b, h, j], ref[key], e)
     return errs
 
 

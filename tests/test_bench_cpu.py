@@ -58,7 +58,7 @@ def test_workload_catalogue():
                 assert f"sweep-{dt}-B{16384 // N}-H16-N{N}-D64-{causal}" in ws
     cover = [n for n in ws if n.startswith("cover")]
     assert len(cover) == 48
-    for g in bench.GENERAL:
+    for g in bench.BENCH_GENERAL:
         assert g.name in ws
 
 
