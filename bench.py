@@ -11,6 +11,13 @@ flushed between steps.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--bwd split|fused]
 
+The default run also adds a `sweep` record: the sequence-length sweep over the
+metric's range (D = 64, H = 16, B*N = 16384, N = 512 .. 16384, bf16 and fp16,
+causal and full), forward and forward+backward TFLOP/s per point with L2
+flushed before every timed step; and `e2e.link`: the host link's rates for
+the step's copies alone and the compute alone, so that the end-to-end time
+can be set against max(compute, host-to-device, device-to-host).
+
 `--bwd fused` times the single-pass backward (fa_bwd_fused: one kernel per key
 tile, dQ summed by fp32 bulk reductions into a workspace, then converted)
 instead of the split one.
@@ -625,6 +632,7 @@ def measure_e2e(args, w, dev, fa, fused=False):
     s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     ev = lambda: torch.cuda.Event()
     in_ready, comp_done, out_done = {}, {}, {}
+    comp_ev = {}        # timed steps: events around each step's compute
 
     def step(i):
         b = i % 2
@@ -638,6 +646,8 @@ def measure_e2e(args, w, dev, fa, fused=False):
             s_comp.wait_event(in_ready[i])
             if i - 2 in out_done:                  # D2H of step i-2 read dout[b]
                 s_comp.wait_event(out_done[i - 2])
+            if i in comp_ev:
+                comp_ev[i][0].record(s_comp)
             q, k, v, do = din[b]
             o, dq, dk, dv = dout[b]
             fa.fwd(q, k, v, o, lse[b], w.causal, w.scale)
@@ -647,6 +657,8 @@ def measure_e2e(args, w, dev, fa, fused=False):
                              workspace=ws[b])
             else:
                 fa.bwd(q, k, v, do, lse[b], delta[b], dq, dk, dv, w.causal, w.scale)
+            if i in comp_ev:
+                comp_ev[i][1].record(s_comp)
             comp_done[i] = ev(); comp_done[i].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[i])
@@ -690,15 +702,19 @@ def measure_e2e(args, w, dev, fa, fused=False):
     cb.record(s_comp)
     torch.cuda.synchronize(dev)
     comp_ms = ca.elapsed_time(cb) / args.steps
+    comp_ev.update({i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for i in range(args.steps)})
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(s_in)
-    for i in range(args.steps):
-        step(i)
-    # the end event follows the last copy of every stream
-    s_in.wait_stream(s_comp); s_in.wait_stream(s_out)
-    end.record(s_in)
-    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        start.record(s_in)
+        for i in range(args.steps):
+            step(i)
+        # the end event follows the last copy of every stream
+        s_in.wait_stream(s_comp); s_in.wait_stream(s_out)
+        end.record(s_in)
+        torch.cuda.synchronize(dev)
     ms = start.elapsed_time(end) / args.steps
+    comp_overlap_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in comp_ev.values())
     world = int(os.environ.get("WORLD_SIZE", "1"))
     nbytes = hq.numel() * hq.element_size()
     return {"value": world * w.fwd_bwd_flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -708,10 +724,13 @@ def measure_e2e(args, w, dev, fa, fused=False):
                      "h2d_gbs": 4 * nbytes / (h2d_ms * 1e-3) / 1e9,
                      "d2h_gbs": 4 * nbytes / (d2h_ms * 1e-3) / 1e9,
                      "compute_alone_ms": comp_ms,
+                     "compute_during_copies_ms": comp_overlap_ms,
+                     "clocks": clocks.summary(),
                      "bound_ms": max(comp_ms, h2d_ms, d2h_ms),
                      "note": "each direction's copies alone on the step's pinned buffers; "
                              "compute alone on the same device buffers; with full overlap "
-                             "a step takes max of the three"}}
+                             "a step takes max of the three; compute_during_copies_ms is the "
+                             "median compute of the timed end-to-end steps"}}
 
 
 if __name__ == "__main__":
