@@ -639,8 +639,12 @@ def measure_e2e(args, w, dev, fa, fused=False):
         with torch.cuda.stream(s_in):
             if i - 2 in comp_done:                 # compute of step i-2 read din[b]
                 s_in.wait_event(comp_done[i - 2])
+            if i in comp_ev:
+                comp_ev[i][2].record(s_in)
             for d, h in zip(din[b], hin):
                 d.copy_(h, non_blocking=True)
+            if i in comp_ev:
+                comp_ev[i][3].record(s_in)
             in_ready[i] = ev(); in_ready[i].record(s_in)
         with torch.cuda.stream(s_comp):
             s_comp.wait_event(in_ready[i])
@@ -662,8 +666,12 @@ def measure_e2e(args, w, dev, fa, fused=False):
             comp_done[i] = ev(); comp_done[i].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[i])
+            if i in comp_ev:
+                comp_ev[i][4].record(s_out)
             for h, d in zip(hout[b], dout[b]):
                 h.copy_(d, non_blocking=True)
+            if i in comp_ev:
+                comp_ev[i][5].record(s_out)
             out_done[i] = ev(); out_done[i].record(s_out)
 
     for i in range(args.warmup):
@@ -702,7 +710,7 @@ def measure_e2e(args, w, dev, fa, fused=False):
     cb.record(s_comp)
     torch.cuda.synchronize(dev)
     comp_ms = ca.elapsed_time(cb) / args.steps
-    comp_ev.update({i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    comp_ev.update({i: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
                     for i in range(args.steps)})
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
@@ -714,7 +722,9 @@ def measure_e2e(args, w, dev, fa, fused=False):
         end.record(s_in)
         torch.cuda.synchronize(dev)
     ms = start.elapsed_time(end) / args.steps
-    comp_overlap_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in comp_ev.values())
+    comp_overlap_ms = statistics.median(e[0].elapsed_time(e[1]) for e in comp_ev.values())
+    h2d_overlap_ms = statistics.median(e[2].elapsed_time(e[3]) for e in comp_ev.values())
+    d2h_overlap_ms = statistics.median(e[4].elapsed_time(e[5]) for e in comp_ev.values())
     world = int(os.environ.get("WORLD_SIZE", "1"))
     nbytes = hq.numel() * hq.element_size()
     return {"value": world * w.fwd_bwd_flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -725,12 +735,14 @@ def measure_e2e(args, w, dev, fa, fused=False):
                      "d2h_gbs": 4 * nbytes / (d2h_ms * 1e-3) / 1e9,
                      "compute_alone_ms": comp_ms,
                      "compute_during_copies_ms": comp_overlap_ms,
+                     "h2d_during_compute_ms": h2d_overlap_ms,
+                     "d2h_during_compute_ms": d2h_overlap_ms,
                      "clocks": clocks.summary(),
                      "bound_ms": max(comp_ms, h2d_ms, d2h_ms),
                      "note": "each direction's copies alone on the step's pinned buffers; "
                              "compute alone on the same device buffers; with full overlap "
-                             "a step takes max of the three; compute_during_copies_ms is the "
-                             "median compute of the timed end-to-end steps"}}
+                             "a step takes max of the three; the *_during_* times are the medians "
+                             "of the timed end-to-end steps"}}
 
 
 if __name__ == "__main__":
