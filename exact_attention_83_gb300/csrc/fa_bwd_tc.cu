@@ -214,8 +214,9 @@ __global__ void __launch_bounds__(320, 1)
     // Lane 0 issues the TMA copies.  For each query tile: Q into its Q slot,
     // then dO into its dO slot, where all 32 lanes also stage L * log2(e) and
     // Delta (4 rows per lane, read from global memory before the slot is
-    // free, so their latency overlaps the wait).  Rows past N get L = +inf,
-    // so their probabilities are exactly 0, and Delta = 0.
+    // free, so their latency overlaps the wait), both negated so that the
+    // elementwise warps add them directly.  Rows past N get L = +inf, so
+    // their probabilities are exactly 0, and Delta = 0.
     if (lane == 0) {
       tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
@@ -258,8 +259,8 @@ __global__ void __launch_bounds__(320, 1)
       for (int t = 0; t < 4; ++t) {
         const int64_t q = q0 + lane * 4 + t;
         const int64_t li = lse_index(a.g, sv, hq, q);
-        lv[t] = q < Nq ? a.lse[li] * kLog2e : INFINITY;
-        dv[t] = q < Nq ? a.delta[li] : 0.f;
+        lv[t] = q < Nq ? -a.lse[li] * kLog2e : -INFINITY;   // staged negated
+        dv[t] = q < Nq ? -a.delta[li] : 0.f;
       }
       const int ds = it % C::ND;
       const uint32_t dr = static_cast<uint32_t>(it / C::ND);
@@ -395,17 +396,25 @@ __global__ void __launch_bounds__(320, 1)
       // the dO slot's arrival also publishes the staged L and Delta
       if (!(ok = wait_warp(b_dfull0 + 8 * ds, (it / C::ND) & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
-      const float* L2s = reinterpret_cast<const float*>(sD + ds * C::DSLOT + C::TILE) + 64 * hf;
-      const float* Ds = L2s + 128;
+      // -L * log2(e) and -Delta of this half's 64 queries
+      const float* nL2s = reinterpret_cast<const float*>(sD + ds * C::DSLOT + C::TILE) + 64 * hf;
+      const float* nDs = nL2s + 128;
       float p[64];
       tmem_ld64(lane_base + C::COL_ST + 64 * hf, p);
+      {
+        // P = exp2(c * S - L * log2(e)), two queries per paired instruction
+        const uint64_t cc = f32x2(c, c);
 #pragma unroll
-      for (int q = 0; q < 64; q += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(L2s + q);
-        p[q] = ex2(fmaf(p[q], c, -l4.x));
-        p[q + 1] = ex2(fmaf(p[q + 1], c, -l4.y));
-        p[q + 2] = ex2(fmaf(p[q + 2], c, -l4.z));
-        p[q + 3] = ex2(fmaf(p[q + 3], c, -l4.w));
+        for (int q = 0; q < 64; q += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(nL2s + q);
+          float x0, x1, x2, x3;
+          f32x2_split(fma_f32x2(f32x2(p[q], p[q + 1]), cc, f32x2(l4.x, l4.y)), x0, x1);
+          f32x2_split(fma_f32x2(f32x2(p[q + 2], p[q + 3]), cc, f32x2(l4.z, l4.w)), x2, x3);
+          p[q] = ex2(x0);
+          p[q + 1] = ex2(x1);
+          p[q + 2] = ex2(x2);
+          p[q + 3] = ex2(x3);
+        }
       }
       if (a.causal && i == kt) {
         // diagonal tile: query (64*hf + q) attends to this key only if it is not earlier
@@ -460,16 +469,19 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int q = 0; q < 64; ++q) {
           const float z = ((keep >> q) & 1u) ? a.drop.rscale : 0.f;
-          dp[q] = p[q] * fmaf(z, dp[q], -Ds[q]);
+          dp[q] = p[q] * fmaf(z, dp[q], nDs[q]);
         }
       } else {
 #pragma unroll
         for (int q = 0; q < 64; q += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(Ds + q);
-          dp[q] = p[q] * (dp[q] - d4.x);
-          dp[q + 1] = p[q + 1] * (dp[q + 1] - d4.y);
-          dp[q + 2] = p[q + 2] * (dp[q + 2] - d4.z);
-          dp[q + 3] = p[q + 3] * (dp[q + 3] - d4.w);
+          // dS = P o (dP - Delta), two queries per paired instruction
+          const float4 d4 = *reinterpret_cast<const float4*>(nDs + q);
+          uint64_t a01 = add_f32x2(f32x2(dp[q], dp[q + 1]), f32x2(d4.x, d4.y));
+          uint64_t a23 = add_f32x2(f32x2(dp[q + 2], dp[q + 3]), f32x2(d4.z, d4.w));
+          a01 = mul_f32x2(a01, f32x2(p[q], p[q + 1]));
+          a23 = mul_f32x2(a23, f32x2(p[q + 2], p[q + 3]));
+          f32x2_split(a01, dp[q], dp[q + 1]);
+          f32x2_split(a23, dp[q + 2], dp[q + 3]);
         }
       }
       tmem_st_packed64<T>(lane_base + C::COL_DPT + 64 * hf, dp);
@@ -833,8 +845,17 @@ __global__ void __launch_bounds__(320, 1)
       int lim = 63;
       if (a.causal && jt == qt) lim = row - 64 * hf;
       if (jt == nk - 1) lim = min(lim, static_cast<int>(Nk - 1 - static_cast<int64_t>(jt) * C::BT) - 64 * hf);
+      {
+        // P = exp2(c * S - L * log2(e)), two keys per paired instruction
+        const uint64_t cc = f32x2(c, c), nl = f32x2(-l2, -l2);
 #pragma unroll
-      for (int q = 0; q < 64; ++q) p[q] = ex2(fmaf(p[q], c, -l2));
+        for (int q = 0; q < 64; q += 2) {
+          float x0, x1;
+          f32x2_split(fma_f32x2(f32x2(p[q], p[q + 1]), cc, nl), x0, x1);
+          p[q] = ex2(x0);
+          p[q + 1] = ex2(x1);
+        }
+      }
       if (lim < 63) {
 #pragma unroll
         for (int q = 0; q < 64; ++q)
@@ -852,8 +873,13 @@ __global__ void __launch_bounds__(320, 1)
           dp[q] = p[q] * fmaf(z, dp[q], -dl);
         }
       } else {
+        // dS = P o (dP - Delta), two keys per paired instruction
+        const uint64_t nd = f32x2(-dl, -dl);
 #pragma unroll
-        for (int q = 0; q < 64; ++q) dp[q] = p[q] * (dp[q] - dl);
+        for (int q = 0; q < 64; q += 2) {
+          const uint64_t x = mul_f32x2(add_f32x2(f32x2(dp[q], dp[q + 1]), nd), f32x2(p[q], p[q + 1]));
+          f32x2_split(x, dp[q], dp[q + 1]);
+        }
       }
       tmem_st_packed64<T>(lane_base + C::COL_DP + 64 * hf, dp);
       tmem_wait_st();
