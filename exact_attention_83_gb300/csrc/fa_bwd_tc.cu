@@ -392,6 +392,17 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     for (int it = 0; it < n; ++it) {
       const int i = i0 + it % per, ds = it % C::ND;
+      // Dropout keep bits, drawn before the scores arrive (they depend on
+      // positions only): bit q set iff weight (query 64*hf + q of this tile,
+      // this key) is kept.  The eight lanes of an octet hold eight
+      // consecutive keys, which one generator call covers for one query
+      // (octet_keep_bits).
+      uint64_t keep = 0;
+      if constexpr (DROP) {
+        const uint32_t bhq = static_cast<uint32_t>(bseq * a.g.Hq + hk * a.g.G + g0 + it / per);
+        keep = octet_keep_bits(a.drop, static_cast<uint32_t>(key >> 3),
+                               static_cast<int64_t>(i) * C::BT + 64 * hf, bhq, lane);
+      }
       if (!(ok = wait_warp(b_sfull, it & 1, ctl, a.status, a.timeout_ns))) break;
       // the dO slot's arrival also publishes the staged L and Delta
       if (!(ok = wait_warp(b_dfull0 + 8 * ds, (it / C::ND) & 1, ctl, a.status, a.timeout_ns))) break;
@@ -421,31 +432,6 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int q = 0; q < 64; ++q)
           if (64 * hf + q < row) p[q] = 0.f;
-      }
-      // Dropout keep bits: bit q set iff weight (query 64*hf + q of this
-      // tile, this key) is kept.
-      // The eight lanes of an octet hold eight consecutive keys, which one
-      // generator call covers for one query.  Lane e of the octet draws for
-      // query 8t + e, the octet exchanges the eight 8-bit results, and each
-      // lane keeps the bit of its own key for the eight queries.
-      uint64_t keep = 0;
-      if constexpr (DROP) {
-        const uint32_t bhq = static_cast<uint32_t>(bseq * a.g.Hq + hk * a.g.G + g0 + it / per);
-        const uint32_t jg = static_cast<uint32_t>(key >> 3);
-        const int e = lane & 7;
-        const int64_t qbase = static_cast<int64_t>(i) * C::BT + 64 * hf;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          uint64_t x = static_cast<uint64_t>(
-                           keep8(a.drop, jg, static_cast<uint32_t>(qbase + 8 * t + e), bhq))
-                       << (8 * e);
-          x |= __shfl_xor_sync(0xffffffffu, x, 1);
-          x |= __shfl_xor_sync(0xffffffffu, x, 2);
-          x |= __shfl_xor_sync(0xffffffffu, x, 4);
-          // bit 8 * e' + e of x is (query 8t + e', this key); gather them
-          const uint64_t y = (x >> e) & 0x0101010101010101ull;
-          keep |= ((y * 0x0102040810204080ull) >> 56) << (8 * t);
-        }
       }
       if constexpr (DROP) {
         float pd[64];

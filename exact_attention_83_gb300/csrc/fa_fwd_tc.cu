@@ -299,13 +299,22 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tO = lane_base + C::COL_O0 + D * g;
     const float c = a.c;
     float m = -INFINITY, l = 0.f;
-    uint32_t keepq = 0;            // dropout: keep bits of the current group of eight keys
-    (void)keepq;
     bool ok = true;
     const int n = ntile[g];
     // last valid key column of the last key tile
     const int lim_last = static_cast<int>(Nk - 1 - static_cast<int64_t>(nk - 1) * C::BN);
     for (int j = 0; j < n; ++j) {
+      // Dropout keep bits of this row's 128 keys, drawn before the scores
+      // arrive (positions only): bit k of kb[k / 32] is key j*128 + k; one
+      // generator call covers eight keys.
+      uint32_t kb[4] = {0u, 0u, 0u, 0u};
+      if constexpr (DROP) {
+#pragma unroll
+        for (int g8 = 0; g8 < 16; ++g8)
+          kb[g8 >> 2] |= keep8(a.drop, static_cast<uint32_t>(j * 16 + g8),
+                               static_cast<uint32_t>(qrow), static_cast<uint32_t>(bh))
+                         << (8 * (g8 & 3));
+      }
       if (!(ok = wait_warp(b_sfull0 + 8 * g, j & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
       float s[128];
@@ -377,13 +386,9 @@ __global__ void __launch_bounds__(320, 1)
           const float p0 = ex2(x0), p1 = ex2(x1);
           acc = add_f32x2(acc, f32x2(p0, p1));
           if constexpr (DROP) {
-            // l sums the undropped weights; P V takes the dropped, rescaled
-            // ones; one generator call covers eight keys
-            const int key = j * C::BN + 64 * hh + 2 * i;
-            if ((i & 3) == 0)
-              keepq = keep8(a.drop, static_cast<uint32_t>(key >> 3), static_cast<uint32_t>(qrow),
-                            static_cast<uint32_t>(bh));
-            const uint32_t bits = keepq >> (2 * (i & 3));
+            // l sums the undropped weights; P V takes the dropped, rescaled ones
+            const int kk = 64 * hh + 2 * i;
+            const uint32_t bits = kb[kk >> 5] >> (kk & 31);
             pk[i] = pack2<T>((bits & 1u) ? p0 * a.drop.rscale : 0.f,
                              (bits & 2u) ? p1 * a.drop.rscale : 0.f);
           } else {
@@ -430,430 +435,6 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-}
-
-// ============================================================================
-// D = 128: CTA pairs (cta_group::2)
-// ============================================================================
-// A cluster of two CTAs works on four query tiles of one head: CTA r holds
-// query tiles 4p + r (its tile 0) and 4p + 2 + r (its tile 1), 256 rows, and
-// the pair shares every key tile.  CTA 0's MMA thread issues each product once
-// for both CTAs with M = 256 (rows 0-127 from CTA 0, rows 128-255 from CTA 1):
-// S_g = [Q_g of CTA 0; Q_g of CTA 1] K^T lands in each CTA's own tensor
-// memory, and O_g += P_g V reads each CTA's own P.  The B operands are split
-// between the CTAs: CTA r loads keys 64r .. 64r+63 of each K tile (N of S) and
-// head-dimension columns 64r .. 64r+63 of each V tile (N of P V), so every SM
-// stages and streams half of each K / V tile.  Against one CTA issuing
-// M = 128 products this halves the shared-memory traffic the tensor cores
-// read for B and the bytes the copy engine writes per SM, which otherwise
-// saturate shared memory together with the A operand reads; it also leaves
-// room for an 8-slot ring of half tiles (four key tiles in flight).
-//
-// Hand-offs between the CTAs: each CTA loads its own halves with its own
-// mbarriers; in CTA 1 the otherwise idle MMA warp relays each completed load
-// to a barrier of CTA 0 (remote arrive), on which CTA 0's MMA thread waits as
-// well.  Commits of the MMA thread arrive on the same barrier of both CTAs
-// (S ready, O final, ring slot free).  The softmax warps of CTA 1 report P
-// written with one remote arrive per warp on CTA 0's barrier.  Every wait is
-// bounded; a CTA that gives up drains its own copies, and both CTAs meet at a
-// final cluster barrier (reached by every thread, also after a timeout)
-// before the tensor memory is released, so no CTA leaves while the other's
-// products may still read its shared or tensor memory.
-struct FwdPairCfg {
-  static constexpr int D = 128;
-  static constexpr int BM = 128, BN = 128;
-  static constexpr int QCHUNK = BM * 128;           // 16 KB: 128 rows x 64 columns
-  static constexpr int QTILE = 2 * QCHUNK;          // one 128 x 128 query tile
-  static constexpr int HALF = 16384;                // one K or V half tile
-  static constexpr int KCHUNK = 64 * 128;           // 8 KB: 64 key rows x 64 columns
-  static constexpr int NS = 8;                      // ring slots (half tiles)
-  static constexpr int OFF_RING = 2 * QTILE;
-  static constexpr int OFF_BAR = OFF_RING + NS * HALF;
-  static constexpr int SMEM = OFF_BAR + 1024 + 1024;
-  static constexpr int THREADS = 320;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S0 = 0, COL_O0 = 256;
-};
-
-struct FwdPairArgs {
-  FwdTcArgs a;
-  int64_t nquads;          // groups of four query tiles of the longest sequence
-};
-
-template <typename T, bool DROP>
-__global__ void __launch_bounds__(320, 1)
-    fwd_pair_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv, const FwdPairArgs pa) {
-  using C = FwdPairCfg;
-  constexpr int D = C::D;
-  const FwdTcArgs& a = pa.a;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sRing = smem + C::OFF_RING;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  Ctl* ctl = reinterpret_cast<Ctl*>(bars + 40);
-  const uint32_t b_q = smem_u32(&bars[0]);                       // own Q tiles landed
-  const uint32_t b_qpair = smem_u32(&bars[1]);                   // CTA 0: CTA 1's Q landed
-  const uint32_t b_full0 = smem_u32(&bars[2]);                   // + 8 * slot: own half landed
-  const uint32_t b_pfull0 = smem_u32(&bars[2 + C::NS]);          // + 8 * slot: CTA 1's half (CTA 0)
-  const uint32_t b_empty0 = smem_u32(&bars[2 + 2 * C::NS]);      // + 8 * slot: slot free
-  const uint32_t b_sfull0 = smem_u32(&bars[2 + 3 * C::NS]);      // + 8 * g
-  const uint32_t b_pready0 = smem_u32(&bars[4 + 3 * C::NS]);     // + 8 * g (CTA 0)
-  const uint32_t b_ofinal0 = smem_u32(&bars[6 + 3 * C::NS]);     // + 8 * g
-  const uint32_t b_mmadone = smem_u32(&bars[8 + 3 * C::NS]);
-  static_assert(9 + 3 * C::NS <= 40, "barriers below the control block");
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();
-  const int64_t cid = blockIdx.x >> 1;
-  const int64_t bh = cid % a.BH;                 // b * Hq + h
-  const int64_t pq = a.causal ? (pa.nquads - 1 - cid / a.BH) : (cid / a.BH);
-  const int64_t h = bh % a.g.Hq;
-  const SeqView sv = seq_view(a.g, bh / a.g.Hq);
-  // Every early exit below depends only on what both CTAs of the pair share.
-  if (!sv.ok) {
-    if (threadIdx.x == 0) record_status(a.status, FA_ERR_SEQLENS);
-    return;
-  }
-  const int64_t Nq = sv.nq, Nk = sv.nk;
-  if (4 * pq * C::BM >= Nq) return;            // all four query tiles lie past the sequence
-  const int32_t hq = static_cast<int32_t>(h), hk = static_cast<int32_t>(h / a.g.G);
-  const int32_t bb = static_cast<int32_t>(sv.b);
-  const int nk = static_cast<int>((Nk + C::BN - 1) / C::BN);
-  int ntile[2];   // key tiles of the pair's tile g (query tiles 4p + 2g and 4p + 2g + 1)
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    const int64_t first = 4 * pq + 2 * g;
-    const int64_t diag = first + 2;
-    ntile[g] = (first * C::BM >= Nq) ? 0
-                                     : (a.causal ? static_cast<int>(diag < nk ? diag : nk) : nk);
-  }
-  const int nmax = max(ntile[0], ntile[1]);
-  if (nmax == 0) {
-    // No key at all (an empty key sequence): O = 0 and L = -inf.
-    if (warp < 8) {
-      const int64_t qrow = (4 * pq + 2 * (warp >> 2) + rank) * C::BM + (warp & 3) * 32 + lane;
-      if (qrow < Nq) {
-        T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qrow) * a.so[2];
-        for (int d = 0; d < a.dreal; ++d) orow[d] = Elem<T>::from_f32(0.f);
-        a.lse[lse_index(a.g, sv, h, qrow)] = -INFINITY;
-      }
-    }
-    return;
-  }
-
-  if (threadIdx.x == 0) {
-    mbar_init(b_q, 1);
-    mbar_init(b_qpair, 1);
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(b_full0 + 8 * s, 1);
-      mbar_init(b_pfull0 + 8 * s, 1);
-      mbar_init(b_empty0 + 8 * s, 1);
-    }
-    for (int g = 0; g < 2; ++g) {
-      mbar_init(b_sfull0 + 8 * g, 1);
-      mbar_init(b_pready0 + 8 * g, 8);   // one arrive per softmax warp of either CTA
-      mbar_init(b_ofinal0 + 8 * g, 1);
-    }
-    mbar_init(b_mmadone, 1);
-    ctl->abort = 0;
-    mbar_fence_init();
-  }
-  if (warp == 8) {
-    tmem_alloc_pair(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
-    tmem_relinquish_pair();
-  }
-  tc_fence_before();
-  __syncthreads();
-  // Both CTAs' barriers and tensor memory exist before either CTA signals the
-  // other or issues a product.
-  cluster_sync_all();
-  tc_fence_after();
-  const uint32_t tmem = ctl->tmem_base;
-
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer (each CTA)
-    if (lane == 0) {
-      tma_prefetch_desc(&tmq);
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
-      uint32_t issued[C::NS];
-#pragma unroll
-      for (int s = 0; s < C::NS; ++s) issued[s] = 0;
-      mbar_arrive_expect_tx(b_q, (ntile[0] > 0 ? C::QTILE : 0) + (ntile[1] > 0 ? C::QTILE : 0));
-      for (int g = 0; g < 2; ++g) {
-        if (ntile[g] == 0) continue;
-        for (int c = 0; c < 2; ++c)
-          tma_load_4d(smem_u32(sQ + g * C::QTILE + c * C::QCHUNK), &tmq, b_q, c * 64,
-                      static_cast<int32_t>(sv.q0 + (4 * pq + 2 * g + rank) * C::BM), hq, bb);
-      }
-      bool ok = true;
-      for (int j = 0; ok && j < nmax; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int u = 2 * j + kv, s = u % C::NS;
-          const uint32_t r = static_cast<uint32_t>(u / C::NS);
-          if (r > 0 && !(ok = wait_bounded(b_empty0 + 8 * s, (r - 1) & 1, ctl, a.status,
-                                           a.timeout_ns)))
-            break;
-          mbar_arrive_expect_tx(b_full0 + 8 * s, C::HALF);
-          uint8_t* dst = sRing + s * C::HALF;
-          const int32_t k0 = static_cast<int32_t>(sv.k0 + j * C::BN);
-          if (kv == 0) {
-            // keys 64r .. 64r+63 of K_j, both 64-column chunks
-            for (int c = 0; c < 2; ++c)
-              tma_load_4d(smem_u32(dst + c * C::KCHUNK), &tmk, b_full0 + 8 * s, c * 64,
-                          k0 + 64 * static_cast<int32_t>(rank), hk, bb);
-          } else {
-            // columns 64r .. 64r+63 of V_j, all 128 keys
-            tma_load_4d(smem_u32(dst), &tmv, b_full0 + 8 * s, 64 * static_cast<int32_t>(rank), k0,
-                        hk, bb);
-          }
-          issued[s] = r + 1;
-        }
-      }
-      // Drain: every copy this CTA issued has landed before it may leave.
-      wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns, false);
-      for (int s = 0; s < C::NS; ++s)
-        if (issued[s]) wait_bounded(b_full0 + 8 * s, (issued[s] - 1) & 1, ctl, a.status,
-                                    a.timeout_ns, false);
-    }
-    __syncwarp();
-  } else if (warp == 9 && rank == 1) {
-    // ------------------------------------------------------------ relay (CTA 1)
-    // Tells CTA 0's MMA thread that this CTA's share of an operand has landed.
-    if (lane == 0) {
-      const uint32_t q_remote = cluster_map(b_qpair, 0);
-      bool ok = wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns);
-      if (ok) mbar_arrive_remote(q_remote);
-      for (int u = 0; ok && u < 2 * nmax; ++u) {
-        const int s = u % C::NS;
-        if (!(ok = wait_bounded(b_full0 + 8 * s, static_cast<uint32_t>(u / C::NS) & 1, ctl,
-                                a.status, a.timeout_ns)))
-          break;
-        mbar_arrive_remote(cluster_map(b_pfull0 + 8 * s, 0));
-      }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer (CTA 0)
-    if (lane == 0) {
-      const uint32_t idS = idesc_f16<T>(256, C::BN, false, false);
-      const uint32_t idO = idesc_f16<T>(256, D, false, true);
-      const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dK0 = sdesc_sw128(smem_u32(sRing), 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(smem_u32(sRing), C::HALF, 1024);
-      auto issue_S = [&](int g, int slot) {
-        const uint64_t qa = dQ0 + static_cast<uint64_t>((g * C::QTILE) >> 4);
-        const uint64_t kb = dK0 + static_cast<uint64_t>((slot * C::HALF) >> 4);
-        const uint32_t d = tmem + C::COL_S0 + 128 * g;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t oq = ((kk >> 2) * C::QCHUNK + (kk & 3) * 32) >> 4;
-          const uint32_t ok_ = ((kk >> 2) * C::KCHUNK + (kk & 3) * 32) >> 4;
-          mma_ss_pair(d, qa + oq, kb + ok_, idS, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_PV = [&](int g, int slot, bool acc) {
-        const uint64_t vb = dV0 + static_cast<uint64_t>((slot * C::HALF) >> 4);
-        const uint32_t d = tmem + C::COL_O0 + D * g, p = tmem + C::COL_S0 + 128 * g;
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts_pair(d, p + kk * 8, vb + static_cast<uint64_t>((kk * 2048) >> 4), idO,
-                      (acc || kk > 0) ? 1u : 0u);
-      };
-      // Both CTAs' share of unit u (ring slot u % NS, round u / NS) has landed.
-      auto wait_unit = [&](int u) {
-        const int s = u % C::NS;
-        const uint32_t par = static_cast<uint32_t>(u / C::NS) & 1;
-        return wait_bounded(b_full0 + 8 * s, par, ctl, a.status, a.timeout_ns) &&
-               wait_bounded_cluster(b_pfull0 + 8 * s, par, ctl, a.status, a.timeout_ns);
-      };
-      bool ok = wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns) &&
-                wait_bounded_cluster(b_qpair, 0, ctl, a.status, a.timeout_ns) && wait_unit(0);
-      if (ok) {
-        tc_fence_after();
-        for (int g = 0; g < 2; ++g)
-          if (ntile[g] > 0) {
-            issue_S(g, 0);
-            // A test can withhold this arrival in the first pair to make the
-            // softmax warps' bounded wait run out (the timeout path, without a fault).
-            if (!(a.withhold_arrival && blockIdx.x == 0 && g == 0)) mma_commit_pair_both(b_sfull0 + 8 * g);
-          }
-        mma_commit_pair_both(b_empty0);
-      }
-      for (int j = 0; ok && j < nmax; ++j) {
-        const int uV = 2 * j + 1, sV = uV % C::NS;
-        const int uK = 2 * j + 2, sK = uK % C::NS;
-        const bool next = j + 1 < nmax;
-        ok = wait_unit(uV);
-        if (ok && next) ok = wait_unit(uK);
-        if (!ok) break;
-        tc_fence_after();
-        for (int g = 0; g < 2; ++g) {
-          if (j >= ntile[g]) continue;
-          if (!(ok = wait_bounded_cluster(b_pready0 + 8 * g, j & 1, ctl, a.status, a.timeout_ns)))
-            break;
-          tc_fence_after();
-          issue_PV(g, sV, j > 0);
-          if (j + 1 < ntile[g]) {
-            issue_S(g, sK);
-            mma_commit_pair_both(b_sfull0 + 8 * g);
-          } else {
-            mma_commit_pair_both(b_ofinal0 + 8 * g);
-          }
-        }
-        if (!ok) break;
-        mma_commit_pair_both(b_empty0 + 8 * sV);
-        if (next) mma_commit_pair_both(b_empty0 + 8 * sK);
-      }
-      // Drain: every product (and every commit arrival) of this thread is complete.
-      mma_commit_pair_local(b_mmadone);
-      wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
-    }
-    __syncwarp();
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int g = warp >> 2, quarter = warp & 3;
-    const int r = quarter * 32 + lane;                       // row in the query tile
-    const int64_t qt = 4 * pq + 2 * g + rank;
-    const int64_t qrow = qt * C::BM + r;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t tS = lane_base + C::COL_S0 + 128 * g;
-    const uint32_t tO = lane_base + C::COL_O0 + D * g;
-    const uint32_t ready = rank == 0 ? (b_pready0 + 8 * g) : cluster_map(b_pready0 + 8 * g, 0);
-    const float c = a.c;
-    float m = -INFINITY, l = 0.f;
-    uint32_t keepq = 0;            // dropout: keep bits of the current group of eight keys
-    (void)keepq;
-    bool ok = true;
-    const int n = ntile[g];
-    // last valid key column of the last key tile
-    const int lim_last = static_cast<int>(Nk - 1 - static_cast<int64_t>(nk - 1) * C::BN);
-    for (int j = 0; j < n; ++j) {
-      if (!(ok = wait_warp(b_sfull0 + 8 * g, j & 1, ctl, a.status, a.timeout_ns))) break;
-      tc_fence_after();
-      float s[128];
-      {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(tS + 0, r0);
-        tmem_ld32(tS + 32, r1);
-        tmem_ld32(tS + 64, r2);
-        tmem_ld32(tS + 96, r3);
-        tmem_wait_ld();
-        reg_fence32(r0); reg_fence32(r1); reg_fence32(r2); reg_fence32(r3);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(r0[i]);
-          s[32 + i] = __uint_as_float(r1[i]);
-          s[64 + i] = __uint_as_float(r2[i]);
-          s[96 + i] = __uint_as_float(r3[i]);
-        }
-      }
-      // Exclude keys past N (last key tile) and keys after the query: the
-      // diagonal tile, and for CTA 0 the pair's last tile, which lies wholly
-      // after its queries.
-      int lim = C::BN - 1;
-      if (a.causal && j == qt) lim = r;
-      if (a.causal && j > qt) lim = -1;
-      if (j == nk - 1) lim = min(lim, lim_last);
-      if (lim < C::BN - 1) {
-#pragma unroll
-        for (int kk = 0; kk < C::BN; ++kk)
-          if (kk > lim) s[kk] = -INFINITY;
-      }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-      for (int kk = 4; kk < C::BN; kk += 4) {
-        mx0 = fmaxf(mx0, s[kk]);
-        mx1 = fmaxf(mx1, s[kk + 1]);
-        mx2 = fmaxf(mx2, s[kk + 2]);
-        mx3 = fmaxf(mx3, s[kk + 3]);
-      }
-      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
-      // Lazy rescale decision (warp-uniform for the TMEM access below).
-      bool rescale = false;
-      float alpha = 1.f;
-      if (j == 0) {
-        m = m_new;
-      } else {
-        const bool need = m_new > m + 8.f;
-        rescale = __any_sync(0xffffffffu, need);
-        if (need) {
-          alpha = ex2(m - m_new);
-          l *= alpha;
-          m = m_new;
-        }
-      }
-      const float negm = -m;
-      float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(s[64 * half + 2 * i], c, negm));
-          const float p1 = ex2(fmaf(s[64 * half + 2 * i + 1], c, negm));
-          sum0 += p0;
-          sum1 += p1;
-          if constexpr (DROP) {
-            const int key = j * C::BN + 64 * half + 2 * i;
-            if ((i & 3) == 0)
-              keepq = keep8(a.drop, static_cast<uint32_t>(key >> 3), static_cast<uint32_t>(qrow),
-                            static_cast<uint32_t>(bh));
-            const uint32_t bits = keepq >> (2 * (i & 3));
-            pk[i] = pack2<T>((bits & 1u) ? p0 * a.drop.rscale : 0.f,
-                             (bits & 2u) ? p1 * a.drop.rscale : 0.f);
-          } else {
-            pk[i] = pack2<T>(p0, p1);
-          }
-        }
-        tmem_st32(tS + 32 * half, pk);
-      }
-      // O *= alpha once the scores are dead (PV_j is not issued before the
-      // arrival below, and PV_{j-1} completed before S_j did).
-      if (rescale) {
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t t[32];
-          tmem_ld32(tO + 32 * cc, t);
-          tmem_wait_ld();
-          reg_fence32(t);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
-          tmem_st32(tO + 32 * cc, t);
-        }
-      }
-      tmem_wait_st();
-      l += sum0 + sum1;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (rank == 0) mbar_arrive(ready);
-        else mbar_arrive_remote(ready);
-      }
-    }
-    if (ok && n > 0) ok = wait_warp(b_ofinal0 + 8 * g, 0, ctl, a.status, a.timeout_ns);
-    if (ok && n > 0) {
-      tc_fence_after();
-      const float inv = 1.f / l;
-      const bool store = qrow < Nq;
-      T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qrow) * a.so[2];
-      store_row_cols<T>(tO, inv, orow, store, a.dreal);
-      if (store) a.lse[lse_index(a.g, sv, h, qrow)] = (m + log2f(l)) * kLn2;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  // Every thread of both CTAs arrives here, also after a timeout: neither CTA
-  // releases its memory while the pair's products may still use it.
-  cluster_sync_all();
-  if (warp == 8) {
-    tc_fence_after();
-    tmem_dealloc_pair(tmem, C::TMEM_COLS);
   }
 }
 
@@ -1069,12 +650,20 @@ __global__ void __launch_bounds__(192, 2)
     const uint32_t tP = lane_base + C::COL_P;
     const float c = a.c;
     float m = -INFINITY, l = 0.f;
-    uint32_t keepq = 0;            // dropout: keep bits of the current group of eight keys
-    (void)keepq;
     bool ok = true;
     // last valid key column of the last key tile
     const int lim_last = static_cast<int>(Nk - 1 - static_cast<int64_t>(nk - 1) * C::BN);
     for (int j = 0; j < n; ++j) {
+      // Dropout keep bits of this row's 128 keys, drawn before the scores
+      // arrive (positions only): bit k of kb[k / 32] is key j*128 + k.
+      uint32_t kb[4] = {0u, 0u, 0u, 0u};
+      if constexpr (DROP) {
+#pragma unroll
+        for (int g8 = 0; g8 < 16; ++g8)
+          kb[g8 >> 2] |= keep8(a.drop, static_cast<uint32_t>(j * 16 + g8),
+                               static_cast<uint32_t>(qrow), static_cast<uint32_t>(bh))
+                         << (8 * (g8 & 3));
+      }
       if (!(ok = wait_warp(b_sfull, j & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
       float s[128];
@@ -1107,13 +696,13 @@ __global__ void __launch_bounds__(192, 2)
         for (int kk = 0; kk < C::BN; ++kk)
           if (kk > lim) s[kk] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int kk = 4; kk < C::BN; kk += 4) {
-        mx0 = fmaxf(mx0, s[kk]);
-        mx1 = fmaxf(mx1, s[kk + 1]);
-        mx2 = fmaxf(mx2, s[kk + 2]);
-        mx3 = fmaxf(mx3, s[kk + 3]);
+      for (int kk = 0; kk < C::BN; kk += 8) {
+        mx0 = max3f(mx0, s[kk], s[kk + 1]);
+        mx1 = max3f(mx1, s[kk + 2], s[kk + 3]);
+        mx2 = max3f(mx2, s[kk + 4], s[kk + 5]);
+        mx3 = max3f(mx3, s[kk + 6], s[kk + 7]);
       }
       const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c);
       // Lazy rescale decision (warp-uniform for the TMEM access below).
@@ -1131,7 +720,9 @@ __global__ void __launch_bounds__(192, 2)
         }
       }
       const float negm = -m;
-      float sum0 = 0.f, sum1 = 0.f;
+      // paired fp32: c * s - m and the row sum two keys at a time
+      const uint64_t cc = f32x2(c, c), nm = f32x2(negm, negm);
+      uint64_t acc = f32x2(0.f, 0.f);
       // P in two halves of 64 keys (32 columns each); the first half waits
       // (in registers) until P_{j-1} V has finished reading the P columns,
       // which also makes O stable for a rescale.
@@ -1140,18 +731,15 @@ __global__ void __launch_bounds__(192, 2)
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(s[64 * half + 2 * i], c, negm));
-          const float p1 = ex2(fmaf(s[64 * half + 2 * i + 1], c, negm));
-          sum0 += p0;
-          sum1 += p1;
+          float x0, x1;
+          f32x2_split(fma_f32x2(f32x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), cc, nm),
+                      x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          acc = add_f32x2(acc, f32x2(p0, p1));
           if constexpr (DROP) {
-            // l sums the undropped weights; P V takes the dropped, rescaled
-            // ones; one generator call covers eight keys
-            const int key = j * C::BN + 64 * half + 2 * i;
-            if ((i & 3) == 0)
-              keepq = keep8(a.drop, static_cast<uint32_t>(key >> 3), static_cast<uint32_t>(qrow),
-                            static_cast<uint32_t>(bh));
-            const uint32_t bits = keepq >> (2 * (i & 3));
+            // l sums the undropped weights; P V takes the dropped, rescaled ones
+            const int kk = 64 * half + 2 * i;
+            const uint32_t bits = kb[kk >> 5] >> (kk & 31);
             pk[i] = pack2<T>((bits & 1u) ? p0 * a.drop.rscale : 0.f,
                              (bits & 2u) ? p1 * a.drop.rscale : 0.f);
           } else {
@@ -1163,21 +751,25 @@ __global__ void __launch_bounds__(192, 2)
           tc_fence_after();
           if (rescale) {
 #pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int c4 = 0; c4 < D / 32; ++c4) {
               uint32_t t[32];
-              tmem_ld32(tO + 32 * cc, t);
+              tmem_ld32(tO + 32 * c4, t);
               tmem_wait_ld();
               reg_fence32(t);
 #pragma unroll
               for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
-              tmem_st32(tO + 32 * cc, t);
+              tmem_st32(tO + 32 * c4, t);
             }
           }
         }
         tmem_st32(tP + 32 * half, pk);
       }
       if (!ok) break;
-      l += sum0 + sum1;
+      {
+        float lo, hi;
+        f32x2_split(acc, lo, hi);
+        l += lo + hi;
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(b_pready);
