@@ -56,10 +56,10 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 1044.4 MB per launch measured on 16 heads,
+    # bwd_dkdv_tc_kernel<bf16,128>: 1043.5 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("dkdv", "b0ea44ade0ac72e28681384579b0a7ea7b7feb98e06e3419274f8130a4a2e383",
-     "long-bf16-B1-H32-N16384-D128-causal"): 2088.7e6,
+    ("dkdv", "cceba2cb0f83c8bf0caeb6d6260e510482fe8a208d01b7a4097f485c3c3df0a9",
+     "long-bf16-B1-H32-N16384-D128-causal"): 2087.0e6,
     # bwd_fused_tc_kernel<bf16,128>: 2927.0 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
     ("fused", "4e901d50139ef9df1f0a88bcfd2e6a96d1aa4d40c654be868c696ba22ad5f3bb",
