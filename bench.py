@@ -245,6 +245,9 @@ def main():
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the sequence-length sweep record of the default run")
     ap.add_argument("--bwd", default="split", choices=["split", "fused"])
+    ap.add_argument("--dropout-in-kernels", action="store_true",
+                    help="dropout workloads: the backward kernels draw the keep decisions "
+                         "again instead of reading the keep mask the forward stored")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -473,6 +476,14 @@ def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
     fused = args.bwd == "fused"
     ws = (torch.empty(fa.workspace_bytes(q, k, w.causal, w.scale, **kw) // 4,
                       dtype=torch.float32, device=dev) if fused else None)
+    # Dropout: by default the forward stores the keep decisions it draws in a
+    # keep mask that the backward reads; with --dropout-in-kernels the
+    # backward kernels draw them again.
+    mask = None
+    if w.dropout_p > 0 and not args.dropout_in_kernels:
+        mask = torch.empty(fa.dropout_mask_bytes(q, k, w.causal, w.scale, **kw),
+                           dtype=torch.uint8, device=dev)
+        kw["dropout_mask"] = mask
 
     def bwd():
         if fused:
@@ -534,6 +545,11 @@ def run_general(args, w: GeneralWorkload, world: int, rank: int, local: int):
                        "Nk": w.Nk, "D": w.D, "causal": w.causal, "packed": w.packed,
                        "dropout_p": w.dropout_p, "parallelism": f"replicas{world}",
                        "backward": BWD_NAMES[args.bwd],
+                       "dropout_decisions": (None if w.dropout_p == 0 else
+                                             "drawn by the forward and again by the backward"
+                                             if mask is None else
+                                             "drawn by the forward, stored in a keep mask the "
+                                             "backward reads"),
                        "flops": "4*D*Hq*(attended pairs), backward credited 2.5x"},
             "fwd_tflops": w.fwd_flops() / (fwd_ms * 1e-3) / 1e12, "fwd_ms": fwd_ms,
             "fwd_frac_of_peak": w.fwd_flops() / (fwd_ms * 1e-3) / 1e12 / peak,

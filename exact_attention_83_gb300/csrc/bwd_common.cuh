@@ -34,28 +34,59 @@ __device__ __forceinline__ void tmem_st_packed64(uint32_t taddr, const float (&x
   tmem_st32(taddr, w);
 }
 
+// The octet's exchange: lane e' of the octet (lane & 7) holds `bits`, the
+// 8-bit keep decisions of query 8t + e' for the octet's eight consecutive
+// keys; returns, for this lane's key (bit e = lane & 7), the decisions of the
+// eight queries 8t .. 8t + 7 as bits 0..7.  Three shuffles and a bit gather;
+// every lane of the warp must call it.
+__device__ __forceinline__ uint64_t octet_gather8(uint32_t bits, int e) {
+  uint64_t x = static_cast<uint64_t>(bits) << (8 * e);
+  x |= __shfl_xor_sync(0xffffffffu, x, 1);
+  x |= __shfl_xor_sync(0xffffffffu, x, 2);
+  x |= __shfl_xor_sync(0xffffffffu, x, 4);
+  // bit 8 * e' + e of x is (query 8t + e', this key); gather them
+  const uint64_t y = (x >> e) & 0x0101010101010101ull;
+  return (y * 0x0102040810204080ull) >> 56;
+}
+
 // Dropout keep bits of the key held by this lane for 64 consecutive queries
 // qbase .. qbase + 63 of flat head bhq: bit q set iff weight (qbase + q, key)
 // is kept.  The eight lanes of an octet hold eight consecutive keys
 // 8*jg .. 8*jg + 7, which one generator call covers for one query: lane e of
-// the octet draws for query qbase + 8t + e, the octet exchanges the eight
-// 8-bit results with three shuffles, and each lane gathers the bit of its own
-// key for the eight queries.  Every lane of the warp must call it.
+// the octet draws for query qbase + 8t + e and the octet exchanges the
+// results (octet_gather8).  Every lane of the warp must call it.
 __device__ __forceinline__ uint64_t octet_keep_bits(const Dropout& d, uint32_t jg, int64_t qbase,
                                                     uint32_t bhq, int lane) {
   const int e = lane & 7;
   uint64_t keep = 0;
 #pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    uint64_t x = static_cast<uint64_t>(keep8(d, jg, static_cast<uint32_t>(qbase + 8 * t + e), bhq))
-                 << (8 * e);
-    x |= __shfl_xor_sync(0xffffffffu, x, 1);
-    x |= __shfl_xor_sync(0xffffffffu, x, 2);
-    x |= __shfl_xor_sync(0xffffffffu, x, 4);
-    // bit 8 * e' + e of x is (query 8t + e', this key); gather them
-    const uint64_t y = (x >> e) & 0x0101010101010101ull;
-    keep |= ((y * 0x0102040810204080ull) >> 56) << (8 * t);
-  }
+  for (int t = 0; t < 8; ++t)
+    keep |= octet_gather8(keep8(d, jg, static_cast<uint32_t>(qbase + 8 * t + e), bhq), e) << (8 * t);
+  return keep;
+}
+
+// The same bits read from the keep mask (Dropout::mask), in two steps so the
+// loads can be issued a step ahead: octet_mask_load reads, for query head h
+// of sequence v, key tile jt, the octet's byte `gbyte` (key group mod 16) of
+// the 16-byte entries of queries qbase .. qbase + 63 (lane e of the octet
+// reads queries qbase + 8t + e; queries past the sequence read as dropped),
+// and octet_mask_bits exchanges them within the octet as for drawn bits.
+// Every lane of the warp must call octet_mask_bits.
+__device__ __forceinline__ void octet_mask_load(const Dropout& d, const Geo& g, const SeqView& v,
+                                                int64_t h, int64_t jt, int64_t qbase, int gbyte,
+                                                int lane, uint32_t (&b)[8]) {
+  const int e = lane & 7;
+  const uint8_t* col = d.mask + mask_entry(d, g, v, h, jt, qbase) + gbyte;
+#pragma unroll
+  for (int t = 0; t < 8; ++t)
+    b[t] = qbase + 8 * t + e < v.nq ? static_cast<uint32_t>(__ldg(col + (8 * t + e) * 16)) : 0u;
+}
+
+__device__ __forceinline__ uint64_t octet_mask_bits(const uint32_t (&b)[8], int lane) {
+  const int e = lane & 7;
+  uint64_t keep = 0;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) keep |= octet_gather8(b[t], e) << (8 * t);
   return keep;
 }
 

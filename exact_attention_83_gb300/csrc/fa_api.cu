@@ -176,6 +176,12 @@ fa_status check_problem(const fa_problem* pr, Problem* out) {
       d.rk0[r] = d.key0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
       d.rk1[r] = d.key1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
     }
+    if (pr->dropout_mask) {
+      if (reinterpret_cast<uintptr_t>(pr->dropout_mask) % 16 != 0) return FA_ERR_ALIGN;
+      if (dropout_mask_bytes(g) == 0) return FA_ERR_SHAPE;
+      d.mask = pr->dropout_mask;
+      d.mask_kt = (g.Nk + 127) / 128;
+    }
   }
   out->g = g; out->D = D; out->causal = pr->causal ? 1 : 0; out->scale = pr->scale;
   out->dtype = dt; out->drop = d;
@@ -200,9 +206,14 @@ fa_status run_fwd(const Problem& pb, const void* q, const int64_t* sq, const voi
   p.status = dev->status; p.timeout_ns = g_timeout_ns.load();
   if (use_tc(pb.dtype) && have_fwd_tc(pb.D, pb.dtype)) {
     p.withhold_arrival = g_withhold_next.exchange(0);
-    return launch_fwd_tc(p, stream);
+    return launch_fwd_tc(p, stream);   // stores the keep mask as it draws it
   }
-  return launch_fwd_ffma(p, stream);
+  FA_TRY(launch_fwd_ffma(p, stream));
+  // the FFMA forward draws inline and stores nothing: fill the caller's keep
+  // mask for the backward
+  if (p.drop.on && p.drop.mask != nullptr)
+    return launch_dropout_mask(g, pb.causal, p.drop, p.drop.mask, p.status, stream);
+  return FA_OK;
 }
 
 // Validates the backward's tensors and fills p (everything but the path).
@@ -352,6 +363,30 @@ fa_status fa_bwd_ex(const fa_problem* prob, const void* q, const int64_t* sq, co
                  stream);
 }
 
+size_t fa_dropout_mask_bytes(const fa_problem* prob) {
+  Problem pb{};
+  if (check_problem(prob, &pb) != FA_OK || !pb.drop.on) return 0;
+  return dropout_mask_bytes(pb.g);
+}
+
+fa_status fa_dropout_mask(const fa_problem* prob, uint8_t* mask, size_t bytes,
+                          cudaStream_t stream) {
+  if (!prob) return FA_ERR_NULL;
+  fa_problem pr = *prob;
+  pr.dropout_mask = nullptr;           // the buffer being filled is not an input
+  Problem pb{};
+  FA_TRY(check_problem(&pr, &pb));
+  if (!pb.drop.on) return FA_ERR_ARG;
+  if (!mask) return FA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(mask) % 16 != 0) return FA_ERR_ALIGN;
+  const size_t need = dropout_mask_bytes(pb.g);
+  if (need == 0) return FA_ERR_SHAPE;
+  if (bytes < need) return FA_ERR_SCRATCH;
+  DeviceInfo* dev = nullptr;
+  FA_TRY(device_setup(&dev));
+  return launch_dropout_mask(pb.g, pb.causal, pb.drop, mask, dev->status, stream);
+}
+
 size_t fa_bwd_fused_workspace_bytes(const fa_problem* prob) {
   Problem pb{};
   if (check_problem(prob, &pb) != FA_OK) return 0;
@@ -434,6 +469,6 @@ void fa_set_profile_events(const cudaEvent_t* events) {
 
 void fa_test_withhold_next_arrival(void) { g_withhold_next.store(1); }
 
-int fa_version(void) { return 0x000100; }
+int fa_version(void) { return 0x000200; }
 
 }  // extern "C"

@@ -192,9 +192,9 @@ __device__ __forceinline__ void form_probs(float (&p)[64], uint64_t& keep, uint3
 #pragma unroll
   for (int q = 0; q < 32; ++q) {
     if constexpr (DROP) {
-      const float z0 = ((keep >> (2 * q)) & 1u) ? drop.rscale : 0.f;
-      const float z1 = ((keep >> (2 * q + 1)) & 1u) ? drop.rscale : 0.f;
-      w[q] = pack2<T>(p[2 * q] * z0, p[2 * q + 1] * z1);
+      // P o keep; Z's 1 / (1 - p) scales dV when it is stored
+      w[q] = pack2<T>(((keep >> (2 * q)) & 1u) ? p[2 * q] : 0.f,
+                      ((keep >> (2 * q + 1)) & 1u) ? p[2 * q + 1] : 0.f);
     } else {
       w[q] = pack2<T>(p[2 * q], p[2 * q + 1]);
     }
@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(320, 1)
       if (split == 1) {
         if (hf == 0) {
           T* out = static_cast<T*>(a.dv) + bb * a.sdv[0] + hk * a.sdv[1] + (sv.k0 + key) * a.sdv[2];
-          store_row_cols<T>(acc, 1.f, out, store, a.dreal);
+          store_row_cols<T>(acc, DROP ? a.drop.rscale : 1.f, out, store, a.dreal);
         } else {
           T* out = static_cast<T*>(a.dk) + bb * a.sdk[0] + hk * a.sdk[1] + (sv.k0 + key) * a.sdk[2];
           store_row_cols<T>(acc, a.scale, out, store, a.dreal);
@@ -699,7 +699,7 @@ __global__ void __launch_bounds__(320, 1)
       T* out = hf == 0
                    ? static_cast<T*>(a.dv) + bb * a.sdv[0] + hk * a.sdv[1] + (sv.k0 + key) * a.sdv[2]
                    : static_cast<T*>(a.dk) + bb * a.sdk[0] + hk * a.sdk[1] + (sv.k0 + key) * a.sdk[2];
-      cluster_reduce_store<T, D>(smem, hf, row, acc, split, hf == 0 ? 1.f : a.scale, out,
+      cluster_reduce_store<T, D>(smem, hf, row, acc, split, hf == 0 ? (DROP ? a.drop.rscale : 1.f) : a.scale, out,
                                  key < Nk, a.dreal);
     }
     cluster_sync_all();

@@ -105,7 +105,7 @@ struct DkdvCfg : BwdShape<D> {
   static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_DV = 256, COL_DK = 256 + D;
 };
 
-template <typename T, int D, bool DROP>
+template <typename T, int D, int DROP>
 __global__ void __launch_bounds__(320, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -390,18 +390,36 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c = a.c;
     bool ok = true;
+    // Dropout keep bits: bit q set iff weight (query 64*hf + q of the step's
+    // query tile, this key) is kept.  The eight lanes of an octet hold eight
+    // consecutive keys, whose decisions for one query are one byte of the
+    // keep mask or one generator call.  Mask bytes are loaded a step ahead
+    // (mb), so their latency overlaps a whole step.
+    uint32_t mb[8];
+    if constexpr (DROP) {
+      static_assert(C::BT == 128, "keep-mask entries cover 128-key tiles");
+      if constexpr (DROP == kDropRead)
+        octet_mask_load(a.drop, a.g, sv, hk * a.g.G + g0, kt, static_cast<int64_t>(i0) * C::BT + 64 * hf,
+                        row >> 3, lane, mb);
+    }
     for (int it = 0; it < n; ++it) {
       const int i = i0 + it % per, ds = it % C::ND;
-      // Dropout keep bits, drawn before the scores arrive (they depend on
-      // positions only): bit q set iff weight (query 64*hf + q of this tile,
-      // this key) is kept.  The eight lanes of an octet hold eight
-      // consecutive keys, which one generator call covers for one query
-      // (octet_keep_bits).
+      // keep bits drawn before the scores arrive (positions only), or the
+      // prefetched mask bytes exchanged and the next step's loads issued
       uint64_t keep = 0;
       if constexpr (DROP) {
-        const uint32_t bhq = static_cast<uint32_t>(bseq * a.g.Hq + hk * a.g.G + g0 + it / per);
-        keep = octet_keep_bits(a.drop, static_cast<uint32_t>(key >> 3),
-                               static_cast<int64_t>(i) * C::BT + 64 * hf, bhq, lane);
+        if constexpr (DROP == kDropRead) {
+          keep = octet_mask_bits(mb, lane);
+          if (it + 1 < n)
+            octet_mask_load(a.drop, a.g, sv, hk * a.g.G + g0 + (it + 1) / per, kt,
+                            static_cast<int64_t>(i0 + (it + 1) % per) * C::BT + 64 * hf, row >> 3,
+                            lane, mb);
+        } else {
+          keep = octet_keep_bits(a.drop, static_cast<uint32_t>(key >> 3),
+                                 static_cast<int64_t>(i) * C::BT + 64 * hf,
+                                 static_cast<uint32_t>(bseq * a.g.Hq + hk * a.g.G + g0 + it / per),
+                                 lane);
+        }
       }
       if (!(ok = wait_warp(b_sfull, it & 1, ctl, a.status, a.timeout_ns))) break;
       // the dO slot's arrival also publishes the staged L and Delta
@@ -434,10 +452,14 @@ __global__ void __launch_bounds__(320, 1)
           if (64 * hf + q < row) p[q] = 0.f;
       }
       if constexpr (DROP) {
-        float pd[64];
+        // P o keep, rounded pairs formed straight from p (no fp32 copy
+        // kept); Z's 1 / (1 - p) scales dV when it is stored
+        uint32_t w[32];
 #pragma unroll
-        for (int q = 0; q < 64; ++q) pd[q] = ((keep >> q) & 1u) ? p[q] * a.drop.rscale : 0.f;
-        tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, pd);
+        for (int i = 0; i < 32; ++i)
+          w[i] = pack2<T>(((keep >> (2 * i)) & 1u) ? p[2 * i] : 0.f,
+                          ((keep >> (2 * i + 1)) & 1u) ? p[2 * i + 1] : 0.f);
+        tmem_st32(lane_base + C::COL_ST + 64 * hf, w);
       } else {
         tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, p);
       }
@@ -448,16 +470,39 @@ __global__ void __launch_bounds__(320, 1)
 
       if (!(ok = wait_warp(b_dpfull, it & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
-      float dp[64];
-      tmem_ld64(lane_base + C::COL_DPT + 64 * hf, dp);
       if constexpr (DROP) {
-        // dS = P o (Z o dP - Delta), Z = keep / (1 - p)
+        // dS = P o (Z o dP - Delta), Z = keep / (1 - p): dP / (1 - p) - Delta
+        // for kept weights, -Delta for dropped ones, two queries per paired
+        // instruction.  In two halves of 32 queries, so that only 32 of dP
+        // are held next to P: half 0's rounded dS lands on columns whose dP
+        // was read first, half 1's on half 0's.
+        const uint64_t rs2 = f32x2(a.drop.rscale, a.drop.rscale);
+        const uint32_t tdp = lane_base + C::COL_DPT + 64 * hf;
 #pragma unroll
-        for (int q = 0; q < 64; ++q) {
-          const float z = ((keep >> q) & 1u) ? a.drop.rscale : 0.f;
-          dp[q] = p[q] * fmaf(z, dp[q], nDs[q]);
+        for (int hq = 0; hq < 2; ++hq) {
+          uint32_t r[32];
+          tmem_ld32(tdp + 32 * hq, r);
+          tmem_wait_ld();
+          reg_fence32(r);
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int q = 32 * hq + j;
+            const float2 d2 = *reinterpret_cast<const float2*>(nDs + q);
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), rs2,
+                                  f32x2(d2.x, d2.y)),
+                        x0, x1);
+            x0 = ((keep >> q) & 1u) ? x0 : d2.x;
+            x1 = ((keep >> (q + 1)) & 1u) ? x1 : d2.y;
+            f32x2_split(mul_f32x2(f32x2(x0, x1), f32x2(p[q], p[q + 1])), x0, x1);
+            w[j / 2] = pack2<T>(x0, x1);
+          }
+          tmem_st16(tdp + 16 * hq, w);
         }
       } else {
+        float dp[64];
+        tmem_ld64(lane_base + C::COL_DPT + 64 * hf, dp);
 #pragma unroll
         for (int q = 0; q < 64; q += 4) {
           // dS = P o (dP - Delta), two queries per paired instruction
@@ -469,8 +514,8 @@ __global__ void __launch_bounds__(320, 1)
           f32x2_split(a01, dp[q], dp[q + 1]);
           f32x2_split(a23, dp[q + 2], dp[q + 3]);
         }
+        tmem_st_packed64<T>(lane_base + C::COL_DPT + 64 * hf, dp);
       }
-      tmem_st_packed64<T>(lane_base + C::COL_DPT + 64 * hf, dp);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(b_dsready0 + 8 * hf);
@@ -484,7 +529,7 @@ __global__ void __launch_bounds__(320, 1)
       if (split == 1) {
         if (hf == 0) {
           T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hk * a.s0[1] + (sv.k0 + key) * a.s0[2];
-          store_row_cols<T>(acc, 1.f, out, store, a.dreal);
+          store_row_cols<T>(acc, DROP ? a.drop.rscale : 1.f, out, store, a.dreal);
         } else {
           T* out = static_cast<T*>(a.out1) + bb * a.s1[0] + hk * a.s1[1] + (sv.k0 + key) * a.s1[2];
           store_row_cols<T>(acc, a.scale, out, store, a.dreal);
@@ -517,7 +562,7 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t acc = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                            (hf == 0 ? C::COL_DV : C::COL_DK);
       const uint32_t st = smem_u32(stage_row<D>(smem, hf, row));
-      const float mul = hf == 0 ? 1.f : a.scale;
+      const float mul = hf == 0 ? (DROP ? a.drop.rscale : 1.f) : a.scale;
       T* out = hf == 0
                    ? static_cast<T*>(a.out0) + bb * a.s0[0] + hk * a.s0[1] + (sv.k0 + key) * a.s0[2]
                    : static_cast<T*>(a.out1) + bb * a.s1[0] + hk * a.s1[1] + (sv.k0 + key) * a.s1[2];
@@ -601,7 +646,7 @@ __device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int row, u
   }
 }
 
-template <typename T, int D, bool DROP>
+template <typename T, int D, int DROP>
 __global__ void __launch_bounds__(320, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
@@ -808,18 +853,35 @@ __global__ void __launch_bounds__(320, 1)
     }
     tc_fence_before();
     mbar_arrive(b_qt);
+    // Dropout keep bits of this row's 64 keys of a key tile: bit q set iff
+    // key 64*hf + q of the tile is kept.  In the keep mask they are bytes
+    // 8*hf .. 8*hf + 7 of the row's entry for the tile, loaded a tile ahead
+    // (mnext) so their latency overlaps a whole tile.
+    const bool mrow = DROP == kDropRead && qrow < Nq;
+    const unsigned long long* mptr =
+        mrow ? reinterpret_cast<const unsigned long long*>(
+                   a.drop.mask + mask_entry(a.drop, a.g, sv, h, 0, qrow) + 8 * hf)
+             : nullptr;
+    const int64_t mstep = a.g.rows_q * 2;            // one key tile, in 8-byte words
+    unsigned long long mnext = (mrow && n > 0) ? __ldg(mptr) : 0ull;
     for (int jt = 0; ok && jt < n; ++jt) {
-      // Dropout keep bits of this row's 64 keys (positions only), drawn before
-      // the scores arrive: bit q set iff key 64*hf + q of this tile is kept.
+      // keep bits drawn before the scores arrive (positions only), or the
+      // prefetched mask word taken and the next tile's issued
       uint64_t keep = 0;
       if constexpr (DROP) {
-        const int64_t kbase = static_cast<int64_t>(jt) * C::BT + 64 * hf;
+        static_assert(C::BT == 128, "keep-mask entries cover 128-key tiles");
+        if constexpr (DROP == kDropRead) {
+          keep = mnext;
+          if (mrow && jt + 1 < n) mnext = __ldg(mptr + (jt + 1) * mstep);
+        } else {
+          const int64_t kbase = static_cast<int64_t>(jt) * C::BT + 64 * hf;
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-          keep |= static_cast<uint64_t>(keep8(a.drop, static_cast<uint32_t>((kbase >> 3) + t),
-                                              static_cast<uint32_t>(qrow),
-                                              static_cast<uint32_t>(bh)))
-                  << (8 * t);
+          for (int t = 0; t < 8; ++t)
+            keep |= static_cast<uint64_t>(keep8(a.drop, static_cast<uint32_t>((kbase >> 3) + t),
+                                                static_cast<uint32_t>(qrow),
+                                                static_cast<uint32_t>(bh)))
+                    << (8 * t);
+        }
       }
       if (!(ok = wait_warp(b_sfull, jt & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
@@ -849,16 +911,37 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (!(ok = wait_warp(b_dpfull, jt & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
-      float dp[64];
-      tmem_ld64(lane_base + C::COL_DP + 64 * hf, dp);
       if constexpr (DROP) {
-        // dS = P o (Z o dP - Delta), Z = keep / (1 - p)
+        // dS = P o (Z o dP - Delta), Z = keep / (1 - p): dP / (1 - p) - Delta
+        // for kept weights, -Delta for dropped ones, two keys per paired
+        // instruction.  In two halves of 32 keys, so that only 32 of dP are
+        // held next to P: half 0's rounded dS lands on columns whose dP was
+        // read first, half 1's on half 0's.
+        const uint64_t rs2 = f32x2(a.drop.rscale, a.drop.rscale), nd = f32x2(-dl, -dl);
+        const uint32_t tdp = lane_base + C::COL_DP + 64 * hf;
 #pragma unroll
-        for (int q = 0; q < 64; ++q) {
-          const float z = ((keep >> q) & 1u) ? a.drop.rscale : 0.f;
-          dp[q] = p[q] * fmaf(z, dp[q], -dl);
+        for (int hq = 0; hq < 2; ++hq) {
+          uint32_t r[32];
+          tmem_ld32(tdp + 32 * hq, r);
+          tmem_wait_ld();
+          reg_fence32(r);
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int q = 32 * hq + j;
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), rs2, nd),
+                        x0, x1);
+            x0 = ((keep >> q) & 1u) ? x0 : -dl;
+            x1 = ((keep >> (q + 1)) & 1u) ? x1 : -dl;
+            f32x2_split(mul_f32x2(f32x2(x0, x1), f32x2(p[q], p[q + 1])), x0, x1);
+            w[j / 2] = pack2<T>(x0, x1);
+          }
+          tmem_st16(tdp + 16 * hq, w);
         }
       } else {
+        float dp[64];
+        tmem_ld64(lane_base + C::COL_DP + 64 * hf, dp);
         // dS = P o (dP - Delta), two keys per paired instruction
         const uint64_t nd = f32x2(-dl, -dl);
 #pragma unroll
@@ -866,8 +949,8 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t x = mul_f32x2(add_f32x2(f32x2(dp[q], dp[q + 1]), nd), f32x2(p[q], p[q + 1]));
           f32x2_split(x, dp[q], dp[q + 1]);
         }
+        tmem_st_packed64<T>(lane_base + C::COL_DP + 64 * hf, dp);
       }
-      tmem_st_packed64<T>(lane_base + C::COL_DP + 64 * hf, dp);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(b_dsready0 + 8 * hf);
@@ -892,7 +975,7 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <typename T, int D, bool DROP>
+template <typename T, int D, int DROP>
 fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
   const Geo& g = p.g;
   // Tensor maps carry the true head dimension (zero fill past it).
@@ -970,7 +1053,9 @@ fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
 
 template <typename T, int D>
 fa_status run_bwd_tc_any(const BwdParams& p, cudaStream_t s) {
-  return p.drop.on ? run_bwd_tc<T, D, true>(p, s) : run_bwd_tc<T, D, false>(p, s);
+  const int dm = bwd_drop_mode(p.drop);
+  return dm == kDropRead ? run_bwd_tc<T, D, kDropRead>(p, s)
+         : dm == kDropDraw ? run_bwd_tc<T, D, kDropDraw>(p, s) : run_bwd_tc<T, D, kDropNone>(p, s);
 }
 
 }  // namespace

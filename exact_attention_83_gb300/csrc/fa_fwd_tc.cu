@@ -37,6 +37,12 @@
 // every earlier MMA of the issuing thread, so when the softmax warps see S_j
 // complete, PV_{j-1} of the same tile is complete too and O may be rescaled.
 //
+// Dropout (FlashAttention-2's dropout of P, decisions from Philox positions):
+// each softmax thread evaluates the generator for its row of the next key
+// tile before the scores arrive and, when the caller gave a keep mask, stores
+// the 16 bytes there for the backward.  P V takes P o keep; the 1 / (1 - p)
+// of Z is folded into the final 1 / l.
+//
 // Every mbarrier wait is bounded (see tc_common.cuh); a wait that runs out
 // records FA_ERR_TIMEOUT, the CTA drains its copies and MMAs in flight,
 // releases its tensor memory and exits.
@@ -84,7 +90,7 @@ struct FwdTcArgs {
   int withhold_arrival;    // test-only: CTA 0 skips the first S-ready arrival of tile 0
 };
 
-template <typename T, int D, bool DROP>
+template <typename T, int D, int DROP>
 __global__ void __launch_bounds__(320, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, const FwdTcArgs a) {
@@ -303,17 +309,18 @@ __global__ void __launch_bounds__(320, 1)
     const int n = ntile[g];
     // last valid key column of the last key tile
     const int lim_last = static_cast<int>(Nk - 1 - static_cast<int64_t>(nk - 1) * C::BN);
+    // keep bits of this row, stored into the caller's keep mask (16 bytes
+    // per key tile, tiles rows_q entries apart) for the backward
+    uint4* mrow = nullptr;
+    if (DROP && a.drop.mask != nullptr && qrow < Nq)
+      mrow = reinterpret_cast<uint4*>(a.drop.mask + mask_entry(a.drop, a.g, sv, h, 0, qrow));
     for (int j = 0; j < n; ++j) {
       // Dropout keep bits of this row's 128 keys, drawn before the scores
-      // arrive (positions only): bit k of kb[k / 32] is key j*128 + k; one
-      // generator call covers eight keys.
+      // arrive (positions only): bit k of kb[k / 32] is key j*128 + k.
       uint32_t kb[4] = {0u, 0u, 0u, 0u};
       if constexpr (DROP) {
-#pragma unroll
-        for (int g8 = 0; g8 < 16; ++g8)
-          kb[g8 >> 2] |= keep8(a.drop, static_cast<uint32_t>(j * 16 + g8),
-                               static_cast<uint32_t>(qrow), static_cast<uint32_t>(bh))
-                         << (8 * (g8 & 3));
+        tile_keep_bits(a.drop, bh, j, qrow, kb);
+        if (mrow) mrow[j * a.g.rows_q] = make_uint4(kb[0], kb[1], kb[2], kb[3]);
       }
       if (!(ok = wait_warp(b_sfull0 + 8 * g, j & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
@@ -386,11 +393,11 @@ __global__ void __launch_bounds__(320, 1)
           const float p0 = ex2(x0), p1 = ex2(x1);
           acc = add_f32x2(acc, f32x2(p0, p1));
           if constexpr (DROP) {
-            // l sums the undropped weights; P V takes the dropped, rescaled ones
+            // l sums the undropped weights; P V takes the kept ones (the
+            // 1 / (1 - p) of Z is applied with 1 / l at the end)
             const int kk = 64 * hh + 2 * i;
             const uint32_t bits = kb[kk >> 5] >> (kk & 31);
-            pk[i] = pack2<T>((bits & 1u) ? p0 * a.drop.rscale : 0.f,
-                             (bits & 2u) ? p1 * a.drop.rscale : 0.f);
+            pk[i] = pack2<T>((bits & 1u) ? p0 : 0.f, (bits & 2u) ? p1 : 0.f);
           } else {
             pk[i] = pack2<T>(p0, p1);
           }
@@ -418,11 +425,12 @@ __global__ void __launch_bounds__(320, 1)
         f32x2_split(acc, lo, hi);
         l += lo + hi;
       }
+      if (!ok) break;
     }
     if (ok && n > 0) ok = wait_warp(b_ofinal0 + 8 * g, 0, ctl, a.status, a.timeout_ns);
     if (ok && n > 0) {
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = (DROP ? a.drop.rscale : 1.f) / l;   // Z's 1 / (1 - p) with dropout
       const bool store = qrow < Nq;
       T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qrow) * a.so[2];
       store_row_cols<T>(tO, inv, orow, store, a.dreal);
@@ -464,7 +472,7 @@ struct Fwd1Cfg {
   static constexpr uint32_t COL_S = 0, COL_O = 128, COL_P = 192;
 };
 
-template <typename T, bool DROP>
+template <typename T, int DROP>
 __global__ void __launch_bounds__(192, 2)
     fwd_tc_1t_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const FwdTcArgs a) {
@@ -653,16 +661,18 @@ __global__ void __launch_bounds__(192, 2)
     bool ok = true;
     // last valid key column of the last key tile
     const int lim_last = static_cast<int>(Nk - 1 - static_cast<int64_t>(nk - 1) * C::BN);
+    // keep bits of this row, stored into the caller's keep mask (16 bytes
+    // per key tile, tiles rows_q entries apart) for the backward
+    uint4* mrow = nullptr;
+    if (DROP && a.drop.mask != nullptr && qrow < Nq)
+      mrow = reinterpret_cast<uint4*>(a.drop.mask + mask_entry(a.drop, a.g, sv, h, 0, qrow));
     for (int j = 0; j < n; ++j) {
       // Dropout keep bits of this row's 128 keys, drawn before the scores
       // arrive (positions only): bit k of kb[k / 32] is key j*128 + k.
       uint32_t kb[4] = {0u, 0u, 0u, 0u};
       if constexpr (DROP) {
-#pragma unroll
-        for (int g8 = 0; g8 < 16; ++g8)
-          kb[g8 >> 2] |= keep8(a.drop, static_cast<uint32_t>(j * 16 + g8),
-                               static_cast<uint32_t>(qrow), static_cast<uint32_t>(bh))
-                         << (8 * (g8 & 3));
+        tile_keep_bits(a.drop, bh, j, qrow, kb);
+        if (mrow) mrow[j * a.g.rows_q] = make_uint4(kb[0], kb[1], kb[2], kb[3]);
       }
       if (!(ok = wait_warp(b_sfull, j & 1, ctl, a.status, a.timeout_ns))) break;
       tc_fence_after();
@@ -737,11 +747,11 @@ __global__ void __launch_bounds__(192, 2)
           const float p0 = ex2(x0), p1 = ex2(x1);
           acc = add_f32x2(acc, f32x2(p0, p1));
           if constexpr (DROP) {
-            // l sums the undropped weights; P V takes the dropped, rescaled ones
+            // l sums the undropped weights; P V takes the kept ones (the
+            // 1 / (1 - p) of Z is applied with 1 / l at the end)
             const int kk = 64 * half + 2 * i;
             const uint32_t bits = kb[kk >> 5] >> (kk & 31);
-            pk[i] = pack2<T>((bits & 1u) ? p0 * a.drop.rscale : 0.f,
-                             (bits & 2u) ? p1 * a.drop.rscale : 0.f);
+            pk[i] = pack2<T>((bits & 1u) ? p0 : 0.f, (bits & 2u) ? p1 : 0.f);
           } else {
             pk[i] = pack2<T>(p0, p1);
           }
@@ -777,7 +787,7 @@ __global__ void __launch_bounds__(192, 2)
     if (ok) ok = wait_warp(b_pvdone, (n - 1) & 1, ctl, a.status, a.timeout_ns);
     if (ok) {
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = (DROP ? a.drop.rscale : 1.f) / l;   // Z's 1 / (1 - p) with dropout
       const bool store = qrow < Nq;
       T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qrow) * a.so[2];
       store_row_cols<T>(tO, inv, orow, store, a.dreal);
@@ -823,14 +833,14 @@ fa_status run_fwd_tc(const FwdParams& p, cudaStream_t stream) {
     a.npairs = (g.Nq + 127) / 128;
     const int64_t blocks1 = a.BH * a.npairs;
     if (blocks1 > 0x7fffffffLL) return FA_ERR_SHAPE;
-    auto kern = p.drop.on ? fwd_tc_1t_kernel<T, true> : fwd_tc_1t_kernel<T, false>;
+    auto kern = p.drop.on ? fwd_tc_1t_kernel<T, kDropDraw> : fwd_tc_1t_kernel<T, kDropNone>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Fwd1Cfg::SMEM) !=
         cudaSuccess)
       return FA_ERR_LAUNCH;
     kern<<<dim3(static_cast<unsigned>(blocks1)), dim3(Fwd1Cfg::THREADS), Fwd1Cfg::SMEM, stream>>>(
         mq, mk, mv, a);
   } else {
-    auto kern = p.drop.on ? fwd_tc_kernel<T, D, true> : fwd_tc_kernel<T, D, false>;
+    auto kern = p.drop.on ? fwd_tc_kernel<T, D, kDropDraw> : fwd_tc_kernel<T, D, kDropNone>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
         cudaSuccess)
       return FA_ERR_LAUNCH;

@@ -41,6 +41,12 @@ struct Dropout {
   float rscale;
   uint32_t key0, key1, offset;
   uint32_t rk0[10], rk1[10];   // round keys
+  // Keep mask, or null: 16 bytes per (sequence-level flat head, key tile of
+  // 128, query row); byte g of key tile t is keep8 of key group 16t + g.
+  // The forward writes it, the backward reads it.  mask_kt = key tiles per
+  // head.
+  uint8_t* mask;
+  int64_t mask_kt;
 };
 
 // Parameters of one forward call.
@@ -134,19 +140,51 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const uint32_t (&rk0)[10
   return c;
 }
 
+// Dropout modes of the tensor-core kernels (template parameter DROP): no
+// dropout, keep decisions drawn in the kernel, or read from the keep mask
+// (the backward, when the forward left one).
+enum : int { kDropNone = 0, kDropDraw = 1, kDropRead = 2 };
+inline int bwd_drop_mode(const Dropout& d) {
+  return !d.on ? kDropNone : (d.mask != nullptr ? kDropRead : kDropDraw);
+}
+
+// Byte offset in the keep mask of the 16-byte entry of (query head h of
+// sequence v, key tile jt, query row `row` of the sequence); entries of
+// consecutive rows are 16 bytes apart.
+__device__ __forceinline__ int64_t mask_entry(const Dropout& d, const Geo& g, const SeqView& v,
+                                              int64_t h, int64_t jt, int64_t row) {
+  return (((v.b * g.Hq + h) * d.mask_kt + jt) * g.rows_q + v.q0 + row) * 16;
+}
+
 // The eight keep decisions for keys 8*jg .. 8*jg+7 of query row i in flat
 // head bh (= b * Hq + h), as bits 0..7.
 __device__ __forceinline__ uint32_t keep8(const Dropout& d, uint32_t jg, uint32_t i,
                                           uint32_t bh) {
   const uint4 r = philox4x32_10(make_uint4(jg, i, bh, d.offset), d.rk0, d.rk1);
   const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+  // half >= thr as whole-word compares against thr * 2^16: the high half
+  // compares as w itself, the low half as w << 16 (fewer integer-pipe
+  // instructions than extracting each half)
+  const uint32_t t16 = d.thr << 16;
   uint32_t bits = 0;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    bits |= ((w[e] & 0xFFFFu) >= d.thr ? 1u : 0u) << (2 * e);
-    bits |= ((w[e] >> 16) >= d.thr ? 1u : 0u) << (2 * e + 1);
+    bits |= (w[e] >= t16 ? 2u : 0u) << (2 * e);
+    bits |= ((w[e] << 16) >= t16 ? 1u : 0u) << (2 * e);
   }
   return bits;
+}
+
+// Keep bits of query row `row` in flat head bh (= b * Hq + h) for the 128
+// keys of key tile jt, drawn: bit k of kb[k / 32] is key 128 jt + k.
+__device__ __forceinline__ void tile_keep_bits(const Dropout& d, int64_t bh, int64_t jt,
+                                               int64_t row, uint32_t (&kb)[4]) {
+  kb[0] = kb[1] = kb[2] = kb[3] = 0u;
+#pragma unroll
+  for (int g8 = 0; g8 < 16; ++g8)
+    kb[g8 >> 2] |= keep8(d, static_cast<uint32_t>(jt * 16 + g8), static_cast<uint32_t>(row),
+                         static_cast<uint32_t>(bh))
+                   << (8 * (g8 & 3));
 }
 #endif
 
@@ -168,6 +206,11 @@ bool have_bwd_tc(int64_t D, fa_dtype dt);
 // `ws` of bwd_fused_workspace_floats(g, D) floats, 16-byte aligned.
 fa_status launch_bwd_fused(const BwdParams& p, float* ws, cudaStream_t s);
 size_t bwd_fused_workspace_floats(const Geo& g, int64_t D);
+// Keep mask (fa_dropout_mask): its size in bytes, and the kernel that fills
+// the entries the attention kernels read (d.on must be set).
+size_t dropout_mask_bytes(const Geo& g);
+fa_status launch_dropout_mask(const Geo& g, int causal, const Dropout& d, uint8_t* mask,
+                              unsigned int* status, cudaStream_t s);
 
 // Encodes a 4-D tiled TMA map (d, n, h, b) over a strided [B,H,N,D] fp16/bf16
 // tensor with 128-byte swizzle and a box of box_cols x box_rows elements.

@@ -86,7 +86,7 @@ typedef enum {
   FA_ERR_SCALE = 10,   /* scale is not finite and > 0                          */
   FA_ERR_ARG = 11,     /* another invalid argument (e.g. an unknown option)    */
   FA_ERR_SCRATCH = 12, /* B*H*N above FA_NOALLOC_MAX_ROWS (fa_bwd_noalloc) or */
-                       /* a workspace too small (fa_bwd_fused)              */
+                       /* a workspace or mask buffer too small              */
   FA_ERR_SEQLENS = 13  /* device-reported: packed offsets inconsistent (below) */
 } fa_status;
 
@@ -207,6 +207,19 @@ FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, con
  *              log-sum-exp of the undropped scores.  fa_bwd_ex with the same
  *              seed and offset rebuilds the same mask:
  *              dV = (P o Z)^T dO, dS = P o (Z o (dO V^T) - Delta).
+ *   dropout_mask  optional, may be NULL (also for zero-initialised structs
+ *              of callers that do not know the field): a DEVICE buffer of at
+ *              least fa_dropout_mask_bytes(prob) bytes, 16-byte aligned, that
+ *              carries the keep decisions from the forward to the backward.
+ *              With dropout_p > 0, fa_fwd_ex stores every decision it draws
+ *              there (the bytes fa_dropout_mask would write), and fa_bwd_ex
+ *              reads them instead of evaluating the generator again; results
+ *              are bitwise identical either way.  So the backward must get a
+ *              buffer that a forward (or fa_dropout_mask) of this same problem
+ *              (sizes, lengths, causal, dropout_p, seed, offset) filled: it
+ *              trusts the contents, and another problem's buffer gives another
+ *              mask without an error.  Ignored when dropout_p = 0.
+ *              FA_ERR_ALIGN unless 16-byte aligned.
  *
  * Rows with no key at all (an empty key sequence) get O = 0 and L = -inf;
  * keys that no query attends to get dK = dV = 0.
@@ -222,6 +235,7 @@ typedef struct fa_problem {
   float dropout_p;
   uint64_t seed;
   uint32_t offset;
+  uint8_t* dropout_mask;
 } fa_problem;
 
 /*
@@ -278,6 +292,35 @@ FA_API fa_status fa_bwd_fused(const fa_problem* prob, const void* q, const int64
                               const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
                               const int64_t* sdv, float* dq_accum, size_t workspace_bytes,
                               cudaStream_t stream);
+
+/*
+ * Dropout keep mask of a general problem: the decisions stated for dropout_p
+ * under fa_problem, 1 bit per (query, key) pair, in the buffer that
+ * fa_problem.dropout_mask names.  fa_fwd_ex fills it as it draws the
+ * decisions (in warps of its own, beside the softmax); fa_dropout_mask fills
+ * it without a forward, e.g. for a backward whose forward ran without one.
+ *
+ * Layout (callers need not read it): 16 bytes per (flat head, key tile of 128
+ * keys, query row), ordered [Bt][Hq][ceil(Nk / 128)][rows][16] with Bt = B,
+ * rows = Nq for fixed lengths and Bt = 1, rows = total_q (the packed row) for
+ * packed sequences; byte g of key tile t holds the decisions for keys
+ * 8(16t + g) .. 8(16t + g) + 7 of the row as bits 0..7 (set: kept).  Written
+ * are the entries the kernels read: rows and key tiles inside the row's
+ * sequence and, under causal masking, key tiles t <= row / 128.  1/8 byte
+ * per (query, key) pair: 1 GiB for 32 heads of 16384 x 16384.
+ *
+ * fa_dropout_mask_bytes returns the size for `prob`, or 0 when the problem is
+ * invalid or has dropout_p = 0.  fa_dropout_mask fills `mask` (a DEVICE
+ * buffer of `bytes` bytes) on `stream` and allocates nothing.  Errors: those
+ * of fa_fwd_ex's problem checks; FA_ERR_ARG for dropout_p = 0; FA_ERR_NULL
+ * for a NULL mask; FA_ERR_ALIGN unless it is 16-byte aligned; FA_ERR_SCRATCH
+ * when bytes < fa_dropout_mask_bytes(prob).  prob->dropout_mask is ignored.
+ * Packed sequences whose offsets break the rules above are skipped (the
+ * forward reports FA_ERR_SEQLENS for them).
+ */
+FA_API size_t fa_dropout_mask_bytes(const fa_problem* prob);
+FA_API fa_status fa_dropout_mask(const fa_problem* prob, uint8_t* mask, size_t bytes,
+                                 cudaStream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the

@@ -92,6 +92,7 @@ def _load():
         lib.oracle_key_rows.argtypes = [_dp] * 4 + _DIMS + _COMMON + _ROWS + [_dp] * 4
         lib.oracle_magnitudes.argtypes = [_dp] * 4 + _DIMS + _COMMON + [_dp] * 4
         lib.oracle_philox4x32_10.argtypes = [ctypes.POINTER(ctypes.c_uint32)] * 3
+        lib.oracle_dropout_z.argtypes = [ctypes.POINTER(Dropout), _i64, _i64, _i64, _i64, _dp]
         lib.oracle_dense.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64,
                                      ctypes.c_int, ctypes.c_double, _dp, _dp, _dp,
                                      _dp, _dp, _dp]
@@ -155,6 +156,15 @@ def philox4x32_10(counter, key):
     out = (ctypes.c_uint32 * 4)()
     _load().oracle_philox4x32_10(c, kk, out)
     return tuple(int(x) for x in out)
+
+
+def dropout_z(dropout, bh: int, nq: int, nk: int, i0: int = 0) -> np.ndarray:
+    """Z = keep / (1 - p) of the weights (i0 + r, j), r < nq, j < nk, of flat
+    query head bh (positions within the sequence), [nq, nk] fp64: the factor
+    the oracle's forward and backward apply."""
+    z = np.empty((nq, nk), dtype=np.float64)
+    _load().oracle_dropout_z(ctypes.byref(dropout), int(bh), int(i0), int(nq), int(nk), _ptr(z))
+    return z
 
 
 def _common(causal, scale, D, dropout):

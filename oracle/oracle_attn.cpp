@@ -326,6 +326,14 @@ void oracle_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* ou
   philox(ctr, key[0], key[1], out);
 }
 
+// Z of the weights (i0 + r, j), r < nq, j < nk, of flat head bh (row-major
+// [nq, nk]): keep / (1 - p), or 1 everywhere without dropout.
+void oracle_dropout_z(const oracle_dropout* dr, int64_t bh, int64_t i0, int64_t nq, int64_t nk,
+                      double* z) {
+  for (int64_t r = 0; r < nq; ++r)
+    for (int64_t j = 0; j < nk; ++j) z[r * nk + j] = zfac(dr, i0 + r, j, bh);
+}
+
 // Forward: O [B,Hq,Nq,D], L [B,Hq,Nq].
 void oracle_fwd(const double* Q, const double* K, const double* V, int64_t B,
                 int64_t Hq, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t D, int causal,

@@ -23,15 +23,20 @@ def _kw(w: GeneralWorkload, cu_q, cu_k):
     return kw
 
 
-def run_general(w: GeneralWorkload, fused: bool = False):
+def run_general(w: GeneralWorkload, fused: bool = False, keep_mask: bool = False):
     """Forward, preprocess and backward (fa_bwd_ex, or fa_bwd_fused when
     `fused`) through the C ABI; outputs start as NaN so any element left
-    unwritten fails the comparison."""
+    unwritten fails the comparison.  keep_mask: the forward stores its
+    dropout decisions in a keep-mask buffer (which starts as 0xA5 bytes) that
+    the backward reads."""
     q, k, v, do, cu_q, cu_k = make_general_inputs(w)
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
     cq = cu_q.to(DEV) if cu_q is not None else None
     ck = cu_k.to(DEV) if cu_k is not None else None
     kw = _kw(w, cq, ck)
+    if keep_mask:
+        kw["dropout_mask"] = torch.full((fa.dropout_mask_bytes(qd, kd, w.causal, w.scale, **kw),),
+                                        0xA5, dtype=torch.uint8, device=DEV)
     o = torch.full_like(qd, float("nan"))
     lse_shape = (w.Hq, q.shape[0]) if w.packed else (w.B, w.Hq, w.Nq)
     lse = torch.full(lse_shape, float("nan"), dtype=torch.float32, device=DEV)

@@ -173,3 +173,40 @@ def test_general_problem_validation_codes(lib):
     assert fwd(pr) == 2
     assert fwd(_problem(B=1), strides=S(0, 300 * 64, 64, 2)) == 5     # FA_ERR_STRIDE
     assert bwd(_problem(B=1), delta=None) == 1
+
+
+def test_dropout_mask_size_and_validation(lib):
+    """fa_dropout_mask_bytes: 16 bytes per (flat head, key tile of 128, query
+    row), 0 without dropout or for an invalid problem.  fa_dropout_mask and a
+    problem's dropout_mask field are checked before any device work."""
+    pr = _problem(B=2, Hq=4, Nq=300, Nk=333)
+    assert lib.fa_dropout_mask_bytes(ctypes.byref(pr)) == 0          # dropout_p = 0
+    pr.dropout_p = 0.1
+    assert lib.fa_dropout_mask_bytes(ctypes.byref(pr)) == 2 * 4 * 3 * 300 * 16
+    pr.Nk = 256
+    assert lib.fa_dropout_mask_bytes(ctypes.byref(pr)) == 2 * 4 * 2 * 300 * 16
+    pk = _problem(B=3, Hq=4, Nq=500, Nk=129)                          # packed: total_q rows
+    pk.cu_seqlens_q, pk.cu_seqlens_k, pk.total_q, pk.total_k = FAKE, FAKE, 700, 300
+    pk.dropout_p = 0.5
+    assert lib.fa_dropout_mask_bytes(ctypes.byref(pk)) == 1 * 4 * 2 * 700 * 16
+    bad = _problem(Hkv=3)
+    bad.dropout_p = 0.1
+    assert lib.fa_dropout_mask_bytes(ctypes.byref(bad)) == 0
+    assert lib.fa_dropout_mask_bytes(None) == 0
+
+    need = lib.fa_dropout_mask_bytes(ctypes.byref(pr))
+    assert lib.fa_dropout_mask(None, FAKE, need, None) == 1             # FA_ERR_NULL
+    assert lib.fa_dropout_mask(ctypes.byref(pr), None, need, None) == 1
+    assert lib.fa_dropout_mask(ctypes.byref(pr), FAKE + 8, need, None) == 6   # FA_ERR_ALIGN
+    assert lib.fa_dropout_mask(ctypes.byref(pr), FAKE, need - 1, None) == 12  # FA_ERR_SCRATCH
+    nodrop = _problem()
+    assert lib.fa_dropout_mask(ctypes.byref(nodrop), FAKE, need, None) == 11  # FA_ERR_ARG
+    assert lib.fa_dropout_mask(ctypes.byref(bad), FAKE, need, None) == 2      # FA_ERR_SHAPE
+
+    # A misaligned keep-mask pointer in the problem is refused by the passes.
+    st = S(0, 0, 64, 1)
+    pr.dropout_mask = FAKE + 4
+    assert lib.fa_fwd_ex(ctypes.byref(pr), FAKE, st, FAKE, st, FAKE, st, FAKE, st, FAKE,
+                         None) == 6
+    assert lib.fa_bwd_ex(ctypes.byref(pr), FAKE, st, FAKE, st, FAKE, st, FAKE, st, FAKE, FAKE,
+                         FAKE, st, FAKE, st, FAKE, st, None) == 6

@@ -1,7 +1,9 @@
 """General problems at the size the benchmark times them, split and single-pass
 backward, against the oracle on sampled rows.
 
-Grouped (Hq 32 / Hkv 8) and multi-query (Hkv 1) heads, dropout p = 0.1,
+Grouped (Hq 32 / Hkv 8) and multi-query (Hkv 1) heads, dropout p = 0.1
+(decisions drawn again by the backward, and read by it from the keep mask
+the forward stored: bitwise the same),
 65536 packed tokens in sequences of 512-8192 rows, and Nq 4096 / Nk 16384
 cross lengths, all D = 128 bf16 with 32 query heads: exactly the inputs and
 launch configuration of `bench.py --workload <name>`.  The oracle computes
@@ -36,12 +38,15 @@ def _lib():
     yield
 
 
-def _run(w, inputs, fused):
+def _run(w, inputs, fused, keep_mask=False):
     q, k, v, do, cu_q, cu_k = inputs
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
     cq = cu_q.to(DEV) if cu_q is not None else None
     ck = cu_k.to(DEV) if cu_k is not None else None
     kw = _kw(w, cq, ck)
+    if keep_mask:
+        kw["dropout_mask"] = torch.full((fa.dropout_mask_bytes(qd, kd, w.causal, w.scale, **kw),),
+                                        0xA5, dtype=torch.uint8, device=DEV)
     o = torch.full_like(qd, float("nan"))
     lse_shape = (w.Hq, q.shape[0]) if w.packed else (w.B, w.Hq, w.Nq)
     lse = torch.full(lse_shape, float("nan"), dtype=torch.float32, device=DEV)
@@ -112,6 +117,13 @@ def test_general_workload_at_bench_size(w):
     q, k, v, do, cu_q, cu_k = inputs
     runs = {name: _run(w, inputs, fused)
             for name, fused in ((w.name, False), (w.name + "-single-pass", True))}
+    if w.dropout_p > 0:
+        # the benchmark's dropout step: the forward stores its decisions in
+        # the keep mask, the backward reads them; bitwise the same as drawing
+        # them again
+        read = _run(w, inputs, False, keep_mask=True)
+        for key in ("o", "lse", "dq", "dk", "dv"):
+            assert torch.equal(read[key], runs[w.name][key]), key
     if not w.packed:
         refs = _refs(w, q, k, v, do)
         for name, got in runs.items():

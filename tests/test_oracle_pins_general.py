@@ -132,6 +132,20 @@ def test_dropout_output_is_masked_probabilities_times_v():
     np.testing.assert_allclose(L, dn["lse"], rtol=1e-13, atol=1e-13)
 
 
+def test_dropout_z_matches_the_generator_layout():
+    """oracle.dropout_z (the factor the oracle's passes apply) equals Z
+    assembled here from the pinned generator, for several flat heads, a ragged
+    key count and a 64-bit seed; without dropout it is 1 everywhere."""
+    seed, off, p = 0xFEDC_BA98_7654_3210, 4, 0.23
+    dr = oracle.dropout_params(p, seed, off)
+    for bh in (0, 3, 70001):
+        z = _mask(p, seed, off, bh, 19, 45)
+        np.testing.assert_array_equal(oracle.dropout_z(dr, bh, 19, 45), z)
+        np.testing.assert_array_equal(oracle.dropout_z(dr, bh, 7, 45, i0=12), z[12:])
+    np.testing.assert_array_equal(oracle.dropout_z(oracle.dropout_params(0.0), 1, 5, 9),
+                                  np.ones((5, 9)))
+
+
 def test_dropout_keep_fraction():
     """About 1 - p of the weights survive (binomial, 6 standard deviations)."""
     p, n = 0.17, 0
