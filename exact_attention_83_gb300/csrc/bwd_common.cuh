@@ -34,35 +34,64 @@ __device__ __forceinline__ void tmem_st_packed64(uint32_t taddr, const float (&x
   tmem_st32(taddr, w);
 }
 
-// The octet's exchange: lane e' of the octet (lane & 7) holds `bits`, the
-// 8-bit keep decisions of query 8t + e' for the octet's eight consecutive
-// keys; returns, for this lane's key (bit e = lane & 7), the decisions of the
-// eight queries 8t .. 8t + 7 as bits 0..7.  Three shuffles and a bit gather;
-// every lane of the warp must call it.
-__device__ __forceinline__ uint64_t octet_gather8(uint32_t bits, int e) {
-  uint64_t x = static_cast<uint64_t>(bits) << (8 * e);
-  x |= __shfl_xor_sync(0xffffffffu, x, 1);
-  x |= __shfl_xor_sync(0xffffffffu, x, 2);
-  x |= __shfl_xor_sync(0xffffffffu, x, 4);
-  // bit 8 * e' + e of x is (query 8t + e', this key); gather them
-  const uint64_t y = (x >> e) & 0x0101010101010101ull;
-  return (y * 0x0102040810204080ull) >> 56;
+// Keep bits of the key held by a lane for 64 consecutive queries, as the
+// octet exchange below leaves them: query qbase + q is bit kbit(q) (a fixed
+// permutation; q is a compile-time constant wherever it is used).
+__device__ __forceinline__ constexpr int kbit(int q) { return 8 * (q & 7) + (q >> 3); }
+
+// Transposes the 8 x 8 bit matrix held in (lo, hi) as bytes (byte r, bit c
+// -> byte c, bit r): three delta swaps of 7, 14 and 28 bit positions.
+__device__ __forceinline__ void bit_transpose8(uint32_t& lo, uint32_t& hi) {
+  uint32_t t;
+  t = (lo ^ (lo >> 7)) & 0x00AA00AAu; lo ^= t ^ (t << 7);
+  t = (hi ^ (hi >> 7)) & 0x00AA00AAu; hi ^= t ^ (t << 7);
+  t = (lo ^ (lo >> 14)) & 0x0000CCCCu; lo ^= t ^ (t << 14);
+  t = (hi ^ (hi >> 14)) & 0x0000CCCCu; hi ^= t ^ (t << 14);
+  t = (lo ^ __funnelshift_r(lo, hi, 28)) & 0xF0F0F0F0u;   // the 64-bit x ^ (x >> 28), low word
+  lo ^= t;
+  hi ^= t >> 4;
+}
+
+// The octet's exchange.  Lane e of the octet (lane & 7) holds b[t], the 8-bit
+// keep decisions of query qbase + 8t + e for the octet's eight consecutive
+// keys (bit k: key k).  Each lane packs its eight bytes, transposes them as
+// an 8 x 8 bit matrix (byte k then holds key k's decisions for its eight
+// queries), and the octet transposes the 8 x 8 byte matrix across its lanes
+// (three butterfly stages, one shuffle each), so that lane k ends with byte e
+// = lane e's byte k: bit 8e + t = kbit(8t + e) is query qbase + 8t + e of
+// key k.  Every lane of the warp must call it.
+__device__ __forceinline__ uint64_t octet_exchange(const uint32_t (&b)[8], int lane) {
+  uint32_t lo = __byte_perm(__byte_perm(b[0], b[1], 0x3340), __byte_perm(b[2], b[3], 0x3340), 0x5410);
+  uint32_t hi = __byte_perm(__byte_perm(b[4], b[5], 0x3340), __byte_perm(b[6], b[7], 0x3340), 0x5410);
+  bit_transpose8(lo, hi);
+  const bool x4 = lane & 4, x2 = lane & 2, x1 = lane & 1;
+  // stage 4: swap the off-diagonal 4 x 4 blocks (words)
+  const uint32_t r4 = __shfl_xor_sync(0xffffffffu, x4 ? lo : hi, 4);
+  if (x4) lo = r4; else hi = r4;
+  // stage 2: within each word, swap the off-diagonal 2 x 2 blocks (16-bit halves)
+  const uint32_t r2 = __shfl_xor_sync(0xffffffffu, __byte_perm(lo, hi, x2 ? 0x5410 : 0x7632), 2);
+  lo = __byte_perm(lo, r2, x2 ? 0x3254 : 0x5410);
+  hi = __byte_perm(hi, r2, x2 ? 0x3276 : 0x7610);
+  // stage 1: swap single bytes
+  const uint32_t r1 = __shfl_xor_sync(0xffffffffu, __byte_perm(lo, hi, x1 ? 0x6420 : 0x7531), 1);
+  lo = __byte_perm(lo, r1, x1 ? 0x3514 : 0x5240);
+  hi = __byte_perm(hi, r1, x1 ? 0x3716 : 0x7260);
+  return static_cast<uint64_t>(hi) << 32 | lo;
 }
 
 // Dropout keep bits of the key held by this lane for 64 consecutive queries
-// qbase .. qbase + 63 of flat head bhq: bit q set iff weight (qbase + q, key)
-// is kept.  The eight lanes of an octet hold eight consecutive keys
+// qbase .. qbase + 63 of flat head bhq, drawn: query qbase + q is bit
+// kbit(q).  The eight lanes of an octet hold eight consecutive keys
 // 8*jg .. 8*jg + 7, which one generator call covers for one query: lane e of
-// the octet draws for query qbase + 8t + e and the octet exchanges the
-// results (octet_gather8).  Every lane of the warp must call it.
+// the octet draws for queries qbase + 8t + e and the octet exchanges the
+// results (octet_exchange).  Every lane of the warp must call it.
 __device__ __forceinline__ uint64_t octet_keep_bits(const Dropout& d, uint32_t jg, int64_t qbase,
                                                     uint32_t bhq, int lane) {
   const int e = lane & 7;
-  uint64_t keep = 0;
+  uint32_t b[8];
 #pragma unroll
-  for (int t = 0; t < 8; ++t)
-    keep |= octet_gather8(keep8(d, jg, static_cast<uint32_t>(qbase + 8 * t + e), bhq), e) << (8 * t);
-  return keep;
+  for (int t = 0; t < 8; ++t) b[t] = keep8(d, jg, static_cast<uint32_t>(qbase + 8 * t + e), bhq);
+  return octet_exchange(b, lane);
 }
 
 // The same bits read from the keep mask (Dropout::mask), in two steps so the
@@ -70,8 +99,9 @@ __device__ __forceinline__ uint64_t octet_keep_bits(const Dropout& d, uint32_t j
 // of sequence v, key tile jt, the octet's byte `gbyte` (key group mod 16) of
 // the 16-byte entries of queries qbase .. qbase + 63 (lane e of the octet
 // reads queries qbase + 8t + e; queries past the sequence read as dropped),
-// and octet_mask_bits exchanges them within the octet as for drawn bits.
-// Every lane of the warp must call octet_mask_bits.
+// and octet_mask_bits exchanges them within the octet as for drawn bits
+// (query qbase + q is bit kbit(q)).  Every lane of the warp must call
+// octet_mask_bits.
 __device__ __forceinline__ void octet_mask_load(const Dropout& d, const Geo& g, const SeqView& v,
                                                 int64_t h, int64_t jt, int64_t qbase, int gbyte,
                                                 int lane, uint32_t (&b)[8]) {
@@ -83,11 +113,7 @@ __device__ __forceinline__ void octet_mask_load(const Dropout& d, const Geo& g, 
 }
 
 __device__ __forceinline__ uint64_t octet_mask_bits(const uint32_t (&b)[8], int lane) {
-  const int e = lane & 7;
-  uint64_t keep = 0;
-#pragma unroll
-  for (int t = 0; t < 8; ++t) keep |= octet_gather8(b[t], e) << (8 * t);
-  return keep;
+  return octet_exchange(b, lane);
 }
 
 // Staging of a CTA's partial dV (t = 0) and dK (t = 1) for the cluster

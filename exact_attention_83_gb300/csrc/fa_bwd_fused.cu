@@ -160,7 +160,7 @@ struct ProbStep {
 
 // P^T for this thread's key and its half's 64 queries: exp2(c*S - L*log2 e),
 // masked (keys past the sequence, causal diagonal), dropout keep bits into
-// `keep` (bit q: query qbase + q kept), and the rounded (dropped, rescaled)
+// `keep` (query qbase + q is bit kbit(q)), and the rounded (dropped)
 // P^T stored back over the scores for dV.
 template <typename T, bool DROP>
 __device__ __forceinline__ void form_probs(float (&p)[64], uint64_t& keep, uint32_t taddr,
@@ -189,12 +189,13 @@ __device__ __forceinline__ void form_probs(float (&p)[64], uint64_t& keep, uint3
   keep = 0;
   if constexpr (DROP) keep = octet_keep_bits(drop, static_cast<uint32_t>(key >> 3), s.qbase, s.bhq, lane);
   uint32_t w[32];
+  const uint32_t kl = static_cast<uint32_t>(keep), kh = static_cast<uint32_t>(keep >> 32);
 #pragma unroll
   for (int q = 0; q < 32; ++q) {
     if constexpr (DROP) {
       // P o keep; Z's 1 / (1 - p) scales dV when it is stored
-      w[q] = pack2<T>(((keep >> (2 * q)) & 1u) ? p[2 * q] : 0.f,
-                      ((keep >> (2 * q + 1)) & 1u) ? p[2 * q + 1] : 0.f);
+      w[q] = pack2<T>(kept64(kl, kh, kbit(2 * q)) ? p[2 * q] : 0.f,
+                      kept64(kl, kh, kbit(2 * q + 1)) ? p[2 * q + 1] : 0.f);
     } else {
       w[q] = pack2<T>(p[2 * q], p[2 * q + 1]);
     }
@@ -570,7 +571,8 @@ __global__ void __launch_bounds__(320, 1)
           // dS = P o (Z o dP - Delta), Z = keep / (1 - p)
 #pragma unroll
           for (int q = 0; q < 64; ++q) {
-            const float z = ((keep >> q) & 1u) ? a.drop.rscale : 0.f;
+            const float z = kept64(static_cast<uint32_t>(keep), static_cast<uint32_t>(keep >> 32),
+                                   kbit(q)) ? a.drop.rscale : 0.f;
             dp[q] = p[q] * fmaf(z, dp[q], -Ds[q]);
           }
         } else {

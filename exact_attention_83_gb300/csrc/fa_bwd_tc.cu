@@ -454,11 +454,12 @@ __global__ void __launch_bounds__(320, 1)
       if constexpr (DROP) {
         // P o keep, rounded pairs formed straight from p (no fp32 copy
         // kept); Z's 1 / (1 - p) scales dV when it is stored
+        const uint32_t kl = static_cast<uint32_t>(keep), kh = static_cast<uint32_t>(keep >> 32);
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          w[i] = pack2<T>(((keep >> (2 * i)) & 1u) ? p[2 * i] : 0.f,
-                          ((keep >> (2 * i + 1)) & 1u) ? p[2 * i + 1] : 0.f);
+          w[i] = pack2<T>(kept64(kl, kh, kbit(2 * i)) ? p[2 * i] : 0.f,
+                          kept64(kl, kh, kbit(2 * i + 1)) ? p[2 * i + 1] : 0.f);
         tmem_st32(lane_base + C::COL_ST + 64 * hf, w);
       } else {
         tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, p);
@@ -477,6 +478,7 @@ __global__ void __launch_bounds__(320, 1)
         // are held next to P: half 0's rounded dS lands on columns whose dP
         // was read first, half 1's on half 0's.
         const uint64_t rs2 = f32x2(a.drop.rscale, a.drop.rscale);
+        const uint32_t kl = static_cast<uint32_t>(keep), kh = static_cast<uint32_t>(keep >> 32);
         const uint32_t tdp = lane_base + C::COL_DPT + 64 * hf;
 #pragma unroll
         for (int hq = 0; hq < 2; ++hq) {
@@ -493,8 +495,8 @@ __global__ void __launch_bounds__(320, 1)
             f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), rs2,
                                   f32x2(d2.x, d2.y)),
                         x0, x1);
-            x0 = ((keep >> q) & 1u) ? x0 : d2.x;
-            x1 = ((keep >> (q + 1)) & 1u) ? x1 : d2.y;
+            x0 = kept64(kl, kh, kbit(q)) ? x0 : d2.x;
+            x1 = kept64(kl, kh, kbit(q + 1)) ? x1 : d2.y;
             f32x2_split(mul_f32x2(f32x2(x0, x1), f32x2(p[q], p[q + 1])), x0, x1);
             w[j / 2] = pack2<T>(x0, x1);
           }
@@ -918,6 +920,7 @@ __global__ void __launch_bounds__(320, 1)
         // held next to P: half 0's rounded dS lands on columns whose dP was
         // read first, half 1's on half 0's.
         const uint64_t rs2 = f32x2(a.drop.rscale, a.drop.rscale), nd = f32x2(-dl, -dl);
+        const uint32_t kl = static_cast<uint32_t>(keep), kh = static_cast<uint32_t>(keep >> 32);
         const uint32_t tdp = lane_base + C::COL_DP + 64 * hf;
 #pragma unroll
         for (int hq = 0; hq < 2; ++hq) {
@@ -932,8 +935,8 @@ __global__ void __launch_bounds__(320, 1)
             float x0, x1;
             f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), rs2, nd),
                         x0, x1);
-            x0 = ((keep >> q) & 1u) ? x0 : -dl;
-            x1 = ((keep >> (q + 1)) & 1u) ? x1 : -dl;
+            x0 = kept64(kl, kh, q) ? x0 : -dl;
+            x1 = kept64(kl, kh, q + 1) ? x1 : -dl;
             f32x2_split(mul_f32x2(f32x2(x0, x1), f32x2(p[q], p[q + 1])), x0, x1);
             w[j / 2] = pack2<T>(x0, x1);
           }

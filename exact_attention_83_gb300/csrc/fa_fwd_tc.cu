@@ -396,8 +396,8 @@ __global__ void __launch_bounds__(320, 1)
             // l sums the undropped weights; P V takes the kept ones (the
             // 1 / (1 - p) of Z is applied with 1 / l at the end)
             const int kk = 64 * hh + 2 * i;
-            const uint32_t bits = kb[kk >> 5] >> (kk & 31);
-            pk[i] = pack2<T>((bits & 1u) ? p0 : 0.f, (bits & 2u) ? p1 : 0.f);
+            pk[i] = pack2<T>((kb[kk >> 5] & (1u << (kk & 31))) ? p0 : 0.f,
+                             (kb[kk >> 5] & (2u << (kk & 31))) ? p1 : 0.f);
           } else {
             pk[i] = pack2<T>(p0, p1);
           }
@@ -750,8 +750,8 @@ __global__ void __launch_bounds__(192, 2)
             // l sums the undropped weights; P V takes the kept ones (the
             // 1 / (1 - p) of Z is applied with 1 / l at the end)
             const int kk = 64 * half + 2 * i;
-            const uint32_t bits = kb[kk >> 5] >> (kk & 31);
-            pk[i] = pack2<T>((bits & 1u) ? p0 : 0.f, (bits & 2u) ? p1 : 0.f);
+            pk[i] = pack2<T>((kb[kk >> 5] & (1u << (kk & 31))) ? p0 : 0.f,
+                             (kb[kk >> 5] & (2u << (kk & 31))) ? p1 : 0.f);
           } else {
             pk[i] = pack2<T>(p0, p1);
           }

@@ -148,6 +148,12 @@ inline int bwd_drop_mode(const Dropout& d) {
   return !d.on ? kDropNone : (d.mask != nullptr ? kDropRead : kDropDraw);
 }
 
+// Keep bit b (a compile-time constant wherever it is used) of 64 bits held
+// as two words: one masked test of one word, no 64-bit shift.
+__device__ __forceinline__ bool kept64(uint32_t lo, uint32_t hi, int b) {
+  return ((b < 32 ? lo : hi) & (1u << (b & 31))) != 0u;
+}
+
 // Byte offset in the keep mask of the 16-byte entry of (query head h of
 // sequence v, key tile jt, query row `row` of the sequence); entries of
 // consecutive rows are 16 bytes apart.
