@@ -454,12 +454,21 @@ __global__ void __launch_bounds__(320, 1)
       if constexpr (DROP) {
         // P o keep, rounded pairs formed straight from p (no fp32 copy
         // kept); Z's 1 / (1 - p) scales dV when it is stored
+        // Queries 8t + e and 8t + e + 1 (e even) are bits t of bytes e and
+        // e + 1 of keep: shifted by 7 - t, the pair's flags are those bytes'
+        // sign bits, which one prmt spreads over the pair's two halves.
         const uint32_t kl = static_cast<uint32_t>(keep), kh = static_cast<uint32_t>(keep >> 32);
         uint32_t w[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          w[i] = pack2<T>(kept64(kl, kh, kbit(2 * i)) ? p[2 * i] : 0.f,
-                          kept64(kl, kh, kbit(2 * i + 1)) ? p[2 * i + 1] : 0.f);
+        for (int t = 0; t < 8; ++t) {
+          const uint32_t xl = kl << (7 - t), xh = kh << (7 - t);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int q = 8 * t + e;
+            w[q / 2] = pack2<T>(p[q], p[q + 1]) &
+                       prmt(e < 4 ? xl : xh, 0u, half_sign_sel(e & 3, (e & 3) + 1));
+          }
+        }
         tmem_st32(lane_base + C::COL_ST + 64 * hf, w);
       } else {
         tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, p);

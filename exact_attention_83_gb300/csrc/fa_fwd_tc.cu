@@ -395,9 +395,12 @@ __global__ void __launch_bounds__(320, 1)
           if constexpr (DROP) {
             // l sums the undropped weights; P V takes the kept ones (the
             // 1 / (1 - p) of Z is applied with 1 / l at the end)
-            const int kk = 64 * hh + 2 * i;
-            pk[i] = pack2<T>((kb[kk >> 5] & (1u << (kk & 31))) ? p0 : 0.f,
-                             (kb[kk >> 5] & (2u << (kk & 31))) ? p1 : 0.f);
+            // keys kk, kk + 1 are bits b, b + 1 of byte kk / 8 % 4 of their
+            // word (b = kk % 8): shifted by 7 - b and 6 - b they are that
+            // byte's sign bits, which one prmt spreads over the pair's halves
+            const int kk = 64 * hh + 2 * i, byte = (kk >> 3) & 3, b = kk & 7;
+            const uint32_t wk = kb[kk >> 5];
+            pk[i] = pack2<T>(p0, p1) & prmt(wk << (7 - b), wk << (6 - b), half_sign_sel(byte, 4 + byte));
           } else {
             pk[i] = pack2<T>(p0, p1);
           }
@@ -749,9 +752,12 @@ __global__ void __launch_bounds__(192, 2)
           if constexpr (DROP) {
             // l sums the undropped weights; P V takes the kept ones (the
             // 1 / (1 - p) of Z is applied with 1 / l at the end)
-            const int kk = 64 * half + 2 * i;
-            pk[i] = pack2<T>((kb[kk >> 5] & (1u << (kk & 31))) ? p0 : 0.f,
-                             (kb[kk >> 5] & (2u << (kk & 31))) ? p1 : 0.f);
+            // keys kk, kk + 1 are bits b, b + 1 of byte kk / 8 % 4 of their
+            // word (b = kk % 8): shifted by 7 - b and 6 - b they are that
+            // byte's sign bits, which one prmt spreads over the pair's halves
+            const int kk = 64 * half + 2 * i, byte = (kk >> 3) & 3, b = kk & 7;
+            const uint32_t wk = kb[kk >> 5];
+            pk[i] = pack2<T>(p0, p1) & prmt(wk << (7 - b), wk << (6 - b), half_sign_sel(byte, 4 + byte));
           } else {
             pk[i] = pack2<T>(p0, p1);
           }

@@ -282,6 +282,21 @@ __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// prmt.b32: byte n of the result is byte (sel >> 4n) & 7 of {b, a} (a bytes
+// 0-3, b bytes 4-7), or, when bit 3 of that nibble is set, that byte's sign
+// bit replicated over all 8 bits.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Mask keeping the 16-bit halves of a packed pair whose flag is set: half 0
+// follows bit 7 of byte i0 of {b, a}, half 1 bit 7 of byte i1 (0..7).
+__device__ __forceinline__ constexpr uint32_t half_sign_sel(int i0, int i1) {
+  return static_cast<uint32_t>((8 | i0) | (8 | i0) << 4 | (8 | i1) << 8 | (8 | i1) << 12);
+}
+
 // ---------------------------------------------------------------- clusters
 // All threads of every CTA of the cluster (release / acquire).
 __device__ __forceinline__ void cluster_sync_all() {
