@@ -70,11 +70,15 @@ MEASURED_TRAFFIC = {
 # The long causal shape with half the heads: inputs (4 x 64 MiB) still exceed
 # L2, device footprint ~0.5 GB; used for counter captures.
 PROFILE_CASE = Workload("long-bf16-B1-H16-N16384-D128-causal", 1, 16, 16384, 128, "bf16", True)
+# The dropout workload at the profiling size (16 heads: inputs, outputs and the
+# 0.5 GB keep mask stay a few GB on the device under ncu).
+PROFILE_DROPOUT = GeneralWorkload("dropout0.1-bf16-B1-H16-N16384-D128-causal", 1, 16, 16, 16384,
+                                  16384, 128, "bf16", True, dropout_p=0.1)
 
 
 def workloads():
     ws = {LONG_CAUSAL.name: LONG_CAUSAL, PROFILE_CASE.name: PROFILE_CASE,
-          TINY_FP32.name: TINY_FP32}
+          TINY_FP32.name: TINY_FP32, PROFILE_DROPOUT.name: PROFILE_DROPOUT}
     ws.update({g.name: g for g in BENCH_GENERAL})
     for c in (False, True):
         w = bf16_n1024(c)
