@@ -117,28 +117,6 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
       "r"(c0), "r"(c1), "r"(c2), "r"(src)
       : "memory");
 }
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// The shared-memory sources of every committed bulk group have been read.
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Every committed bulk group has completed.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy reads (tensor-core operands, TMA sources).
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
-                                             uint32_t w) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
-               "r"(w)
-               : "memory");
-}
 
 // Writes one 128-byte row (8 16-byte units) of a 128-byte-swizzled tile:
 // unit u of row r goes to unit u ^ (r mod 8).

@@ -178,28 +178,52 @@ __global__ void __launch_bounds__(320, 1)
     return;
   }
 
-  if (threadIdx.x == 0) {
-    mbar_init(b_kv, 1);
-    for (int s = 0; s < C::NQ; ++s) {
-      mbar_init(b_qfull0 + 8 * s, 1);
-      mbar_init(b_qempty0 + 8 * s, 1);
-    }
-    for (int s = 0; s < C::ND; ++s) {
-      mbar_init(b_dfull0 + 8 * s, 32);
-      mbar_init(b_dempty0 + 8 * s, 1);
-    }
-    mbar_init(b_sfull, 1);
-    mbar_init(b_dpfull, 1);
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(b_pready0 + 8 * h, 128);
-      mbar_init(b_dsready0 + 8 * h, 128);
-    }
-    mbar_init(b_accdone, 1);
-    mbar_init(b_mmadone, 1);
-    ctl->abort = 0;
-    mbar_fence_init();
-  }
+  // The producer's lane 0 sets up the barriers and sends the first copies
+  // (K, V, Q and dO of the first step) before the block-wide sync, so their
+  // latency overlaps the set-up; the first step's L, Delta and the dO
+  // barrier's arrivals follow in the producer loop.
+  const int64_t q_first = static_cast<int64_t>(i0) * C::BT;
+  const int32_t hq_first = static_cast<int32_t>(hk * a.g.G + g0);
   if (warp == 8) {
+    if (lane == 0) {
+      mbar_init(b_kv, 1);
+      for (int s = 0; s < C::NQ; ++s) {
+        mbar_init(b_qfull0 + 8 * s, 1);
+        mbar_init(b_qempty0 + 8 * s, 1);
+      }
+      for (int s = 0; s < C::ND; ++s) {
+        mbar_init(b_dfull0 + 8 * s, 32);
+        mbar_init(b_dempty0 + 8 * s, 1);
+      }
+      mbar_init(b_sfull, 1);
+      mbar_init(b_dpfull, 1);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(b_pready0 + 8 * h, 128);
+        mbar_init(b_dsready0 + 8 * h, 128);
+      }
+      mbar_init(b_accdone, 1);
+      mbar_init(b_mmadone, 1);
+      ctl->abort = 0;
+      mbar_fence_init();
+      tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
+      mbar_arrive_expect_tx(b_kv, 2 * C::TILE);
+      for (int c = 0; c < C::DC; ++c) {
+        tma_load_4d(smem_u32(sK + c * C::CHUNK), &tmk, b_kv, c * 64,
+                    static_cast<int32_t>(sv.k0 + kt * C::BT), hk, bb);
+        tma_load_4d(smem_u32(sV + c * C::CHUNK), &tmv, b_kv, c * 64,
+                    static_cast<int32_t>(sv.k0 + kt * C::BT), hk, bb);
+      }
+      mbar_arrive_expect_tx(b_qfull0, C::TILE);
+      for (int c = 0; c < C::DC; ++c)
+        tma_load_4d(smem_u32(sQ + c * C::CHUNK), &tmq, b_qfull0, c * 64,
+                    static_cast<int32_t>(sv.q0 + q_first), hq_first, bb);
+      mbar_expect_tx(b_dfull0, C::TILE);
+      for (int c = 0; c < C::DC; ++c)
+        tma_load_4d(smem_u32(sD + c * C::CHUNK), &tmdo, b_dfull0, c * 64,
+                    static_cast<int32_t>(sv.q0 + q_first), hq_first, bb);
+    }
+    __syncwarp();
     tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -217,17 +241,7 @@ __global__ void __launch_bounds__(320, 1)
     // free, so their latency overlaps the wait), both negated so that the
     // elementwise warps add them directly.  Rows past N get L = +inf, so
     // their probabilities are exactly 0, and Delta = 0.
-    if (lane == 0) {
-      tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
-      mbar_arrive_expect_tx(b_kv, 2 * C::TILE);
-      for (int c = 0; c < C::DC; ++c) {
-        tma_load_4d(smem_u32(sK + c * C::CHUNK), &tmk, b_kv, c * 64,
-                    static_cast<int32_t>(sv.k0 + kt * C::BT), hk, bb);
-        tma_load_4d(smem_u32(sV + c * C::CHUNK), &tmv, b_kv, c * 64,
-                    static_cast<int32_t>(sv.k0 + kt * C::BT), hk, bb);
-      }
-    }
+    // (K, V and the first step's Q and dO tiles were sent before the sync)
     uint32_t q_round[C::NQ], d_round[C::ND];
 #pragma unroll
     for (int s = 0; s < C::NQ; ++s) q_round[s] = 0;
@@ -240,7 +254,9 @@ __global__ void __launch_bounds__(320, 1)
       // Q_i
       const int qs = it % C::NQ;
       const uint32_t qr = static_cast<uint32_t>(it / C::NQ);
-      if (lane == 0) {
+      if (lane == 0 && it == 0) {
+        q_round[0] = 1;                      // sent before the sync
+      } else if (lane == 0) {
         if (qr > 0 && !wait_bounded(b_qempty0 + 8 * qs, (qr - 1) & 1, ctl, a.status, a.timeout_ns))
           ok = false;
         if (ok) {
@@ -274,13 +290,13 @@ __global__ void __launch_bounds__(320, 1)
         L2s[lane * 4 + t] = lv[t];
         Ds[lane * 4 + t] = dv[t];
       }
-      if (lane == 0) {
+      if (lane == 0 && it > 0) {
         mbar_arrive_expect_tx(b_dfull0 + 8 * ds, C::TILE);
         for (int c = 0; c < C::DC; ++c)
           tma_load_4d(smem_u32(slot + c * C::CHUNK), &tmdo, b_dfull0 + 8 * ds, c * 64,
                       static_cast<int32_t>(sv.q0 + q0), hq, bb);
       } else {
-        mbar_arrive(b_dfull0 + 8 * ds);
+        mbar_arrive(b_dfull0 + 8 * ds);     // step 0: dO sent (expect_tx) before the sync
       }
       d_round[ds] = dr + 1;
     }
@@ -533,19 +549,31 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (ok) ok = wait_warp(b_accdone, 0, ctl, a.status, a.timeout_ns);
     ew_ok = ok;
-    if (ok) {
+    const uint32_t acc = lane_base + (hf == 0 ? C::COL_DV : C::COL_DK);
+    const float mul = hf == 0 ? (DROP ? a.drop.rscale : 1.f) : a.scale;
+    if (split == 1) {
+      // Rows staged in shared memory (the Q ring is idle once every product
+      // has completed) as the loads lay them out, then stored by the
+      // warpgroup with consecutive threads on consecutive 16 bytes of a row:
+      // whole lines per warp store instead of each thread's scattered row.
+      // Rows past the sequence (the next packed sequence's) are not written.
+      // Every thread of the warpgroup passes the barrier, also after a
+      // timeout; the stores go out only if all of them got this far.
+      const uint32_t stg = smem_u32(sQ) + static_cast<uint32_t>(hf * C::TILE);
+      if (ok) {
+        tc_fence_after();
+        stage_row_sw128<T>(acc, mul, stg, row, 0, D);
+      }
+      if (bar_red_and(1 + hf, 128, ok)) {
+        const int64_t* st = hf == 0 ? a.s0 : a.s1;
+        T* row0 = static_cast<T*>(hf == 0 ? a.out0 : a.out1) + bb * st[0] + hk * st[1] +
+                  (sv.k0 + kt * C::BT) * st[2];
+        store_staged_tile<T>(stg, D, threadIdx.x & 127, 128, row0, st[2],
+                             static_cast<int>(Nk - kt * C::BT < C::BT ? Nk - kt * C::BT : C::BT), a.dreal);
+      }
+    } else if (ok) {
       tc_fence_after();
-      const bool store = key < Nk;
-      const uint32_t acc = lane_base + (hf == 0 ? C::COL_DV : C::COL_DK);
-      if (split == 1) {
-        if (hf == 0) {
-          T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hk * a.s0[1] + (sv.k0 + key) * a.s0[2];
-          store_row_cols<T>(acc, DROP ? a.drop.rscale : 1.f, out, store, a.dreal);
-        } else {
-          T* out = static_cast<T*>(a.out1) + bb * a.s1[0] + hk * a.s1[1] + (sv.k0 + key) * a.s1[2];
-          store_row_cols<T>(acc, a.scale, out, store, a.dreal);
-        }
-      } else if (rank != 0) {
+      if (rank != 0) {
         // partial sums into this CTA's shared memory for rank 0 to read
         float* st = stage_row<D>(smem, hf, row);
 #pragma unroll 1
@@ -711,23 +739,48 @@ __global__ void __launch_bounds__(320, 1)
     return;
   }
 
-  if (threadIdx.x == 0) {
-    mbar_init(b_q, 1);
-    for (int s = 0; s < C::NST; ++s) {
-      mbar_init(b_kvfull0 + 8 * s, 1);
-      mbar_init(b_kvempty0 + 8 * s, 1);
+  // The producer's lane 0 sets up the barriers and sends the first copies
+  // (Q, dO and the K | V tiles of the stages that do not hold Q | dO) before
+  // the block-wide sync, so their latency overlaps the set-up.
+  const int jt_early = n < C::QSLOT ? n : C::QSLOT;   // key tiles sent before the sync
+  auto load_kv = [&](int jt, int st) {
+    uint8_t* stage = sStage + st * C::STAGE;
+    mbar_arrive_expect_tx(b_kvfull0 + 8 * st, 2 * C::TILE);
+    for (int c = 0; c < C::DC; ++c) {
+      const int32_t krow = static_cast<int32_t>(sv.k0 + static_cast<int64_t>(jt) * C::BT);
+      tma_load_4d(smem_u32(stage + c * C::CHUNK), &tmk, b_kvfull0 + 8 * st, c * 64, krow, hk, bb);
+      tma_load_4d(smem_u32(stage + C::TILE + c * C::CHUNK), &tmv, b_kvfull0 + 8 * st, c * 64,
+                  krow, hk, bb);
     }
-    mbar_init(b_sfull, 1);
-    mbar_init(b_sfree, 256);
-    mbar_init(b_dpfull, 1);
-    for (int h = 0; h < 2; ++h) mbar_init(b_dsready0 + 8 * h, 128);
-    mbar_init(b_accdone, 1);
-    mbar_init(b_mmadone, 1);
-    mbar_init(b_qt, 256);
-    ctl->abort = 0;
-    mbar_fence_init();
-  }
+  };
   if (warp == 8) {
+    if (lane == 0) {
+      mbar_init(b_q, 1);
+      for (int s = 0; s < C::NST; ++s) {
+        mbar_init(b_kvfull0 + 8 * s, 1);
+        mbar_init(b_kvempty0 + 8 * s, 1);
+      }
+      mbar_init(b_sfull, 1);
+      mbar_init(b_sfree, 256);
+      mbar_init(b_dpfull, 1);
+      for (int h = 0; h < 2; ++h) mbar_init(b_dsready0 + 8 * h, 128);
+      mbar_init(b_accdone, 1);
+      mbar_init(b_mmadone, 1);
+      mbar_init(b_qt, 256);
+      ctl->abort = 0;
+      mbar_fence_init();
+      tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
+      mbar_arrive_expect_tx(b_q, 2 * C::TILE);
+      for (int c = 0; c < C::DC; ++c) {
+        tma_load_4d(smem_u32(sQ + c * C::CHUNK), &tmq, b_q, c * 64,
+                    static_cast<int32_t>(sv.q0 + qt * C::BT), hq, bb);
+        tma_load_4d(smem_u32(sDO + c * C::CHUNK), &tmdo, b_q, c * 64,
+                    static_cast<int32_t>(sv.q0 + qt * C::BT), hq, bb);
+      }
+      for (int jt = 0; jt < jt_early; ++jt) load_kv(jt, jt);   // stages 0 .. QSLOT - 1, round 0
+    }
+    __syncwarp();
     tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -739,19 +792,11 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
-      mbar_arrive_expect_tx(b_q, 2 * C::TILE);
-      for (int c = 0; c < C::DC; ++c) {
-        tma_load_4d(smem_u32(sQ + c * C::CHUNK), &tmq, b_q, c * 64,
-                    static_cast<int32_t>(sv.q0 + qt * C::BT), hq, bb);
-        tma_load_4d(smem_u32(sDO + c * C::CHUNK), &tmdo, b_q, c * 64,
-                    static_cast<int32_t>(sv.q0 + qt * C::BT), hq, bb);
-      }
+      // (Q, dO and key tiles 0 .. jt_early - 1 were sent before the sync)
       uint32_t last_round[C::NST];
 #pragma unroll
-      for (int s = 0; s < C::NST; ++s) last_round[s] = 0;
-      for (int jt = 0; jt < n; ++jt) {
+      for (int s = 0; s < C::NST; ++s) last_round[s] = s < jt_early ? 1u : 0u;
+      for (int jt = jt_early; jt < n; ++jt) {
         const int st = jt % C::NST;
         const uint32_t r = static_cast<uint32_t>(jt / C::NST);
         if (r > 0) {
@@ -760,14 +805,7 @@ __global__ void __launch_bounds__(320, 1)
           // this stage still holds Q | dO until they have been copied into TMEM
           if (!wait_bounded(b_qt, 0, ctl, a.status, a.timeout_ns)) break;
         }
-        uint8_t* stage = sStage + st * C::STAGE;
-        mbar_arrive_expect_tx(b_kvfull0 + 8 * st, 2 * C::TILE);
-        for (int c = 0; c < C::DC; ++c) {
-          const int32_t krow = static_cast<int32_t>(sv.k0 + static_cast<int64_t>(jt) * C::BT);
-          tma_load_4d(smem_u32(stage + c * C::CHUNK), &tmk, b_kvfull0 + 8 * st, c * 64, krow, hk, bb);
-          tma_load_4d(smem_u32(stage + C::TILE + c * C::CHUNK), &tmv, b_kvfull0 + 8 * st, c * 64,
-                      krow, hk, bb);
-        }
+        load_kv(jt, st);
         last_round[st] = r + 1;
       }
       wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns, false);
@@ -968,14 +1006,22 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(b_dsready0 + 8 * hf);
     }
     if (ok) ok = wait_warp(b_accdone, 0, ctl, a.status, a.timeout_ns);
+    // Each warpgroup stages half the columns of its rows in shared memory (the
+    // K | V stages are idle once every product has completed) as the loads
+    // lay them out; then the 256 threads store the tile with consecutive
+    // threads on consecutive 16 bytes of a row (whole lines per warp store).
+    // Rows past the sequence and columns past a narrow head dimension are not
+    // written.  Every elementwise thread passes the barrier, also after a
+    // timeout; the stores go out only if all of them got this far.
+    const uint32_t stg = smem_u32(sStage);
     if (ok) {
       tc_fence_after();
-      // each warpgroup stores half the columns; a zero-padded narrow head
-      // dimension is stored by warpgroup 0 alone
-      const int half = a.dreal == D ? D / 2 : (hf == 0 ? a.dreal : 0);
-      const int c0 = a.dreal == D ? (D / 2) * hf : 0;
-      T* out = static_cast<T*>(a.out0) + bb * a.s0[0] + hq * a.s0[1] + (sv.q0 + qrow) * a.s0[2] + c0;
-      if (half > 0) store_row_cols<T>(lane_base + C::COL_DQ + c0, a.scale, out, qrow < Nq, half);
+      stage_row_sw128<T>(lane_base + C::COL_DQ + (D / 2) * hf, a.scale, stg, row, (D / 2) * hf, D / 2);
+    }
+    if (bar_red_and(1, 256, ok)) {
+      T* row0 = static_cast<T*>(a.out0) + bb * a.s0[0] + hq * a.s0[1] + (sv.q0 + qt * C::BT) * a.s0[2];
+      store_staged_tile<T>(stg, D, threadIdx.x, 256, row0, a.s0[2],
+                           static_cast<int>(Nq - qt * C::BT < C::BT ? Nq - qt * C::BT : C::BT), a.dreal);
     }
   }
 
@@ -1021,6 +1067,7 @@ fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
   if (blocks1 > 0x7fffffffLL) return FA_ERR_SHAPE;
   a.out0 = p.dv; a.out1 = p.dk;
   for (int i = 0; i < 4; ++i) { a.s0[i] = p.sdv[i]; a.s1[i] = p.sdk[i]; }
+
   auto k1 = bwd_dkdv_tc_kernel<T, D, DROP>;
   if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM) != cudaSuccess)
     return FA_ERR_LAUNCH;

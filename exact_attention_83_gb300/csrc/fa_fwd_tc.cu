@@ -148,23 +148,52 @@ __global__ void __launch_bounds__(320, 1)
     return;
   }
 
-  if (threadIdx.x == 0) {
-    mbar_init(b_q, 1);
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(b_full0 + 8 * s, 1);
-      mbar_init(b_empty0 + 8 * s, 1);
-    }
-    for (int g = 0; g < 2; ++g) {
-      mbar_init(b_sfull0 + 8 * g, 1);
-      mbar_init(b_pready0 + 8 * (2 * g), 128);
-      mbar_init(b_pready0 + 8 * (2 * g + 1), 128);
-      mbar_init(b_ofinal0 + 8 * g, 1);
-    }
-    mbar_init(b_mmadone, 1);
-    ctl->abort = 0;
-    mbar_fence_init();
-  }
+  // K | V ring units: unit u = 2j + kv (K_j, V_j) in slot u % NS.  The
+  // producer's lane 0 sets up the barriers and sends Q and the ring's first
+  // round of units before the block-wide sync, so their latency overlaps the
+  // set-up.
+  uint32_t issued[C::NS];   // producer lane 0: rounds issued per ring slot
+#pragma unroll
+  for (int s = 0; s < C::NS; ++s) issued[s] = 0;
+  auto issue_unit = [&](int u) {
+    const int j = u >> 1, kv = u & 1, s = u % C::NS;
+    mbar_arrive_expect_tx(b_full0 + 8 * s, C::TILE);
+    for (int c = 0; c < C::DC; ++c)
+      tma_load_4d(smem_u32(sRing + s * C::TILE + c * C::CHUNK), kv ? &tmv : &tmk,
+                  b_full0 + 8 * s, c * 64, static_cast<int32_t>(sv.k0 + j * C::BN), hk, bb);
+    issued[s] = static_cast<uint32_t>(u / C::NS) + 1;
+  };
+  const int u_early = 2 * nmax < C::NS ? 2 * nmax : C::NS;   // round 0 of the ring
   if (warp == 8) {
+    if (lane == 0) {
+      mbar_init(b_q, 1);
+      for (int s = 0; s < C::NS; ++s) {
+        mbar_init(b_full0 + 8 * s, 1);
+        mbar_init(b_empty0 + 8 * s, 1);
+      }
+      for (int g = 0; g < 2; ++g) {
+        mbar_init(b_sfull0 + 8 * g, 1);
+        mbar_init(b_pready0 + 8 * (2 * g), 128);
+        mbar_init(b_pready0 + 8 * (2 * g + 1), 128);
+        mbar_init(b_ofinal0 + 8 * g, 1);
+      }
+      mbar_init(b_mmadone, 1);
+      ctl->abort = 0;
+      mbar_fence_init();
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      const uint32_t qbytes = (ntile[0] > 0 ? C::TILE : 0) + (ntile[1] > 0 ? C::TILE : 0);
+      mbar_arrive_expect_tx(b_q, qbytes);
+      for (int g = 0; g < 2; ++g) {
+        if (ntile[g] == 0) continue;
+        for (int c = 0; c < C::DC; ++c)
+          tma_load_4d(smem_u32(sQ + g * C::TILE + c * C::CHUNK), &tmq, b_q, c * 64,
+                      static_cast<int32_t>(sv.q0 + (2 * pr + g) * C::BM), hq, bb);
+      }
+      for (int u = 0; u < u_early; ++u) issue_unit(u);
+    }
+    __syncwarp();
     tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -176,34 +205,14 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmq);
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
-      uint32_t issued[C::NS];
-#pragma unroll
-      for (int s = 0; s < C::NS; ++s) issued[s] = 0;
-      const uint32_t qbytes = (ntile[0] > 0 ? C::TILE : 0) + (ntile[1] > 0 ? C::TILE : 0);
-      mbar_arrive_expect_tx(b_q, qbytes);
-      for (int g = 0; g < 2; ++g) {
-        if (ntile[g] == 0) continue;
-        for (int c = 0; c < C::DC; ++c)
-          tma_load_4d(smem_u32(sQ + g * C::TILE + c * C::CHUNK), &tmq, b_q, c * 64,
-                      static_cast<int32_t>(sv.q0 + (2 * pr + g) * C::BM), hq, bb);
-      }
       bool ok = true;
-      for (int j = 0; ok && j < nmax; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          const int u = 2 * j + kv, s = u % C::NS;
-          const uint32_t r = static_cast<uint32_t>(u / C::NS);
-          if (r > 0 && !(ok = wait_bounded(b_empty0 + 8 * s, (r - 1) & 1, ctl, a.status,
-                                           a.timeout_ns)))
-            break;
-          mbar_arrive_expect_tx(b_full0 + 8 * s, C::TILE);
-          for (int c = 0; c < C::DC; ++c)
-            tma_load_4d(smem_u32(sRing + s * C::TILE + c * C::CHUNK), kv ? &tmv : &tmk,
-                        b_full0 + 8 * s, c * 64, static_cast<int32_t>(sv.k0 + j * C::BN), hk, bb);
-          issued[s] = r + 1;
-        }
+      for (int u = u_early; ok && u < 2 * nmax; ++u) {
+        const int s = u % C::NS;
+        const uint32_t r = static_cast<uint32_t>(u / C::NS);
+        if (r > 0 && !(ok = wait_bounded(b_empty0 + 8 * s, (r - 1) & 1, ctl, a.status,
+                                         a.timeout_ns)))
+          break;
+        issue_unit(u);
       }
       // Drain: every copy issued has landed before the CTA may exit.
       wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns, false);
@@ -431,13 +440,28 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) break;
     }
     if (ok && n > 0) ok = wait_warp(b_ofinal0 + 8 * g, 0, ctl, a.status, a.timeout_ns);
-    if (ok && n > 0) {
-      tc_fence_after();
-      const float inv = (DROP ? a.drop.rscale : 1.f) / l;   // Z's 1 / (1 - p) with dropout
-      const bool store = qrow < Nq;
-      T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qrow) * a.so[2];
-      store_row_cols<T>(tO, inv, orow, store, a.dreal);
-      if (store) a.lse[lse_index(a.g, sv, h, qrow)] = (m + log2f(l)) * kLn2;
+    // O / l staged in shared memory over this tile's Q (no product reads it
+    // once the tile's last P V, committed after its last S, has completed;
+    // the other tile's products may still be using the K | V ring) and
+    // stored by the tile's four warps with consecutive threads on
+    // consecutive 16 bytes of a row (whole lines per warp store); rows past
+    // the sequence are not written.  Every thread of the tile's warpgroup
+    // passes the barrier, also after a timeout; the stores go out only if
+    // all of them got this far.
+    if (n > 0) {
+      const uint32_t stg = smem_u32(sQ) + static_cast<uint32_t>(g * C::TILE);
+      if (ok) {
+        tc_fence_after();
+        const float inv = (DROP ? a.drop.rscale : 1.f) / l;   // Z's 1 / (1 - p) with dropout
+        stage_row_sw128<T>(tO, inv, stg, r, 0, D);
+        if (qrow < Nq) a.lse[lse_index(a.g, sv, h, qrow)] = (m + log2f(l)) * kLn2;
+      }
+      if (bar_red_and(1 + g, 128, ok)) {
+        T* row0 = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qt * C::BM) * a.so[2];
+        store_staged_tile<T>(stg, D, threadIdx.x & 127, 128, row0, a.so[2],
+                             static_cast<int>(Nq - qt * C::BM < C::BM ? Nq - qt * C::BM : C::BM),
+                             a.dreal);
+      }
     }
   }
 
@@ -528,21 +552,48 @@ __global__ void __launch_bounds__(192, 2)
     return;
   }
 
-  if (threadIdx.x == 0) {
-    mbar_init(b_q, 1);
-    for (int s = 0; s < C::NS; ++s) {
-      mbar_init(b_full0 + 8 * s, 1);
-      mbar_init(b_empty0 + 8 * s, 1);
-    }
-    mbar_init(b_sfull, 1);
-    mbar_init(b_sfree, 128);
-    mbar_init(b_pready, 128);
-    mbar_init(b_pvdone, 1);
-    mbar_init(b_mmadone, 1);
-    ctl->abort = 0;
-    mbar_fence_init();
-  }
+  // K | V ring units in consumption order K_0, K_1, V_0, K_2, V_1, ...; unit
+  // 2*n - 1 would be K_n (absent).  The producer's lane 0 sets up the
+  // barriers and sends Q and the ring's first round of units before the
+  // block-wide sync, so their latency overlaps the set-up.
+  uint32_t issued[C::NS];   // producer lane 0: rounds issued per ring slot
+#pragma unroll
+  for (int s = 0; s < C::NS; ++s) issued[s] = 0;
+  auto issue_unit = [&](int u) {
+    int j, kv;
+    if (u == 0) { j = 0; kv = 0; }
+    else if (u & 1) { j = (u + 1) / 2; kv = 0; }
+    else { j = (u - 2) / 2; kv = 1; }
+    if (j >= n) return;
+    const int s = u % C::NS;
+    mbar_arrive_expect_tx(b_full0 + 8 * s, C::TILE);
+    tma_load_4d(smem_u32(sRing + s * C::TILE), kv ? &tmv : &tmk, b_full0 + 8 * s, 0,
+                static_cast<int32_t>(sv.k0 + j * C::BN), hk, bb);
+    issued[s] = static_cast<uint32_t>(u / C::NS) + 1;
+  };
+  const int u_early = 2 * n + 1 < C::NS ? 2 * n + 1 : C::NS;   // round 0 of the ring
   if (warp == 4) {
+    if (lane == 0) {
+      mbar_init(b_q, 1);
+      for (int s = 0; s < C::NS; ++s) {
+        mbar_init(b_full0 + 8 * s, 1);
+        mbar_init(b_empty0 + 8 * s, 1);
+      }
+      mbar_init(b_sfull, 1);
+      mbar_init(b_sfree, 128);
+      mbar_init(b_pready, 128);
+      mbar_init(b_pvdone, 1);
+      mbar_init(b_mmadone, 1);
+      ctl->abort = 0;
+      mbar_fence_init();
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      mbar_arrive_expect_tx(b_q, C::TILE);
+      tma_load_4d(smem_u32(sQ), &tmq, b_q, 0, static_cast<int32_t>(sv.q0 + qt * C::BM), hq, bb);
+      for (int u = 0; u < u_early; ++u) issue_unit(u);
+    }
+    __syncwarp();
     tmem_alloc(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -554,31 +605,14 @@ __global__ void __launch_bounds__(192, 2)
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmq);
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
-      uint32_t issued[C::NS];
-#pragma unroll
-      for (int s = 0; s < C::NS; ++s) issued[s] = 0;
-      mbar_arrive_expect_tx(b_q, C::TILE);
-      tma_load_4d(smem_u32(sQ), &tmq, b_q, 0, static_cast<int32_t>(sv.q0 + qt * C::BM), hq, bb);
       bool ok = true;
-      // units in consumption order; unit 2*n - 1 would be K_n (absent)
-      for (int u = 0; ok && u <= 2 * n; ++u) {
-        int j, kv;
-        if (u == 0) { j = 0; kv = 0; }
-        else if (u & 1) { j = (u + 1) / 2; kv = 0; }
-        else { j = (u - 2) / 2; kv = 1; }
-        if (j >= n) continue;
+      for (int u = u_early; ok && u <= 2 * n; ++u) {
         const int s = u % C::NS;
         const uint32_t r = static_cast<uint32_t>(u / C::NS);
         if (r > 0 && !(ok = wait_bounded(b_empty0 + 8 * s, (r - 1) & 1, ctl, a.status,
                                          a.timeout_ns)))
           break;
-        mbar_arrive_expect_tx(b_full0 + 8 * s, C::TILE);
-        tma_load_4d(smem_u32(sRing + s * C::TILE), kv ? &tmv : &tmk, b_full0 + 8 * s, 0,
-                    static_cast<int32_t>(sv.k0 + j * C::BN), hk, bb);
-        issued[s] = r + 1;
+        issue_unit(u);
       }
       // Drain: every copy issued has landed before the CTA may exit.
       wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns, false);
@@ -791,13 +825,23 @@ __global__ void __launch_bounds__(192, 2)
       mbar_arrive(b_pready);
     }
     if (ok) ok = wait_warp(b_pvdone, (n - 1) & 1, ctl, a.status, a.timeout_ns);
+    // O / l staged in shared memory (the K | V ring is idle once the last
+    // P V has completed) as the loads lay it out, then stored by the four
+    // warps with consecutive threads on consecutive 16 bytes of a row (whole
+    // lines per warp store); rows past the sequence are not written.  Every
+    // softmax thread passes the barrier, also after a timeout; the stores go
+    // out only if all of them got this far.
+    const uint32_t stg = smem_u32(sRing);
     if (ok) {
       tc_fence_after();
       const float inv = (DROP ? a.drop.rscale : 1.f) / l;   // Z's 1 / (1 - p) with dropout
-      const bool store = qrow < Nq;
-      T* orow = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qrow) * a.so[2];
-      store_row_cols<T>(tO, inv, orow, store, a.dreal);
-      if (store) a.lse[lse_index(a.g, sv, h, qrow)] = (m + log2f(l)) * kLn2;
+      stage_row_sw128<T>(tO, inv, stg, r, 0, D);
+      if (qrow < Nq) a.lse[lse_index(a.g, sv, h, qrow)] = (m + log2f(l)) * kLn2;
+    }
+    if (bar_red_and(1, 128, ok)) {
+      T* row0 = static_cast<T*>(a.o) + bb * a.so[0] + hq * a.so[1] + (sv.q0 + qt * C::BM) * a.so[2];
+      store_staged_tile<T>(stg, D, threadIdx.x, 128, row0, a.so[2],
+                           static_cast<int>(Nq - qt * C::BM < C::BM ? Nq - qt * C::BM : C::BM), a.dreal);
     }
   }
 

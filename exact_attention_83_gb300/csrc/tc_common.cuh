@@ -47,6 +47,13 @@ __device__ __forceinline__ void mbar_fence_init() {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Raises the transaction count of the barrier's current phase without an
+// arrival (the arrivals come separately).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
@@ -116,6 +123,39 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The shared-memory sources of every committed bulk group have been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every committed bulk group has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads (tensor-core operands, TMA sources).
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
+               "r"(w)
+               : "memory");
+}
+// Barrier `id` (1..15) over `count` threads (a multiple of 32) that also
+// returns the AND of every participant's `v`.  Every participating thread
+// must reach it, including those whose earlier waits ran out.
+__device__ __forceinline__ bool bar_red_and(int id, int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, %3, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}" : "=r"(r) : "r"(v ? 1u : 0u), "r"(id), "r"(count) : "memory");
+  return r != 0u;
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -455,6 +495,57 @@ __device__ __forceinline__ float ex2(float x) {
 namespace fa {
 namespace tc {
 
+// Epilogue staging: `ncols` (a multiple of 32) fp32 columns of this thread's
+// TMEM lane starting at taddr, times `mul`, rounded to T, written as columns
+// col0 .. col0 + ncols - 1 (col0 a multiple of 32) of row `row` of a
+// shared-memory tile laid out as the 128-byte-swizzled loads are (64-column
+// chunks of 128 rows x 128 bytes, chunk c at tile + c * 16384, 16-byte unit u
+// of a row at unit u ^ (row % 8)); a warp's eight-row groups cover all banks.
+template <typename T>
+__device__ __forceinline__ void stage_row_sw128(uint32_t taddr, float mul, uint32_t tile, int row,
+                                                int col0, int ncols) {
+  for (int c = 0; c < ncols; c += 32) {
+    uint32_t t[32];
+    tmem_ld32(taddr + c, t);
+    tmem_wait_ld();
+    reg_fence32(t);
+    const int col = col0 + c;
+    const uint32_t rbase = tile + static_cast<uint32_t>(col / 64) * 16384u + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int u = ((col % 64) / 8) + v, e = 8 * v;
+      st_shared_v4(rbase + static_cast<uint32_t>((u ^ (row & 7)) * 16),
+                   pack2<T>(__uint_as_float(t[e]) * mul, __uint_as_float(t[e + 1]) * mul),
+                   pack2<T>(__uint_as_float(t[e + 2]) * mul, __uint_as_float(t[e + 3]) * mul),
+                   pack2<T>(__uint_as_float(t[e + 4]) * mul, __uint_as_float(t[e + 5]) * mul),
+                   pack2<T>(__uint_as_float(t[e + 6]) * mul, __uint_as_float(t[e + 7]) * mul));
+    }
+  }
+}
+
+// Stores a tile staged by stage_row_sw128 (`ncols` columns, 128 rows) from
+// shared memory to global memory, thread t of `nthreads` taking every
+// nthreads-th 16-byte unit: consecutive threads write consecutive units of a
+// row, so a warp's store covers whole lines.  Rows at or past `nrows` and
+// columns at or past `dreal` (a multiple of 8) are not written.
+template <typename T>
+__device__ __forceinline__ void store_staged_tile(uint32_t tile, int ncols, int t, int nthreads,
+                                                  T* row0, int64_t row_stride, int nrows,
+                                                  int dreal) {
+  const int units = ncols / 8;   // 16-byte units per row
+  for (int j = t; j < 128 * units; j += nthreads) {
+    const int r = j / units, u = j % units;
+    if (r < nrows && 8 * u < dreal) {
+      uint32_t x, y, z, w;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(x), "=r"(y), "=r"(z), "=r"(w)
+                   : "r"(tile + static_cast<uint32_t>((u >> 3) * 16384 + r * 128 +
+                                                      (((u & 7) ^ (r & 7)) * 16))));
+      *reinterpret_cast<uint4*>(row0 + r * row_stride + 8 * u) = make_uint4(x, y, z, w);
+    }
+  }
+}
+
 // Epilogue store: `ncols` (a multiple of 16, at most 128, uniform across the
 // warp) fp32 columns of this thread's TMEM lane starting at taddr, times
 // `mul`, rounded to T and written to `row` (16-byte vector stores) when
@@ -464,6 +555,29 @@ template <typename T>
 __device__ __forceinline__ void store_row_cols(uint32_t taddr, float mul, T* row, bool store,
                                                int ncols) {
   int c = 0;
+  // 64 columns per wait: two loads in flight, one latency
+  for (; c + 64 <= ncols; c += 64) {
+    uint32_t t0[32], t1[32];
+    tmem_ld32(taddr + c, t0);
+    tmem_ld32(taddr + c + 32, t1);
+    tmem_wait_ld();
+    reg_fence32(t0);
+    reg_fence32(t1);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const uint32_t* t = hh ? t1 : t0;
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w[i] = pack2<T>(__uint_as_float(t[2 * i]) * mul, __uint_as_float(t[2 * i + 1]) * mul);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(row + c + 32 * hh);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+      }
+    }
+  }
   for (; c + 32 <= ncols; c += 32) {
     uint32_t t[32];
     tmem_ld32(taddr + c, t);
