@@ -649,6 +649,492 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ============================================================================
+// dK / dV, persistent (D <= 64, no dropout, no cluster split): short sequences
+// ============================================================================
+// At short lengths a dK/dV CTA does 1-8 steps, and a clock64 trace put most
+// of its time in set-up, the first loads, the epilogue and the launch of the
+// next CTA.  This variant keeps one CTA per SM for the whole launch and walks
+// the same (key tile, key/value head) items, most work first, round-robin
+// over the CTAs.  Barriers and tensor memory are set up once; K | V are
+// double-buffered in shared memory and dV | dK in tensor memory (all 512
+// columns: S^T, dP^T, two accumulator pairs), so the producer loads item
+// i+1's tiles while item i computes, and item i's epilogue (staged in its own
+// shared memory) overlaps item i+1's products.  Every ring phase runs on a
+// global step count; per-item barriers on the item count.  The per-step work
+// is the non-persistent kernel's (no dropout).
+struct DkdvPCfg : BwdShape<64> {
+  using S = BwdShape<64>;
+  static constexpr int NQ = 3, ND = 2;
+  static constexpr int DSLOT = S::TILE + 1024;
+  static constexpr int OFF_KV = 0;                           // 2 x (K | V)
+  static constexpr int OFF_Q = 4 * S::TILE;
+  static constexpr int OFF_DO = OFF_Q + NQ * S::TILE;
+  static constexpr int OFF_STG = OFF_DO + ND * DSLOT;        // epilogue staging: dV | dK
+  static constexpr int OFF_BAR = OFF_STG + 2 * S::TILE;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;
+  static constexpr uint32_t COL_ST = 0, COL_DPT = 128, COL_ACC = 256;   // acc pair b: 256 + 128 b
+};
+
+template <typename T>
+__global__ void __launch_bounds__(320, 1)
+    bwd_dkdv_persist_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                            const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
+                            const BwdTcArgs a) {
+  using C = DkdvPCfg;
+  constexpr int D = 64;
+  static_assert(C::SMEM <= 232448, "shared memory per block");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sD = smem + C::OFF_DO;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  Ctl* ctl = reinterpret_cast<Ctl*>(bars + 56);
+  const uint32_t b_kvfull0 = smem_u32(&bars[0]);       // + 8 * buffer (2)
+  const uint32_t b_kvempty0 = smem_u32(&bars[2]);      // + 8 * buffer (2)
+  const uint32_t b_qfull0 = smem_u32(&bars[4]);        // + 8 * Q slot (3)
+  const uint32_t b_qempty0 = smem_u32(&bars[7]);       // + 8 * Q slot (3)
+  const uint32_t b_dfull0 = smem_u32(&bars[10]);       // + 8 * dO slot (2)
+  const uint32_t b_dempty0 = smem_u32(&bars[12]);      // + 8 * dO slot (2)
+  const uint32_t b_sfull = smem_u32(&bars[14]);
+  const uint32_t b_dpfull = smem_u32(&bars[15]);
+  const uint32_t b_pready0 = smem_u32(&bars[16]);      // + 8 * half
+  const uint32_t b_dsready0 = smem_u32(&bars[18]);     // + 8 * half
+  const uint32_t b_accdone0 = smem_u32(&bars[20]);     // + 8 * accumulator pair (2)
+  const uint32_t b_accfree0 = smem_u32(&bars[22]);     // + 8 * accumulator pair (2)
+  const uint32_t b_mmadone = smem_u32(&bars[24]);
+  static_assert(25 * 8 <= 56 * 8, "barriers below the control block");
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nitems = a.BH * a.ntiles;
+  // One item: key tile kt of key/value head bhk (b * Hkv + head); low tiles
+  // (most work under causal masking) first.
+  struct Item {
+    int64_t kt, bhk, bseq; int32_t hk, bb; SeqView sv; int64_t Nq, Nk; int i0, per, n;
+  };
+  // Round r of the walk: items r*P .. r*P + P - 1 (P CTAs), taken in snake
+  // order (CTA c takes the c-th in even rounds, the c-th from the end in odd
+  // ones), which pairs long and short items under causal masking.
+  auto item_id = [&](int64_t r) {
+    const int64_t P = gridDim.x;
+    return r * P + ((r & 1) ? P - 1 - blockIdx.x : blockIdx.x);
+  };
+  auto item_at = [&](int64_t id) {   // id < 2^31 (checked at launch): 32-bit divisions
+    Item it{};
+    const uint32_t u = static_cast<uint32_t>(id), bh = static_cast<uint32_t>(a.BH),
+                   hkv = static_cast<uint32_t>(a.g.Hkv);
+    const uint32_t kt = u / bh, bhk = u - kt * bh, bseq = bhk / hkv;
+    it.bhk = bhk; it.kt = kt; it.bseq = bseq;
+    it.hk = static_cast<int32_t>(bhk - bseq * hkv);
+    it.sv = seq_view(a.g, it.bseq);
+    it.bb = static_cast<int32_t>(it.sv.b);
+    it.Nq = it.sv.nq; it.Nk = it.sv.nk;
+    const int nq = static_cast<int>((it.Nq + C::BT - 1) / C::BT);
+    it.i0 = a.causal ? static_cast<int>(it.kt) : 0;
+    it.per = nq > it.i0 ? nq - it.i0 : 0;
+    it.n = (it.sv.ok && it.kt * C::BT < it.Nk) ? it.per * static_cast<int>(a.g.G) : 0;
+    return it;
+  };
+
+  if (warp == 8) {
+    if (lane == 0) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(b_kvfull0 + 8 * b, 1);
+        mbar_init(b_kvempty0 + 8 * b, 1);
+        mbar_init(b_accdone0 + 8 * b, 1);
+        mbar_init(b_accfree0 + 8 * b, 256);
+      }
+      for (int s = 0; s < C::NQ; ++s) {
+        mbar_init(b_qfull0 + 8 * s, 1);
+        mbar_init(b_qempty0 + 8 * s, 1);
+      }
+      for (int s = 0; s < C::ND; ++s) {
+        mbar_init(b_dfull0 + 8 * s, 32);
+        mbar_init(b_dempty0 + 8 * s, 1);
+      }
+      mbar_init(b_sfull, 1);
+      mbar_init(b_dpfull, 1);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(b_pready0 + 8 * h, 128);
+        mbar_init(b_dsready0 + 8 * h, 128);
+      }
+      mbar_init(b_mmadone, 1);
+      ctl->abort = 0;
+      mbar_fence_init();
+      tma_prefetch_desc(&tmq); tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv); tma_prefetch_desc(&tmdo);
+    }
+    __syncwarp();
+    tmem_alloc(smem_u32(&ctl->tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    // Per item: K, V into buffer (item count) & 1 once the item two back has
+    // released it; then per step Q and dO (+ negated L * log2(e) and Delta,
+    // staged by all 32 lanes) into their rings, slots and rounds counted
+    // over every step this CTA has run.
+    uint32_t kv_round[2] = {0u, 0u}, q_round[C::NQ], d_round[C::ND];
+#pragma unroll
+    for (int s = 0; s < C::NQ; ++s) q_round[s] = 0;
+#pragma unroll
+    for (int s = 0; s < C::ND; ++s) d_round[s] = 0;
+    uint32_t gstep = 0;   // steps of this CTA so far (< 2^31)
+    int li = 0;
+    bool ok = true;
+    for (int64_t r = 0; ok && r * gridDim.x < nitems; ++r) {
+      const int64_t id = item_id(r);
+      if (id >= nitems) continue;
+      const Item itm = item_at(id);
+      if (itm.n == 0) continue;
+      const int buf = li & 1;
+      if (lane == 0) {
+        if (li >= 2 && !wait_bounded(b_kvempty0 + 8 * buf, ((li >> 1) - 1) & 1, ctl, a.status,
+                                     a.timeout_ns))
+          ok = false;
+        if (ok) {
+          uint8_t* kv = smem + C::OFF_KV + buf * 2 * C::TILE;
+          mbar_arrive_expect_tx(b_kvfull0 + 8 * buf, 2 * C::TILE);
+          tma_load_4d(smem_u32(kv), &tmk, b_kvfull0 + 8 * buf, 0,
+                      static_cast<int32_t>(itm.sv.k0 + itm.kt * C::BT), itm.hk, itm.bb);
+          tma_load_4d(smem_u32(kv + C::TILE), &tmv, b_kvfull0 + 8 * buf, 0,
+                      static_cast<int32_t>(itm.sv.k0 + itm.kt * C::BT), itm.hk, itm.bb);
+          kv_round[buf] = static_cast<uint32_t>(li >> 1) + 1;
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      for (int it = 0; ok && it < itm.n; ++it) {
+        const uint32_t g = gstep + static_cast<uint32_t>(it);
+        const int64_t q0 = static_cast<int64_t>(itm.i0 + it % itm.per) * C::BT;
+        const int32_t hq = static_cast<int32_t>(itm.hk * a.g.G + it / itm.per);
+        const int qs = static_cast<int>(g % C::NQ);
+        const uint32_t qr = static_cast<uint32_t>(g / C::NQ);
+        if (lane == 0) {
+          if (qr > 0 && !wait_bounded(b_qempty0 + 8 * qs, (qr - 1) & 1, ctl, a.status, a.timeout_ns))
+            ok = false;
+          if (ok) {
+            mbar_arrive_expect_tx(b_qfull0 + 8 * qs, C::TILE);
+            tma_load_4d(smem_u32(sQ + qs * C::TILE), &tmq, b_qfull0 + 8 * qs, 0,
+                        static_cast<int32_t>(itm.sv.q0 + q0), hq, itm.bb);
+            q_round[qs] = qr + 1;
+          }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        float lv[4], dv[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int64_t q = q0 + lane * 4 + t;
+          const int64_t li2 = lse_index(a.g, itm.sv, hq, q);
+          lv[t] = q < itm.Nq ? -a.lse[li2] * kLog2e : -INFINITY;   // staged negated
+          dv[t] = q < itm.Nq ? -a.delta[li2] : 0.f;
+        }
+        const int ds = static_cast<int>(g % C::ND);
+        const uint32_t dr = static_cast<uint32_t>(g / C::ND);
+        if (dr > 0 && !(ok = wait_warp(b_dempty0 + 8 * ds, (dr - 1) & 1, ctl, a.status, a.timeout_ns)))
+          break;
+        uint8_t* slot = sD + ds * C::DSLOT;
+        float* L2s = reinterpret_cast<float*>(slot + C::TILE);
+        float* Ds = L2s + 128;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          L2s[lane * 4 + t] = lv[t];
+          Ds[lane * 4 + t] = dv[t];
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(b_dfull0 + 8 * ds, C::TILE);
+          tma_load_4d(smem_u32(slot), &tmdo, b_dfull0 + 8 * ds, 0,
+                      static_cast<int32_t>(itm.sv.q0 + q0), hq, itm.bb);
+        } else {
+          mbar_arrive(b_dfull0 + 8 * ds);
+        }
+        d_round[ds] = dr + 1;
+      }
+      gstep += static_cast<uint32_t>(itm.n);
+      ++li;
+    }
+    // Drain: every copy issued has landed.
+    if (lane == 0) {
+      for (int b = 0; b < 2; ++b)
+        if (kv_round[b]) wait_bounded(b_kvfull0 + 8 * b, (kv_round[b] - 1) & 1, ctl, a.status,
+                                      a.timeout_ns, false);
+      for (int s = 0; s < C::NQ; ++s)
+        if (q_round[s]) wait_bounded(b_qfull0 + 8 * s, (q_round[s] - 1) & 1, ctl, a.status,
+                                     a.timeout_ns, false);
+      for (int s = 0; s < C::ND; ++s)
+        if (d_round[s]) wait_bounded(b_dfull0 + 8 * s, (d_round[s] - 1) & 1, ctl, a.status,
+                                     a.timeout_ns, false);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    // The non-persistent kernel's order per step; per item K | V from buffer
+    // (item count) & 1 and dV | dK into accumulator pair (item count) & 1,
+    // whose first product waits until the epilogue of the item two back has
+    // read that pair.
+    if (lane == 0) {
+      const uint32_t idS = idesc_f16<T>(128, C::BT, false, false);
+      const uint32_t idG = idesc_f16<T>(128, D, false, true);
+      const uint64_t dKV0 = sdesc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);
+      const uint64_t dQk = sdesc_sw128(smem_u32(sQ), 16, 1024);          // K-major views
+      const uint64_t dDk = sdesc_sw128(smem_u32(sD), 16, 1024);
+      const uint64_t dQm = sdesc_sw128(smem_u32(sQ), C::CHUNK, 1024);    // MN-major views
+      const uint64_t dDm = sdesc_sw128(smem_u32(sD), C::CHUNK, 1024);
+      auto issue_ST = [&](int qs, int buf) {   // S^T = K Q^T
+        const uint64_t q = dQk + static_cast<uint64_t>((qs * C::TILE) >> 4);
+        const uint64_t kd = dKV0 + static_cast<uint64_t>((buf * 2 * C::TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::COL_ST, kd + off, q + off, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(b_sfull);
+      };
+      auto issue_DPT = [&](int ds, int buf) {  // dP^T = V dO^T
+        const uint64_t gd = dDk + static_cast<uint64_t>((ds * C::DSLOT) >> 4);
+        const uint64_t vd = dKV0 + static_cast<uint64_t>((buf * 2 * C::TILE + C::TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::COL_DPT, vd + off, gd + off, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(b_dpfull);
+      };
+      uint32_t gstep = 0;   // steps of this CTA so far (< 2^31)
+      int li = 0;
+      bool ok = true;
+      for (int64_t r = 0; ok && r * gridDim.x < nitems; ++r) {
+        const int64_t id = item_id(r);
+        if (id >= nitems) continue;
+        const Item itm = item_at(id);
+        if (itm.n == 0) continue;
+        const int buf = li & 1;
+        const uint32_t accv = tmem + C::COL_ACC + 128 * buf, acck = accv + 64;
+        ok = wait_bounded(b_kvfull0 + 8 * buf, (li >> 1) & 1, ctl, a.status, a.timeout_ns) &&
+             wait_bounded(b_qfull0 + 8 * static_cast<int>(gstep % C::NQ),
+                          static_cast<uint32_t>(gstep / C::NQ) & 1, ctl, a.status, a.timeout_ns) &&
+             wait_bounded(b_dfull0 + 8 * static_cast<int>(gstep % C::ND),
+                          static_cast<uint32_t>(gstep / C::ND) & 1, ctl, a.status, a.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+        issue_ST(static_cast<int>(gstep % C::NQ), buf);
+        issue_DPT(static_cast<int>(gstep % C::ND), buf);
+        if (li >= 2 && !(ok = wait_bounded(b_accfree0 + 8 * buf, ((li >> 1) - 1) & 1, ctl, a.status,
+                                           a.timeout_ns)))
+          break;
+        for (int it = 0; ok && it < itm.n; ++it) {
+          const uint32_t g = gstep + static_cast<uint32_t>(it);
+          const int qs = static_cast<int>(g % C::NQ), ds = static_cast<int>(g % C::ND);
+          const bool next = it + 1 < itm.n;
+          const int qs1 = static_cast<int>((g + 1) % C::NQ), ds1 = static_cast<int>((g + 1) % C::ND);
+          const uint32_t par = g & 1u;
+          // dV += P^T dO (B: this step's dO read MN-major, N = d)
+          const uint64_t mdo = dDm + static_cast<uint64_t>((ds * C::DSLOT) >> 4);
+          for (int h = 0; ok && h < 2; ++h) {
+            if (!(ok = wait_bounded(b_pready0 + 8 * h, par, ctl, a.status, a.timeout_ns))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(accv, tmem + C::COL_ST + 64 * h + 8 * kk,
+                     mdo + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
+                     (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          if (next) {
+            if (!(ok = wait_bounded(b_qfull0 + 8 * qs1, static_cast<uint32_t>((g + 1) / C::NQ) & 1,
+                                    ctl, a.status, a.timeout_ns)))
+              break;
+            tc_fence_after();
+            issue_ST(qs1, buf);
+          }
+          // dK += dS^T Q (B: this step's Q read MN-major)
+          const uint64_t mq = dQm + static_cast<uint64_t>((qs * C::TILE) >> 4);
+          for (int h = 0; ok && h < 2; ++h) {
+            if (!(ok = wait_bounded(b_dsready0 + 8 * h, par, ctl, a.status, a.timeout_ns))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(acck, tmem + C::COL_DPT + 64 * h + 8 * kk,
+                     mq + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
+                     (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!ok) break;
+          mma_commit(b_qempty0 + 8 * qs);
+          mma_commit(b_dempty0 + 8 * ds);
+          if (next) {
+            if (!(ok = wait_bounded(b_dfull0 + 8 * ds1, static_cast<uint32_t>((g + 1) / C::ND) & 1,
+                                    ctl, a.status, a.timeout_ns)))
+              break;
+            tc_fence_after();
+            issue_DPT(ds1, buf);
+          }
+        }
+        if (!ok) break;
+        mma_commit(b_kvempty0 + 8 * buf);
+        mma_commit(b_accdone0 + 8 * buf);
+        gstep += static_cast<uint32_t>(itm.n);
+        ++li;
+      }
+      mma_commit(b_mmadone);
+      wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ elementwise + epilogue
+    const int hf = warp >> 2, quarter = warp & 3;
+    const int row = quarter * 32 + lane;                 // key within the tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c = a.c;
+    const uint32_t stg = smem_u32(smem + C::OFF_STG) + static_cast<uint32_t>(hf * C::TILE);
+    uint32_t gstep = 0;   // steps of this CTA so far (< 2^31)
+    int li = 0;
+    bool ok = true;
+    // Epilogue of item `e` (item count `eli`): its accumulator pair, staged in
+    // the CTA's own staging tiles (dV | dK) and stored with consecutive
+    // threads on consecutive 16 bytes of a row; the pair is released to the
+    // MMA thread once read.  Every thread of the warpgroup passes the
+    // barrier, also after a timeout.
+    T* pend_row0 = nullptr;   // the pending item's first output row (dV or dK of this warpgroup)
+    int pend_rows = 0, pend_li = -1;
+    auto epilogue = [&](T* row0, int nrows, int eli) {
+      const int buf = eli & 1;
+      if (ok)
+        ok = wait_warp(b_accdone0 + 8 * buf, static_cast<uint32_t>(eli >> 1) & 1, ctl, a.status,
+                       a.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        stage_row_sw128<T>(lane_base + C::COL_ACC + 128 * buf + 64 * hf, hf == 0 ? 1.f : a.scale,
+                           stg, row, 0, D);
+      }
+      tc_fence_before();
+      mbar_arrive(b_accfree0 + 8 * buf);
+      if (bar_red_and(1 + hf, 128, ok))
+        store_staged_tile<T>(stg, D, threadIdx.x & 127, 128, row0, (hf == 0 ? a.s0 : a.s1)[2], nrows,
+                             a.dreal);
+    };
+    // After a wait ran out (ok false) the warp still walks every item and
+    // passes each epilogue barrier, doing nothing else, so that the other
+    // warps of its warpgroup never wait on it at a barrier.
+    for (int64_t r = 0; r * gridDim.x < nitems; ++r) {
+      const int64_t id = item_id(r);
+      if (id >= nitems) continue;
+      const Item itm = item_at(id);
+      if (!itm.sv.ok) {
+        if (threadIdx.x == 0 && itm.kt == 0) record_status(a.status, FA_ERR_SEQLENS);
+        continue;
+      }
+      if (itm.kt * C::BT >= itm.Nk) continue;           // this key tile lies past the sequence
+      if (itm.n == 0) {
+        // no query attends to these keys: dK = dV = 0
+        const int64_t* st = hf == 0 ? a.s0 : a.s1;
+        T* row0 = static_cast<T*>(hf == 0 ? a.out0 : a.out1) + itm.bb * st[0] + itm.hk * st[1] +
+                  (itm.sv.k0 + itm.kt * C::BT) * st[2];
+        if (row < itm.Nk - itm.kt * C::BT)
+          for (int d = 0; d < a.dreal; ++d) row0[row * st[2] + d] = Elem<T>::from_f32(0.f);
+        continue;
+      }
+      for (int it = 0; ok && it < itm.n; ++it) {
+        const uint32_t g = gstep + static_cast<uint32_t>(it);
+        const int i = itm.i0 + it % itm.per, ds = static_cast<int>(g % C::ND);
+        const uint32_t par = g & 1u;
+        if (!(ok = wait_warp(b_sfull, par, ctl, a.status, a.timeout_ns))) break;
+        // the dO slot's arrival also publishes the staged L and Delta
+        if (!(ok = wait_warp(b_dfull0 + 8 * ds, static_cast<uint32_t>(g / C::ND) & 1, ctl, a.status,
+                             a.timeout_ns)))
+          break;
+        tc_fence_after();
+        // -L * log2(e) and -Delta of this half's 64 queries
+        const float* nL2s = reinterpret_cast<const float*>(sD + ds * C::DSLOT + C::TILE) + 64 * hf;
+        const float* nDs = nL2s + 128;
+        float p[64];
+        tmem_ld64(lane_base + C::COL_ST + 64 * hf, p);
+        {
+          // P = exp2(c * S - L * log2(e)), two queries per paired instruction
+          const uint64_t cc = f32x2(c, c);
+#pragma unroll
+          for (int q = 0; q < 64; q += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(nL2s + q);
+            float x0, x1, x2, x3;
+            f32x2_split(fma_f32x2(f32x2(p[q], p[q + 1]), cc, f32x2(l4.x, l4.y)), x0, x1);
+            f32x2_split(fma_f32x2(f32x2(p[q + 2], p[q + 3]), cc, f32x2(l4.z, l4.w)), x2, x3);
+            p[q] = ex2(x0);
+            p[q + 1] = ex2(x1);
+            p[q + 2] = ex2(x2);
+            p[q + 3] = ex2(x3);
+          }
+        }
+        if (a.causal && i == itm.kt) {
+          // diagonal tile: query (64*hf + q) attends to this key only if it is not earlier
+#pragma unroll
+          for (int q = 0; q < 64; ++q)
+            if (64 * hf + q < row) p[q] = 0.f;
+        }
+        tmem_st_packed64<T>(lane_base + C::COL_ST + 64 * hf, p);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(b_pready0 + 8 * hf);
+
+        if (!(ok = wait_warp(b_dpfull, par, ctl, a.status, a.timeout_ns))) break;
+        tc_fence_after();
+        // dS = P o (dP - Delta), two queries per paired instruction, in two
+        // halves of 32 columns (only 32 of dP held next to P): half 0's
+        // rounded dS lands on columns whose dP was read first, half 1's on
+        // half 0's
+        const uint32_t tdp = lane_base + C::COL_DPT + 64 * hf;
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+          uint32_t r[32];
+          tmem_ld32(tdp + 32 * hq, r);
+          tmem_wait_ld();
+          reg_fence32(r);
+          uint32_t w[16];
+#pragma unroll
+          for (int j2 = 0; j2 < 32; j2 += 2) {
+            const int q = 32 * hq + j2;
+            const float2 d2 = *reinterpret_cast<const float2*>(nDs + q);
+            float x0, x1;
+            f32x2_split(mul_f32x2(add_f32x2(f32x2(__uint_as_float(r[j2]), __uint_as_float(r[j2 + 1])),
+                                            f32x2(d2.x, d2.y)),
+                                  f32x2(p[q], p[q + 1])),
+                        x0, x1);
+            w[j2 / 2] = pack2<T>(x0, x1);
+          }
+          tmem_st16(tdp + 16 * hq, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(b_dsready0 + 8 * hf);
+      }
+      // The previous item's epilogue, deferred to here so that its products
+      // have long completed and this item's steps ran without waiting for it.
+      if (pend_li >= 0) epilogue(pend_row0, pend_rows, pend_li);
+      {
+        const int64_t* st = hf == 0 ? a.s0 : a.s1;
+        pend_row0 = static_cast<T*>(hf == 0 ? a.out0 : a.out1) + itm.bb * st[0] + itm.hk * st[1] +
+                    (itm.sv.k0 + itm.kt * C::BT) * st[2];
+        pend_rows = static_cast<int>(itm.Nk - itm.kt * C::BT < C::BT ? itm.Nk - itm.kt * C::BT : C::BT);
+      }
+      pend_li = li;
+      gstep += static_cast<uint32_t>(itm.n);
+      ++li;
+    }
+    if (pend_li >= 0) epilogue(pend_row0, pend_rows, pend_li);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================================
 // dQ
 // ============================================================================
 // Q_i and dO_i are only A operands (of S = Q K^T and dP = dO V^T), so they are
@@ -1033,6 +1519,10 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
+// Longest sequence (query and key rows) for which the D <= 64 backward runs
+// the persistent dK/dV kernel.
+constexpr int64_t kPersistMaxN = 1024;
+
 template <typename T, int D, int DROP>
 fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
   const Geo& g = p.g;
@@ -1067,12 +1557,32 @@ fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
   if (blocks1 > 0x7fffffffLL) return FA_ERR_SHAPE;
   a.out0 = p.dv; a.out1 = p.dk;
   for (int i = 0; i < 4; ++i) { a.s0[i] = p.sdv[i]; a.s1[i] = p.sdk[i]; }
-
+  // Short sequences (a few steps per key tile) at D <= 64 without dropout:
+  // the persistent kernel, one CTA per SM walking the key tiles, hides each
+  // tile's set-up, first loads and epilogue behind its neighbours'.
+  bool persist = false;
+  if constexpr (D == 64 && DROP == kDropNone)
+    persist = split == 1 && g.Nq <= kPersistMaxN && g.Nk <= kPersistMaxN;
   auto k1 = bwd_dkdv_tc_kernel<T, D, DROP>;
-  if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM) != cudaSuccess)
-    return FA_ERR_LAUNCH;
-  prof_record(p, 0, stream);
-  if (split == 1) {
+  if (persist) {
+    auto kp = bwd_dkdv_persist_kernel<T>;
+    if (cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvPCfg::SMEM) !=
+        cudaSuccess)
+      return FA_ERR_LAUNCH;
+    const int64_t sms = device_sm_count();
+    const int64_t grid = base1 < sms ? base1 : sms;
+    prof_record(p, 0, stream);
+    kp<<<dim3(static_cast<unsigned>(grid)), dim3(DkdvCfg<D>::THREADS), DkdvPCfg::SMEM, stream>>>(
+        mq, mk, mv, mdo, a);
+  } else {
+    if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM) !=
+        cudaSuccess)
+      return FA_ERR_LAUNCH;
+    prof_record(p, 0, stream);
+  }
+  if (persist) {
+    // launched above
+  } else if (split == 1) {
     k1<<<dim3(static_cast<unsigned>(blocks1)), dim3(DkdvCfg<D>::THREADS), DkdvCfg<D>::SMEM,
          stream>>>(mq, mk, mv, mdo, a);
   } else {
