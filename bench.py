@@ -56,14 +56,14 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 1043.5 MB per launch measured on 16 heads,
+    # bwd_dkdv_tc_kernel<bf16,128>: 1059.1 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("dkdv", "cceba2cb0f83c8bf0caeb6d6260e510482fe8a208d01b7a4097f485c3c3df0a9",
-     "long-bf16-B1-H32-N16384-D128-causal"): 2087.0e6,
-    # bwd_fused_tc_kernel<bf16,128>: 2927.0 MB per launch measured on 16 heads,
+    ("dkdv", "2603f5ecd4f321ede3d40be96316f6609c1a2b27ee50cb4f2dd425b9f5b2613a",
+     "long-bf16-B1-H32-N16384-D128-causal"): 2118.1e6,
+    # bwd_fused_tc_kernel<bf16,128>: 2929.2 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("fused", "4e901d50139ef9df1f0a88bcfd2e6a96d1aa4d40c654be868c696ba22ad5f3bb",
-     "long-bf16-B1-H32-N16384-D128-causal"): 5854.0e6,
+    ("fused", "7a40ac2fd235fad28a6a7f44662e8e368ab7a4b4121be356c5b381d64da86cd1",
+     "long-bf16-B1-H32-N16384-D128-causal"): 5858.5e6,
 }
 
 
