@@ -1177,6 +1177,12 @@ __global__ void __launch_bounds__(320, 1)
                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo,
                      const BwdTcArgs a) {
   using C = DqCfg<D>;
+  // At D <= 64, Q and dO stay in shared memory (their stage is not reused)
+  // and S, dP read them from there: no per-CTA copy into TMEM before the
+  // first product, which short sequences cannot hide; NST - 1 stages still
+  // hold K | V.  At D = 128 the stage is needed for K | V (three stages).
+  constexpr bool QS = D == 64;
+  constexpr int NR = QS ? C::NST - 1 : C::NST;   // K | V ring stages
   static_assert(C::SMEM <= 232448, "shared memory per block");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1283,11 +1289,11 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
       for (int s = 0; s < C::NST; ++s) last_round[s] = s < jt_early ? 1u : 0u;
       for (int jt = jt_early; jt < n; ++jt) {
-        const int st = jt % C::NST;
-        const uint32_t r = static_cast<uint32_t>(jt / C::NST);
+        const int st = jt % NR;
+        const uint32_t r = static_cast<uint32_t>(jt / NR);
         if (r > 0) {
           if (!wait_bounded(b_kvempty0 + 8 * st, (r - 1) & 1, ctl, a.status, a.timeout_ns)) break;
-        } else if (st == C::QSLOT) {
+        } else if (!QS && st == C::QSLOT) {
           // this stage still holds Q | dO until they have been copied into TMEM
           if (!wait_bounded(b_qt, 0, ctl, a.status, a.timeout_ns)) break;
         }
@@ -1310,23 +1316,31 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t idG = idesc_f16<T>(128, D, false, true);
       const uint64_t dSt0 = sdesc_sw128(smem_u32(sStage), 16, 1024);
       const uint64_t dSt0mn = sdesc_sw128(smem_u32(sStage), C::CHUNK, 1024);
-      auto issue_S = [&](int st) {   // S = Q K^T, Q from TMEM
+      const uint64_t dQa = sdesc_sw128(smem_u32(sQ), 16, 1024);     // K-major A views (QS)
+      const uint64_t dDa = sdesc_sw128(smem_u32(sDO), 16, 1024);
+      auto issue_S = [&](int st) {   // S = Q K^T, Q from TMEM (or shared memory, QS)
         const uint64_t kb = dSt0 + static_cast<uint64_t>((st * C::STAGE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          mma_ts(tmem + C::COL_S, tmem + C::COL_Q + 8 * kk, kb + off, idS, kk > 0 ? 1u : 0u);
+          if constexpr (QS)
+            mma_ss(tmem + C::COL_S, dQa + off, kb + off, idS, kk > 0 ? 1u : 0u);
+          else
+            mma_ts(tmem + C::COL_S, tmem + C::COL_Q + 8 * kk, kb + off, idS, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_dP = [&](int st) {  // dP = dO V^T, dO from TMEM
+      auto issue_dP = [&](int st) {  // dP = dO V^T, dO from TMEM (or shared memory, QS)
         const uint64_t vb = dSt0 + static_cast<uint64_t>((st * C::STAGE + C::TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          mma_ts(tmem + C::COL_DP, tmem + C::COL_DO + 8 * kk, vb + off, idS, kk > 0 ? 1u : 0u);
+          if constexpr (QS)
+            mma_ss(tmem + C::COL_DP, dDa + off, vb + off, idS, kk > 0 ? 1u : 0u);
+          else
+            mma_ts(tmem + C::COL_DP, tmem + C::COL_DO + 8 * kk, vb + off, idS, kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = wait_bounded(b_qt, 0, ctl, a.status, a.timeout_ns) &&
+      bool ok = wait_bounded(QS ? b_q : b_qt, 0, ctl, a.status, a.timeout_ns) &&
                 wait_bounded(b_kvfull0, 0, ctl, a.status, a.timeout_ns);
       if (ok) {
         tc_fence_after();
@@ -1336,11 +1350,11 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(b_dpfull);
       }
       for (int jt = 0; ok && jt < n; ++jt) {
-        const int st = jt % C::NST;
+        const int st = jt % NR;
         const bool next = jt + 1 < n;
-        const int stn = (jt + 1) % C::NST;
+        const int stn = (jt + 1) % NR;
         if (next) {
-          if (!(ok = wait_bounded(b_kvfull0 + 8 * stn, ((jt + 1) / C::NST) & 1, ctl, a.status,
+          if (!(ok = wait_bounded(b_kvfull0 + 8 * stn, ((jt + 1) / NR) & 1, ctl, a.status,
                                   a.timeout_ns)))
             break;
           if (!(ok = wait_bounded(b_sfree, jt & 1, ctl, a.status, a.timeout_ns))) break;
@@ -1380,14 +1394,18 @@ __global__ void __launch_bounds__(320, 1)
     const int64_t li = lse_index(a.g, sv, h, qrow);
     const float l2 = qrow < Nq ? a.lse[li] * kLog2e : INFINITY;
     const float dl = qrow < Nq ? a.delta[li] : 0.f;
-    // Q (warps 0-3) and dO (warps 4-7) into TMEM as A operands.
-    bool ok = wait_warp(b_q, 0, ctl, a.status, a.timeout_ns);
-    if (ok) {
-      tile_row_to_tmem<D>(hf == 0 ? sQ : sDO, row, lane_base + (hf == 0 ? C::COL_Q : C::COL_DO));
-      tmem_wait_st();
+    // Q (warps 0-3) and dO (warps 4-7) into TMEM as A operands (not in QS
+    // mode, where the products read them from shared memory).
+    bool ok = true;
+    if constexpr (!QS) {
+      ok = wait_warp(b_q, 0, ctl, a.status, a.timeout_ns);
+      if (ok) {
+        tile_row_to_tmem<D>(hf == 0 ? sQ : sDO, row, lane_base + (hf == 0 ? C::COL_Q : C::COL_DO));
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(b_qt);
     }
-    tc_fence_before();
-    mbar_arrive(b_qt);
     // Dropout keep bits of this row's 64 keys of a key tile: bit q set iff
     // key 64*hf + q of the tile is kept.  In the keep mask they are bytes
     // 8*hf .. 8*hf + 7 of the row's entry for the tile, loaded a tile ahead
