@@ -37,6 +37,7 @@ import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -115,17 +116,33 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region.
+
+    nvidia-smi's start-up (NVML initialisation) stalls the GPU for tens of
+    milliseconds, so __enter__ returns only once the first sample has been
+    printed: the stall then lies before the timed region, not inside it.  A
+    reader thread drains the pipe so that a long region cannot fill it."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    START_TIMEOUT_S = 10.0
+    SETTLE_S = 0.2
 
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
+        self.lines = []
+
+    def _read(self, first):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self.lines.append(ln)
+                first.set()
+        first.set()
 
     def __enter__(self):
+        self.lines = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
@@ -133,18 +150,24 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        first = threading.Event()
+        self.reader = threading.Thread(target=self._read, args=(first,), daemon=True)
+        self.reader.start()
+        first.wait(self.START_TIMEOUT_S)
+        time.sleep(self.SETTLE_S)
+        self.lines.clear()          # samples from before the region
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+                self.proc.wait()
+            self.reader.join(timeout=5)
         return False
 
     def summary(self):
