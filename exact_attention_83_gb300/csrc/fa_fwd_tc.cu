@@ -61,7 +61,9 @@ struct FwdCfg {
   static constexpr int DC = D / 64;               // 128-byte column chunks per row
   static constexpr int CHUNK = BM * 128;          // bytes of one 128-row chunk
   static constexpr int TILE = DC * CHUNK;         // bytes of one 128 x D tile
-  static constexpr int NS = D == 128 ? 4 : 8;     // K/V ring slots
+  static constexpr int NS = D == 128 ? 4 : 8;     // K/V ring tiles
+  static constexpr int NP = NS / 2;               // ring slots of a V tile + a K tile
+  static constexpr int PAIR = 2 * TILE;
   static constexpr int OFF_RING = 2 * TILE;
   static constexpr int OFF_BAR = OFF_RING + NS * TILE;
   static constexpr int SMEM = OFF_BAR + 1024 + 1024;   // + barriers, + alignment slack
@@ -148,26 +150,39 @@ __global__ void __launch_bounds__(320, 1)
     return;
   }
 
-  // K | V ring units: unit u = 2j + kv (K_j, V_j) in slot u % NS.  The
+  // K | V ring units in consumption order, one per step: unit 0 = K_0 (the
+  // first score products), unit u >= 1 = V_{u-1} and K_u (step u - 1's P V
+  // and next score products; no K_u at u = nmax), in slot u % NP with V in
+  // the slot's first tile and K in its second.  The MMA thread stays only a
+  // product or two ahead of the tensor pipe, so each wait or commit it makes
+  // between products can leave the pipe idle: with one unit per step it
+  // waits once and commits once per step for the ring.  The
   // producer's lane 0 sets up the barriers and sends Q and the ring's first
   // round of units before the block-wide sync, so their latency overlaps the
   // set-up.
-  uint32_t issued[C::NS];   // producer lane 0: rounds issued per ring slot
+  uint32_t issued[C::NP];   // producer lane 0: rounds issued per ring slot
 #pragma unroll
-  for (int s = 0; s < C::NS; ++s) issued[s] = 0;
+  for (int s = 0; s < C::NP; ++s) issued[s] = 0;
   auto issue_unit = [&](int u) {
-    const int j = u >> 1, kv = u & 1, s = u % C::NS;
-    mbar_arrive_expect_tx(b_full0 + 8 * s, C::TILE);
-    for (int c = 0; c < C::DC; ++c)
-      tma_load_4d(smem_u32(sRing + s * C::TILE + c * C::CHUNK), kv ? &tmv : &tmk,
-                  b_full0 + 8 * s, c * 64, static_cast<int32_t>(sv.k0 + j * C::BN), hk, bb);
-    issued[s] = static_cast<uint32_t>(u / C::NS) + 1;
+    const int s = u % C::NP;
+    const bool hasV = u > 0, hasK = u < nmax;
+    mbar_arrive_expect_tx(b_full0 + 8 * s, (hasV ? C::TILE : 0) + (hasK ? C::TILE : 0));
+    for (int c = 0; c < C::DC; ++c) {
+      if (hasV)
+        tma_load_4d(smem_u32(sRing + s * C::PAIR + c * C::CHUNK), &tmv, b_full0 + 8 * s, c * 64,
+                    static_cast<int32_t>(sv.k0 + (u - 1) * C::BN), hk, bb);
+      if (hasK)
+        tma_load_4d(smem_u32(sRing + s * C::PAIR + C::TILE + c * C::CHUNK), &tmk, b_full0 + 8 * s,
+                    c * 64, static_cast<int32_t>(sv.k0 + u * C::BN), hk, bb);
+    }
+    issued[s] = static_cast<uint32_t>(u / C::NP) + 1;
   };
-  const int u_early = 2 * nmax < C::NS ? 2 * nmax : C::NS;   // round 0 of the ring
+  const int nunits = nmax + 1;
+  const int u_early = nunits < C::NP ? nunits : C::NP;   // round 0 of the ring
   if (warp == 8) {
     if (lane == 0) {
       mbar_init(b_q, 1);
-      for (int s = 0; s < C::NS; ++s) {
+      for (int s = 0; s < C::NP; ++s) {
         mbar_init(b_full0 + 8 * s, 1);
         mbar_init(b_empty0 + 8 * s, 1);
       }
@@ -206,9 +221,9 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       bool ok = true;
-      for (int u = u_early; ok && u < 2 * nmax; ++u) {
-        const int s = u % C::NS;
-        const uint32_t r = static_cast<uint32_t>(u / C::NS);
+      for (int u = u_early; ok && u < nunits; ++u) {
+        const int s = u % C::NP;
+        const uint32_t r = static_cast<uint32_t>(u / C::NP);
         if (r > 0 && !(ok = wait_bounded(b_empty0 + 8 * s, (r - 1) & 1, ctl, a.status,
                                          a.timeout_ns)))
           break;
@@ -216,7 +231,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       // Drain: every copy issued has landed before the CTA may exit.
       wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns, false);
-      for (int s = 0; s < C::NS; ++s)
+      for (int s = 0; s < C::NP; ++s)
         if (issued[s]) wait_bounded(b_full0 + 8 * s, (issued[s] - 1) & 1, ctl, a.status,
                                     a.timeout_ns, false);
     }
@@ -230,11 +245,11 @@ __global__ void __launch_bounds__(320, 1)
       // to the start-address field (addresses stay below 256 KiB, so the
       // 14-bit field never carries).
       const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dK0 = sdesc_sw128(smem_u32(sRing), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sRing + C::TILE), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sRing), C::CHUNK, 1024);
       auto issue_S = [&](int g, int slot) {
         const uint64_t qa = dQ0 + static_cast<uint64_t>((g * C::TILE) >> 4);
-        const uint64_t kb = dK0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
+        const uint64_t kb = dK0 + static_cast<uint64_t>((slot * C::PAIR) >> 4);
         const uint32_t d = tmem + C::COL_S0 + 128 * g;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -244,7 +259,7 @@ __global__ void __launch_bounds__(320, 1)
       };
       // O_g += P V over keys 64h .. 64h+63 (P columns 32h .. 32h+31)
       auto issue_PV_half = [&](int g, int slot, int hh, bool acc) {
-        const uint64_t vb = dV0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
+        const uint64_t vb = dV0 + static_cast<uint64_t>((slot * C::PAIR) >> 4);
         const uint32_t d = tmem + C::COL_O0 + D * g, p = tmem + C::COL_S0 + 128 * g;
 #pragma unroll
         for (int k4 = 0; k4 < C::BN / 32; ++k4) {
@@ -267,36 +282,29 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(b_empty0);
       }
       for (int j = 0; ok && j < nmax; ++j) {
-        const int uV = 2 * j + 1, sV = uV % C::NS;
-        const int uK = 2 * j + 2, sK = uK % C::NS;
-        const bool next = j + 1 < nmax;
-        ok = wait_bounded(b_full0 + 8 * sV, (uV / C::NS) & 1, ctl, a.status, a.timeout_ns);
-        if (ok && next)
-          ok = wait_bounded(b_full0 + 8 * sK, (uK / C::NS) & 1, ctl, a.status, a.timeout_ns);
+        // unit j + 1: V_j for this step's P V, K_{j+1} for its score products
+        const int u = j + 1, su = u % C::NP;
+        // (the fence after each P-ready wait below orders the products after
+        // this wait too)
+        ok = wait_bounded(b_full0 + 8 * su, (u / C::NP) & 1, ctl, a.status, a.timeout_ns);
         if (!ok) break;
-        tc_fence_after();
         for (int g = 0; g < 2 && ok; ++g) {
           if (j >= ntile[g]) continue;
-          // P V per half of the keys, each as soon as the softmax warps have
-          // written that half of P
-          for (int hh = 0; hh < 2; ++hh) {
-            if (!(ok = wait_bounded(b_pready0 + 8 * (2 * g + hh), j & 1, ctl, a.status,
-                                    a.timeout_ns)))
-              break;
-            tc_fence_after();
-            issue_PV_half(g, sV, hh, j > 0);
-          }
-          if (!ok) break;
+          // P V once the softmax warps have written all of P
+          if (!(ok = wait_bounded(b_pready0 + 8 * (2 * g), j & 1, ctl, a.status, a.timeout_ns)))
+            break;
+          tc_fence_after();
+          issue_PV_half(g, su, 0, j > 0);
+          issue_PV_half(g, su, 1, true);
           if (j + 1 < ntile[g]) {
-            issue_S(g, sK);
+            issue_S(g, su);
             mma_commit(b_sfull0 + 8 * g);
           } else {
             mma_commit(b_ofinal0 + 8 * g);
           }
         }
         if (!ok) break;
-        mma_commit(b_empty0 + 8 * sV);
-        if (next) mma_commit(b_empty0 + 8 * sK);
+        mma_commit(b_empty0 + 8 * su);
       }
       // Drain: every MMA (and every commit arrival) of this thread is complete.
       mma_commit(b_mmadone);
@@ -332,6 +340,9 @@ __global__ void __launch_bounds__(320, 1)
         if (mrow) mrow[j * a.g.rows_q] = make_uint4(kb[0], kb[1], kb[2], kb[3]);
       }
       if (!(ok = wait_warp(b_sfull0 + 8 * g, j & 1, ctl, a.status, a.timeout_ns))) break;
+      // S_j complete: every product reading ring unit j has completed (see the
+      // ring above); release it if the producer still has a unit for its slot
+
       tc_fence_after();
       float s[128];
       {
@@ -430,9 +441,11 @@ __global__ void __launch_bounds__(320, 1)
             tmem_st16(tO + 16 * cc4, t);
           }
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(b_pready0 + 8 * (2 * g + hh));
+        if (hh == 1) {
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(b_pready0 + 8 * (2 * g));
+        }
         float lo, hi;
         f32x2_split(acc, lo, hi);
         l += lo + hi;
