@@ -238,7 +238,12 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop and its waits, so the loop control
+    // and descriptor arithmetic are warp-uniform; one elected lane issues
+    // the products and commits.  (With the loop inside a one-lane branch the
+    // same code issued products more slowly than the tensor pipe ran them.)
+    {
+      const bool leader = elect_one();
       const uint32_t idS = idesc_f16<T>(128, C::BN, false, false);
       const uint32_t idO = idesc_f16<T>(128, D, false, true);
       // Descriptors are built once and advanced by adding (byte offset >> 4)
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          mma_ss(d, qa + off, kb + off, idS, kk > 0 ? 1u : 0u);
+          if (leader) mma_ss(d, qa + off, kb + off, idS, kk > 0 ? 1u : 0u);
         }
       };
       // O_g += P V over keys 64h .. 64h+63 (P columns 32h .. 32h+31)
@@ -264,12 +269,12 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int k4 = 0; k4 < C::BN / 32; ++k4) {
           const int kk = 4 * hh + k4;
-          mma_ts(d, p + kk * 8, vb + static_cast<uint64_t>((kk * 2048) >> 4), idO,
+          if (leader) mma_ts(d, p + kk * 8, vb + static_cast<uint64_t>((kk * 2048) >> 4), idO,
                  (acc || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns) &&
-                wait_bounded(b_full0, 0, ctl, a.status, a.timeout_ns);
+      bool ok = wait_warp(b_q, 0, ctl, a.status, a.timeout_ns) &&
+                wait_warp(b_full0, 0, ctl, a.status, a.timeout_ns);
       if (ok) {
         tc_fence_after();
         for (int g = 0; g < 2; ++g)
@@ -277,37 +282,38 @@ __global__ void __launch_bounds__(320, 1)
             issue_S(g, 0);
             // A test can withhold this arrival in CTA 0 to make the softmax
             // warps' bounded wait run out (the timeout path, without a fault).
-            if (!(a.withhold_arrival && blockIdx.x == 0 && g == 0)) mma_commit(b_sfull0 + 8 * g);
+            if (leader && !(a.withhold_arrival && blockIdx.x == 0 && g == 0))
+              mma_commit(b_sfull0 + 8 * g);
           }
-        mma_commit(b_empty0);
+        if (leader) mma_commit(b_empty0);
       }
       for (int j = 0; ok && j < nmax; ++j) {
         // unit j + 1: V_j for this step's P V, K_{j+1} for its score products
         const int u = j + 1, su = u % C::NP;
         // (the fence after each P-ready wait below orders the products after
         // this wait too)
-        ok = wait_bounded(b_full0 + 8 * su, (u / C::NP) & 1, ctl, a.status, a.timeout_ns);
+        ok = wait_warp(b_full0 + 8 * su, (u / C::NP) & 1, ctl, a.status, a.timeout_ns);
         if (!ok) break;
         for (int g = 0; g < 2 && ok; ++g) {
           if (j >= ntile[g]) continue;
           // P V once the softmax warps have written all of P
-          if (!(ok = wait_bounded(b_pready0 + 8 * (2 * g), j & 1, ctl, a.status, a.timeout_ns)))
+          if (!(ok = wait_warp(b_pready0 + 8 * (2 * g), j & 1, ctl, a.status, a.timeout_ns)))
             break;
           tc_fence_after();
           issue_PV_half(g, su, 0, j > 0);
           issue_PV_half(g, su, 1, true);
           if (j + 1 < ntile[g]) {
             issue_S(g, su);
-            mma_commit(b_sfull0 + 8 * g);
+            if (leader) mma_commit(b_sfull0 + 8 * g);
           } else {
-            mma_commit(b_ofinal0 + 8 * g);
+            if (leader) mma_commit(b_ofinal0 + 8 * g);
           }
         }
         if (!ok) break;
-        mma_commit(b_empty0 + 8 * su);
+        if (leader) mma_commit(b_empty0 + 8 * su);
       }
       // Drain: every MMA (and every commit arrival) of this thread is complete.
-      mma_commit(b_mmadone);
+      if (leader) mma_commit(b_mmadone);
       wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
     }
     __syncwarp();
@@ -636,7 +642,8 @@ __global__ void __launch_bounds__(192, 2)
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
+      const bool leader = elect_one();
       const uint32_t idS = idesc_f16<T>(128, C::BN, false, false);
       const uint32_t idO = idesc_f16<T>(128, D, false, true);
       const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -648,53 +655,53 @@ __global__ void __launch_bounds__(192, 2)
         const uint64_t kb = dK0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::COL_S, dQ0 + ((kk * 32) >> 4), kb + ((kk * 32) >> 4), idS,
+          if (leader) mma_ss(tmem + C::COL_S, dQ0 + ((kk * 32) >> 4), kb + ((kk * 32) >> 4), idS,
                  kk > 0 ? 1u : 0u);
       };
       auto issue_PV = [&](int slot, bool acc) {   // O += P V, P from tensor memory
         const uint64_t vb = dV0 + static_cast<uint64_t>((slot * C::TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ts(tmem + C::COL_O, tmem + C::COL_P + 8 * kk,
+          if (leader) mma_ts(tmem + C::COL_O, tmem + C::COL_P + 8 * kk,
                  vb + static_cast<uint64_t>((kk * 2048) >> 4), idO, (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = wait_bounded(b_q, 0, ctl, a.status, a.timeout_ns) &&
-                wait_bounded(b_full0 + 8 * slot_of(unit_k(0)), parity_of(unit_k(0)), ctl,
+      bool ok = wait_warp(b_q, 0, ctl, a.status, a.timeout_ns) &&
+                wait_warp(b_full0 + 8 * slot_of(unit_k(0)), parity_of(unit_k(0)), ctl,
                              a.status, a.timeout_ns);
       if (ok) {
         tc_fence_after();
         issue_S(slot_of(unit_k(0)));
         // A test can withhold this arrival in CTA 0 to make the softmax warps'
         // bounded wait run out (the timeout path, without a fault).
-        if (!(a.withhold_arrival && blockIdx.x == 0)) mma_commit(b_sfull);
-        mma_commit(b_empty0 + 8 * slot_of(unit_k(0)));
+        if (leader && !(a.withhold_arrival && blockIdx.x == 0)) mma_commit(b_sfull);
+        if (leader) mma_commit(b_empty0 + 8 * slot_of(unit_k(0)));
       }
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n) {
           // S_{j+1} once S_j has been read out of TMEM
           const int uk = unit_k(j + 1);
-          if (!(ok = wait_bounded(b_full0 + 8 * slot_of(uk), parity_of(uk), ctl, a.status,
+          if (!(ok = wait_warp(b_full0 + 8 * slot_of(uk), parity_of(uk), ctl, a.status,
                                   a.timeout_ns)))
             break;
-          if (!(ok = wait_bounded(b_sfree, j & 1, ctl, a.status, a.timeout_ns))) break;
+          if (!(ok = wait_warp(b_sfree, j & 1, ctl, a.status, a.timeout_ns))) break;
           tc_fence_after();
           issue_S(slot_of(uk));
-          mma_commit(b_sfull);
-          mma_commit(b_empty0 + 8 * slot_of(uk));
+          if (leader) mma_commit(b_sfull);
+          if (leader) mma_commit(b_empty0 + 8 * slot_of(uk));
         }
         // P_j V_j once P_j is in TMEM
         const int uv = unit_v(j);
-        if (!(ok = wait_bounded(b_full0 + 8 * slot_of(uv), parity_of(uv), ctl, a.status,
+        if (!(ok = wait_warp(b_full0 + 8 * slot_of(uv), parity_of(uv), ctl, a.status,
                                 a.timeout_ns)))
           break;
-        if (!(ok = wait_bounded(b_pready, j & 1, ctl, a.status, a.timeout_ns))) break;
+        if (!(ok = wait_warp(b_pready, j & 1, ctl, a.status, a.timeout_ns))) break;
         tc_fence_after();
         issue_PV(slot_of(uv), j > 0);
-        mma_commit(b_pvdone);
-        mma_commit(b_empty0 + 8 * slot_of(uv));
+        if (leader) mma_commit(b_pvdone);
+        if (leader) mma_commit(b_empty0 + 8 * slot_of(uv));
       }
       // Drain: every MMA (and every commit arrival) of this thread is complete.
-      mma_commit(b_mmadone);
+      if (leader) mma_commit(b_mmadone);
       wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
     }
     __syncwarp();
