@@ -313,6 +313,8 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // Issued from one lane: the whole-warp form of the other kernels ran this
+    // kernel about 3 % slower, its pace being set by the elementwise warps.
     if (lane == 0) {
       const uint32_t idS = idesc_f16<T>(128, C::BT, false, false);
       const uint32_t idG = idesc_f16<T>(128, D, false, true);
@@ -877,7 +879,11 @@ __global__ void __launch_bounds__(320, 1)
     // (item count) & 1 and dV | dK into accumulator pair (item count) & 1,
     // whose first product waits until the epilogue of the item two back has
     // read that pair.
-    if (lane == 0) {
+    // The whole warp runs the issue loop and its waits (warp-uniform loop
+    // control and descriptor arithmetic); one elected lane issues the
+    // products and commits.
+    {
+      const bool leader = elect_one();
       const uint32_t idS = idesc_f16<T>(128, C::BT, false, false);
       const uint32_t idG = idesc_f16<T>(128, D, false, true);
       const uint64_t dKV0 = sdesc_sw128(smem_u32(smem + C::OFF_KV), 16, 1024);
@@ -891,9 +897,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_ST, kd + off, q + off, idS, kk > 0 ? 1u : 0u);
+          if (leader) mma_ss(tmem + C::COL_ST, kd + off, q + off, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(b_sfull);
+        if (leader) mma_commit(b_sfull);
       };
       auto issue_DPT = [&](int ds, int buf) {  // dP^T = V dO^T
         const uint64_t gd = dDk + static_cast<uint64_t>((ds * C::DSLOT) >> 4);
@@ -901,9 +907,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_DPT, vd + off, gd + off, idS, kk > 0 ? 1u : 0u);
+          if (leader) mma_ss(tmem + C::COL_DPT, vd + off, gd + off, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(b_dpfull);
+        if (leader) mma_commit(b_dpfull);
       };
       uint32_t gstep = 0;   // steps of this CTA so far (< 2^31)
       int li = 0;
@@ -915,16 +921,16 @@ __global__ void __launch_bounds__(320, 1)
         if (itm.n == 0) continue;
         const int buf = li & 1;
         const uint32_t accv = tmem + C::COL_ACC + 128 * buf, acck = accv + 64;
-        ok = wait_bounded(b_kvfull0 + 8 * buf, (li >> 1) & 1, ctl, a.status, a.timeout_ns) &&
-             wait_bounded(b_qfull0 + 8 * static_cast<int>(gstep % C::NQ),
+        ok = wait_warp(b_kvfull0 + 8 * buf, (li >> 1) & 1, ctl, a.status, a.timeout_ns) &&
+             wait_warp(b_qfull0 + 8 * static_cast<int>(gstep % C::NQ),
                           static_cast<uint32_t>(gstep / C::NQ) & 1, ctl, a.status, a.timeout_ns) &&
-             wait_bounded(b_dfull0 + 8 * static_cast<int>(gstep % C::ND),
+             wait_warp(b_dfull0 + 8 * static_cast<int>(gstep % C::ND),
                           static_cast<uint32_t>(gstep / C::ND) & 1, ctl, a.status, a.timeout_ns);
         if (!ok) break;
         tc_fence_after();
         issue_ST(static_cast<int>(gstep % C::NQ), buf);
         issue_DPT(static_cast<int>(gstep % C::ND), buf);
-        if (li >= 2 && !(ok = wait_bounded(b_accfree0 + 8 * buf, ((li >> 1) - 1) & 1, ctl, a.status,
+        if (li >= 2 && !(ok = wait_warp(b_accfree0 + 8 * buf, ((li >> 1) - 1) & 1, ctl, a.status,
                                            a.timeout_ns)))
           break;
         for (int it = 0; ok && it < itm.n; ++it) {
@@ -936,17 +942,17 @@ __global__ void __launch_bounds__(320, 1)
           // dV += P^T dO (B: this step's dO read MN-major, N = d)
           const uint64_t mdo = dDm + static_cast<uint64_t>((ds * C::DSLOT) >> 4);
           for (int h = 0; ok && h < 2; ++h) {
-            if (!(ok = wait_bounded(b_pready0 + 8 * h, par, ctl, a.status, a.timeout_ns))) break;
+            if (!(ok = wait_warp(b_pready0 + 8 * h, par, ctl, a.status, a.timeout_ns))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(accv, tmem + C::COL_ST + 64 * h + 8 * kk,
+              if (leader) mma_ts(accv, tmem + C::COL_ST + 64 * h + 8 * kk,
                      mdo + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
                      (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
           }
           if (!ok) break;
           if (next) {
-            if (!(ok = wait_bounded(b_qfull0 + 8 * qs1, static_cast<uint32_t>((g + 1) / C::NQ) & 1,
+            if (!(ok = wait_warp(b_qfull0 + 8 * qs1, static_cast<uint32_t>((g + 1) / C::NQ) & 1,
                                     ctl, a.status, a.timeout_ns)))
               break;
             tc_fence_after();
@@ -955,19 +961,19 @@ __global__ void __launch_bounds__(320, 1)
           // dK += dS^T Q (B: this step's Q read MN-major)
           const uint64_t mq = dQm + static_cast<uint64_t>((qs * C::TILE) >> 4);
           for (int h = 0; ok && h < 2; ++h) {
-            if (!(ok = wait_bounded(b_dsready0 + 8 * h, par, ctl, a.status, a.timeout_ns))) break;
+            if (!(ok = wait_warp(b_dsready0 + 8 * h, par, ctl, a.status, a.timeout_ns))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(acck, tmem + C::COL_DPT + 64 * h + 8 * kk,
+              if (leader) mma_ts(acck, tmem + C::COL_DPT + 64 * h + 8 * kk,
                      mq + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
                      (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
           }
           if (!ok) break;
-          mma_commit(b_qempty0 + 8 * qs);
-          mma_commit(b_dempty0 + 8 * ds);
+          if (leader) mma_commit(b_qempty0 + 8 * qs);
+          if (leader) mma_commit(b_dempty0 + 8 * ds);
           if (next) {
-            if (!(ok = wait_bounded(b_dfull0 + 8 * ds1, static_cast<uint32_t>((g + 1) / C::ND) & 1,
+            if (!(ok = wait_warp(b_dfull0 + 8 * ds1, static_cast<uint32_t>((g + 1) / C::ND) & 1,
                                     ctl, a.status, a.timeout_ns)))
               break;
             tc_fence_after();
@@ -975,12 +981,12 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         if (!ok) break;
-        mma_commit(b_kvempty0 + 8 * buf);
-        mma_commit(b_accdone0 + 8 * buf);
+        if (leader) mma_commit(b_kvempty0 + 8 * buf);
+        if (leader) mma_commit(b_accdone0 + 8 * buf);
         gstep += static_cast<uint32_t>(itm.n);
         ++li;
       }
-      mma_commit(b_mmadone);
+      if (leader) mma_commit(b_mmadone);
       wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
     }
     __syncwarp();
@@ -1311,7 +1317,11 @@ __global__ void __launch_bounds__(320, 1)
     // Order: S_0, dP_0, then per key tile jt: S_jt+1 (once S_jt has been read
     // out of TMEM), dQ += dS_jt K_jt (per half as ready), dP_jt+1 (it
     // overwrites dS_jt, read only by the dQ products issued before it).
-    if (lane == 0) {
+    // The whole warp runs the issue loop and its waits (warp-uniform loop
+    // control and descriptor arithmetic); one elected lane issues the
+    // products and commits.
+    {
+      const bool leader = elect_one();
       const uint32_t idS = idesc_f16<T>(128, C::BT, false, false);
       const uint32_t idG = idesc_f16<T>(128, D, false, true);
       const uint64_t dSt0 = sdesc_sw128(smem_u32(sStage), 16, 1024);
@@ -1323,10 +1333,11 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          if constexpr (QS)
-            mma_ss(tmem + C::COL_S, dQa + off, kb + off, idS, kk > 0 ? 1u : 0u);
-          else
-            mma_ts(tmem + C::COL_S, tmem + C::COL_Q + 8 * kk, kb + off, idS, kk > 0 ? 1u : 0u);
+          if constexpr (QS) {
+            if (leader) mma_ss(tmem + C::COL_S, dQa + off, kb + off, idS, kk > 0 ? 1u : 0u);
+          } else {
+            if (leader) mma_ts(tmem + C::COL_S, tmem + C::COL_Q + 8 * kk, kb + off, idS, kk > 0 ? 1u : 0u);
+          }
         }
       };
       auto issue_dP = [&](int st) {  // dP = dO V^T, dO from TMEM (or shared memory, QS)
@@ -1334,53 +1345,54 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          if constexpr (QS)
-            mma_ss(tmem + C::COL_DP, dDa + off, vb + off, idS, kk > 0 ? 1u : 0u);
-          else
-            mma_ts(tmem + C::COL_DP, tmem + C::COL_DO + 8 * kk, vb + off, idS, kk > 0 ? 1u : 0u);
+          if constexpr (QS) {
+            if (leader) mma_ss(tmem + C::COL_DP, dDa + off, vb + off, idS, kk > 0 ? 1u : 0u);
+          } else {
+            if (leader) mma_ts(tmem + C::COL_DP, tmem + C::COL_DO + 8 * kk, vb + off, idS, kk > 0 ? 1u : 0u);
+          }
         }
       };
-      bool ok = wait_bounded(QS ? b_q : b_qt, 0, ctl, a.status, a.timeout_ns) &&
-                wait_bounded(b_kvfull0, 0, ctl, a.status, a.timeout_ns);
+      bool ok = wait_warp(QS ? b_q : b_qt, 0, ctl, a.status, a.timeout_ns) &&
+                wait_warp(b_kvfull0, 0, ctl, a.status, a.timeout_ns);
       if (ok) {
         tc_fence_after();
         issue_S(0);
-        mma_commit(b_sfull);
+        if (leader) mma_commit(b_sfull);
         issue_dP(0);
-        mma_commit(b_dpfull);
+        if (leader) mma_commit(b_dpfull);
       }
       for (int jt = 0; ok && jt < n; ++jt) {
         const int st = jt % NR;
         const bool next = jt + 1 < n;
         const int stn = (jt + 1) % NR;
         if (next) {
-          if (!(ok = wait_bounded(b_kvfull0 + 8 * stn, ((jt + 1) / NR) & 1, ctl, a.status,
+          if (!(ok = wait_warp(b_kvfull0 + 8 * stn, ((jt + 1) / NR) & 1, ctl, a.status,
                                   a.timeout_ns)))
             break;
-          if (!(ok = wait_bounded(b_sfree, jt & 1, ctl, a.status, a.timeout_ns))) break;
+          if (!(ok = wait_warp(b_sfree, jt & 1, ctl, a.status, a.timeout_ns))) break;
           tc_fence_after();
           issue_S(stn);
-          mma_commit(b_sfull);
+          if (leader) mma_commit(b_sfull);
         }
         const uint64_t kmn = dSt0mn + static_cast<uint64_t>((st * C::STAGE) >> 4);
         for (int h = 0; ok && h < 2; ++h) {
-          if (!(ok = wait_bounded(b_dsready0 + 8 * h, jt & 1, ctl, a.status, a.timeout_ns))) break;
+          if (!(ok = wait_warp(b_dsready0 + 8 * h, jt & 1, ctl, a.status, a.timeout_ns))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + C::COL_DQ, tmem + C::COL_DP + 64 * h + 8 * kk,
+            if (leader) mma_ts(tmem + C::COL_DQ, tmem + C::COL_DP + 64 * h + 8 * kk,
                    kmn + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
                    (jt > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        mma_commit(b_kvempty0 + 8 * st);
+        if (leader) mma_commit(b_kvempty0 + 8 * st);
         if (next) {
           issue_dP(stn);
-          mma_commit(b_dpfull);
+          if (leader) mma_commit(b_dpfull);
         }
       }
-      if (ok) mma_commit(b_accdone);
-      mma_commit(b_mmadone);
+      if (ok && leader) mma_commit(b_accdone);
+      if (leader) mma_commit(b_mmadone);
       wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
     }
     __syncwarp();
