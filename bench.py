@@ -57,10 +57,10 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 1059.1 MB per launch measured on 16 heads,
+    # bwd_dkdv_tc_kernel<bf16,128>: 1054.6 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("dkdv", "2603f5ecd4f321ede3d40be96316f6609c1a2b27ee50cb4f2dd425b9f5b2613a",
-     "long-bf16-B1-H32-N16384-D128-causal"): 2118.1e6,
+    ("dkdv", "dcc23652d15ff4e163ec9f00c843d05db4ddca802745dca019a788aab259a703",
+     "long-bf16-B1-H32-N16384-D128-causal"): 2109.1e6,
     # bwd_fused_tc_kernel<bf16,128>: 2929.2 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
     ("fused", "7a40ac2fd235fad28a6a7f44662e8e368ab7a4b4121be356c5b381d64da86cd1",
@@ -758,13 +758,17 @@ def measure_e2e(args, w, dev, fa, fused=False):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
         start.record(s_in)
+        h0 = time.perf_counter()
         for i in range(args.steps):
             step(i)
+        host_issue_ms = (time.perf_counter() - h0) * 1e3
         # the end event follows the last copy of every stream
         s_in.wait_stream(s_comp); s_in.wait_stream(s_out)
         end.record(s_in)
         torch.cuda.synchronize(dev)
     ms = start.elapsed_time(end) / args.steps
+    # compute idle between consecutive steps (0 when the copies are hidden)
+    idle = [comp_ev[i][1].elapsed_time(comp_ev[i + 1][0]) for i in range(args.steps - 1)]
     comp_overlap_ms = statistics.median(e[0].elapsed_time(e[1]) for e in comp_ev.values())
     h2d_overlap_ms = statistics.median(e[2].elapsed_time(e[3]) for e in comp_ev.values())
     d2h_overlap_ms = statistics.median(e[4].elapsed_time(e[5]) for e in comp_ev.values())
@@ -780,12 +784,15 @@ def measure_e2e(args, w, dev, fa, fused=False):
                      "compute_during_copies_ms": comp_overlap_ms,
                      "h2d_during_compute_ms": h2d_overlap_ms,
                      "d2h_during_compute_ms": d2h_overlap_ms,
+                     "compute_idle_between_steps_ms": statistics.median(idle) if idle else 0.0,
+                     "host_issue_ms": host_issue_ms,
                      "clocks": clocks.summary(),
                      "bound_ms": max(comp_ms, h2d_ms, d2h_ms),
                      "note": "each direction's copies alone on the step's pinned buffers; "
                              "compute alone on the same device buffers; with full overlap "
-                             "a step takes max of the three; the *_during_* times are the medians "
-                             "of the timed end-to-end steps"}}
+                             "a step takes max of the three; the *_during_* times and the compute "
+                             "idle between steps are medians over the timed end-to-end steps; "
+                             "host_issue_ms is the host time to enqueue all timed steps"}}
 
 
 if __name__ == "__main__":
