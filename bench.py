@@ -57,10 +57,10 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 1054.6 MB per launch measured on 16 heads,
+    # bwd_dkdv_tc_kernel<bf16,128>: 395.7 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("dkdv", "dcc23652d15ff4e163ec9f00c843d05db4ddca802745dca019a788aab259a703",
-     "long-bf16-B1-H32-N16384-D128-causal"): 2109.1e6,
+    ("dkdv", "a8f01e6e6afad400d79ce12074feef0616d586f950bfa02b768a87b72028125e",
+     "long-bf16-B1-H32-N16384-D128-causal"): 791.4e6,
     # bwd_fused_tc_kernel<bf16,128>: 2929.2 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
     ("fused", "7a40ac2fd235fad28a6a7f44662e8e368ab7a4b4121be356c5b381d64da86cd1",

@@ -32,6 +32,7 @@ std::atomic<int> g_withhold_next{0};   // one-shot test switch (fa_test_withhold
 struct DeviceInfo {
   int state = 0;              // 0: not set up, 1: ready, -1: not sm_103
   int sm_count = 0;
+  int64_t l2_bytes = 0;
   unsigned int* status = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -44,10 +45,11 @@ fa_status device_setup(DeviceInfo** out) {
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceInfo& d = g_dev[dev];
   if (d.state == 0) {
-    int major = 0, minor = 0, sms = 0;
+    int major = 0, minor = 0, sms = 0, l2 = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
       return FA_ERR_LAUNCH;
     if (major != 10 || minor != 3) {
       d.state = -1;
@@ -56,6 +58,7 @@ fa_status device_setup(DeviceInfo** out) {
       if (cudaGetSymbolAddress(&p, fa_device_status_word) != cudaSuccess) return FA_ERR_LAUNCH;
       d.status = static_cast<unsigned int*>(p);
       d.sm_count = sms;
+      d.l2_bytes = l2;
       d.state = 1;
     }
   }
@@ -293,6 +296,24 @@ int device_sm_count() {
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   return sms > 0 ? sms : 1;
+}
+
+int64_t head_group(int64_t BH, int64_t per_head_bytes) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int64_t l2 = 0;
+  if (dev >= 0 && dev < kMaxDevices && g_dev[dev].state == 1) {
+    l2 = g_dev[dev].l2_bytes;
+  } else {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev);
+    l2 = v;
+  }
+  // All heads at once when their operands fit in L2 together (the order is
+  // then the plain longest-first one); otherwise groups of 3/8 of L2.
+  if (per_head_bytes <= 0 || BH * per_head_bytes <= l2 * 3 / 4) return BH;
+  const int64_t g = l2 * 3 / 8 / per_head_bytes;
+  return g < 1 ? 1 : (g > BH ? BH : g);
 }
 
 }  // namespace fa

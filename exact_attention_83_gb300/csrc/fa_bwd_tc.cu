@@ -60,6 +60,7 @@ struct BwdTcArgs {
   Geo g;
   int64_t BH;              // dK/dV kernel: B * Hkv;  dQ kernel: B * Hq
   int64_t ntiles;          // dK/dV kernel: key tiles;  dQ kernel: query tiles (longest sequence)
+  int64_t hgroup;          // heads per group of the block order (grouped_tile)
   int dreal;               // head dimension stored (<= D; narrower ones run zero-padded)
   int64_t s0[4], s1[4];    // strides of out0, out1
   int causal;
@@ -145,8 +146,10 @@ __global__ void __launch_bounds__(320, 1)
   const int split = a.split;
   const int rank = static_cast<int>(blockIdx.x % split);
   const int64_t id = blockIdx.x / split;
-  const int64_t bhk = id % a.BH;                // b * Hkv + key/value head
-  const int64_t kt = id / a.BH;                 // key tile; low tiles (most work) first
+  // Grouped order (grouped_tile): the key-tile CTAs in flight belong to a few
+  // heads, whose Q and dO tiles stay in L2; low key tiles (most work) first.
+  int64_t bhk, kt;                              // b * Hkv + key/value head, key tile
+  grouped_tile(id, a.BH, a.ntiles, a.hgroup, bhk, kt);
   const int64_t bseq = bhk / a.g.Hkv;
   const int32_t hk = static_cast<int32_t>(bhk % a.g.Hkv);
   const SeqView sv = seq_view(a.g, bseq);
@@ -1211,8 +1214,11 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t id = blockIdx.x;
-  const int64_t bh = id % a.BH;                 // b * Hq + h
-  const int64_t qt = a.causal ? (a.ntiles - 1 - id / a.BH) : (id / a.BH);   // longest first
+  // Grouped order (grouped_tile): the query-tile CTAs in flight belong to a
+  // few heads, whose K and V tiles stay in L2; the longest tiles first.
+  int64_t bh, t;                                // b * Hq + h
+  grouped_tile(id, a.BH, a.ntiles, a.hgroup, bh, t);
+  const int64_t qt = a.causal ? (a.ntiles - 1 - t) : t;
   const int64_t h = bh % a.g.Hq;
   const SeqView sv = seq_view(a.g, bh / a.g.Hq);
   if (!sv.ok) {
@@ -1579,6 +1585,9 @@ fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
   // shares each key tile's query heads, so the grid fills the SMs and the
   // heaviest key tiles no longer run alone.
   a.BH = g.B * g.Hkv; a.ntiles = (g.Nk + 127) / 128;
+  const int64_t esz = p.dtype == FA_F32 ? 4 : 2;
+  // Q and dO of a key/value head's G query heads: the operand all its CTAs read
+  a.hgroup = head_group(a.BH, 2 * g.Nq * p.D * esz * g.G);
   const int64_t base1 = a.BH * a.ntiles;
   int split = 1;
   while (split < 8 && g.G % (2 * split) == 0 && base1 * split < 2 * device_sm_count()) split *= 2;
@@ -1636,6 +1645,8 @@ fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
   // dQ: one CTA per (b, query head, query tile)
   a.split = 1;
   a.BH = g.B * g.Hq; a.ntiles = (g.Nq + 127) / 128;
+  // K and V of a query head's key/value head: the operand all its CTAs read
+  a.hgroup = head_group(a.BH, 2 * g.Nk * p.D * esz);
   const int64_t blocks2 = a.BH * a.ntiles;
   if (blocks2 > 0x7fffffffLL) return FA_ERR_SHAPE;
   a.out0 = p.dq; a.out1 = nullptr;

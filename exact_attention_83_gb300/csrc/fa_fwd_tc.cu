@@ -82,6 +82,7 @@ struct FwdTcArgs {
   float* lse;
   Geo g;
   int64_t BH, npairs;      // B * Hq; query-tile pairs of the longest sequence
+  int64_t hgroup;          // heads per group of the block order
   int dreal;               // head dimension stored (<= D; narrower ones run zero-padded)
   int64_t so[4];
   int causal;
@@ -116,8 +117,11 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t id = blockIdx.x;
-  const int64_t bh = id % a.BH;                 // b * Hq + h
-  const int64_t pr = a.causal ? (a.npairs - 1 - id / a.BH) : (id / a.BH);
+  // Grouped order (grouped_tile): the CTAs in flight belong to a few heads,
+  // whose K and V tiles stay in L2; the longest query-tile pairs first.
+  int64_t bh, t;                                // b * Hq + h
+  grouped_tile(id, a.BH, a.npairs, a.hgroup, bh, t);
+  const int64_t pr = a.causal ? (a.npairs - 1 - t) : t;
   const int64_t h = bh % a.g.Hq;
   const SeqView sv = seq_view(a.g, bh / a.g.Hq);
   if (!sv.ok) {
@@ -544,8 +548,9 @@ __global__ void __launch_bounds__(192, 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t id = blockIdx.x;
-  const int64_t bh = id % a.BH;                 // b * Hq + h
-  const int64_t qt = a.causal ? (a.npairs - 1 - id / a.BH) : (id / a.BH);   // query tile
+  int64_t bh, t;                                // b * Hq + h (grouped order, as above)
+  grouped_tile(id, a.BH, a.npairs, a.hgroup, bh, t);
+  const int64_t qt = a.causal ? (a.npairs - 1 - t) : t;   // query tile
   const int64_t h = bh % a.g.Hq;
   const SeqView sv = seq_view(a.g, bh / a.g.Hq);
   if (!sv.ok) {
@@ -889,6 +894,8 @@ fa_status run_fwd_tc(const FwdParams& p, cudaStream_t stream) {
   a.o = p.o; a.lse = p.lse;
   a.g = g;
   a.BH = g.B * g.Hq; a.npairs = (g.Nq + 255) / 256;
+  // K and V of a head: the operand all of its CTAs read
+  a.hgroup = head_group(a.BH, 2 * g.Nk * p.D * (p.dtype == FA_F32 ? 4 : 2));
   for (int i = 0; i < 4; ++i) a.so[i] = p.so[i];
   a.causal = p.causal;
   a.c = p.scale * kLog2e;

@@ -232,6 +232,33 @@ bool encode_f32_rows_map(CUtensorMap* map, const float* base, int64_t cols, int6
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Heads per group of the grouped block order (grouped_tile), from
+// `per_head_bytes` (the operand that all CTAs of a head read) and the current
+// device's L2: all BH heads when their operands fit in 3/4 of L2 together,
+// else as many as fit in 3/8 of it (at least 1).
+int64_t head_group(int64_t BH, int64_t per_head_bytes);
+
+// Grouped block order of the tiled kernels.  Blocks run roughly in index
+// order; heads are taken in groups of `hg`, and within a group the tile
+// index t varies slowest (t = 0 first: callers map it to their longest
+// tile) with the group's heads interleaved.  So the CTAs in flight belong to
+// a few heads, whose shared operand stays in L2, while each group still runs
+// longest first and the grid ends on short tiles.  With hg >= BH this is the
+// plain tile-major order over all heads.  Block `id` of BH * nt maps to head
+// `bh` and tile `t`.  The grid holds fewer than 2^31 blocks, so every value
+// here fits 32-bit unsigned arithmetic (cheaper divisions in the prologue).
+__device__ __forceinline__ void grouped_tile(int64_t id, int64_t BH, int64_t nt, int64_t hg,
+                                             int64_t& bh, int64_t& t) {
+  const uint32_t i = static_cast<uint32_t>(id), nh = static_cast<uint32_t>(BH);
+  const uint32_t g = static_cast<uint32_t>(hg), per = g * static_cast<uint32_t>(nt);
+  const uint32_t grp = i / per, rem = i - grp * per;
+  const uint32_t g0 = grp * g;
+  const uint32_t gh = nh - g0 < g ? nh - g0 : g;     // heads in this group
+  const uint32_t tt = rem / gh;
+  t = tt;
+  bh = g0 + (rem - tt * gh);
+}
+
 // Every argument check of fa_bwd_preprocess followed by fa_bwd on a square
 // problem (shape, dtype, scale, each tensor's pointer, alignment and strides,
 // lse), except the delta pointer, which the caller supplies itself.  Touches
