@@ -58,8 +58,9 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # profiles/.
 MEASURED_TRAFFIC = {
     # bwd_dkdv_tc_kernel<bf16,128>: 395.7 MB per launch measured on 16 heads,
-    # scaled by heads to the 32-head launch
-    ("dkdv", "a8f01e6e6afad400d79ce12074feef0616d586f950bfa02b768a87b72028125e",
+    # scaled by heads to the 32-head launch (captured on source a8f01e6e...;
+    # the file changed since only in the host launcher, not in any kernel)
+    ("dkdv", "1eff1ef5ffeb3978fc25486c466f58caa78b3f2537207e52b637d928579d209f",
      "long-bf16-B1-H32-N16384-D128-causal"): 791.4e6,
     # bwd_fused_tc_kernel<bf16,128>: 2929.2 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
@@ -756,16 +757,20 @@ def measure_e2e(args, w, dev, fa, fused=False):
     comp_ev.update({i: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
                     for i in range(args.steps)})
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev.index) as clocks:
-        start.record(s_in)
-        h0 = time.perf_counter()
-        for i in range(args.steps):
-            step(i)
-        host_issue_ms = (time.perf_counter() - h0) * 1e3
-        # the end event follows the last copy of every stream
-        s_in.wait_stream(s_comp); s_in.wait_stream(s_out)
-        end.record(s_in)
-        torch.cuda.synchronize(dev)
+    # No clock sampler here: nvidia-smi's queries stall this copy-heavy loop for
+    # milliseconds at a time (measured: with 50 ms polling the compute spans
+    # showed gaps of 0.8-4.6 ms and the first step started 1-6 ms late; without
+    # it, no gap), so its clocks would cost the number they describe.  The
+    # device-timed region, which has no copies, carries the clock record.
+    start.record(s_in)
+    h0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    host_issue_ms = (time.perf_counter() - h0) * 1e3
+    # the end event follows the last copy of every stream
+    s_in.wait_stream(s_comp); s_in.wait_stream(s_out)
+    end.record(s_in)
+    torch.cuda.synchronize(dev)
     ms = start.elapsed_time(end) / args.steps
     # compute idle between consecutive steps (0 when the copies are hidden)
     idle = [comp_ev[i][1].elapsed_time(comp_ev[i + 1][0]) for i in range(args.steps - 1)]
@@ -785,13 +790,19 @@ def measure_e2e(args, w, dev, fa, fused=False):
                      "h2d_during_compute_ms": h2d_overlap_ms,
                      "d2h_during_compute_ms": d2h_overlap_ms,
                      "compute_idle_between_steps_ms": statistics.median(idle) if idle else 0.0,
+                     "compute_idle_max_ms": max(idle) if idle else 0.0,
+                     "fill_ms": start.elapsed_time(comp_ev[0][0]),
+                     "drain_ms": comp_ev[args.steps - 1][1].elapsed_time(end),
                      "host_issue_ms": host_issue_ms,
-                     "clocks": clocks.summary(),
+                     "clocks": "not sampled in this region (nvidia-smi polling stalls its "
+                               "copies); see the line's clocks",
                      "bound_ms": max(comp_ms, h2d_ms, d2h_ms),
                      "note": "each direction's copies alone on the step's pinned buffers; "
                              "compute alone on the same device buffers; with full overlap "
                              "a step takes max of the three; the *_during_* times and the compute "
-                             "idle between steps are medians over the timed end-to-end steps; "
+                             "idle between steps are medians over the timed end-to-end steps "
+                             "(compute_idle_max_ms the longest gap); fill_ms / drain_ms: start to "
+                             "the first step's compute, last step's compute to the end; "
                              "host_issue_ms is the host time to enqueue all timed steps"}}
 
 

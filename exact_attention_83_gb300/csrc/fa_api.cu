@@ -252,10 +252,11 @@ fa_status run_bwd(const Problem& pb, const void* q, const int64_t* sq, const voi
                   const int64_t* sk, const void* v, const int64_t* sv, const void* dout,
                   const int64_t* sdo, const float* lse, const float* delta, void* dq,
                   const int64_t* sdq, void* dk, const int64_t* sdk, void* dv,
-                  const int64_t* sdv, cudaStream_t stream) {
-  BwdParams p;
+                  const int64_t* sdv, cudaStream_t stream, bool allow_side = true) {
+  BwdParams p{};
   FA_TRY(prepare_bwd(pb, q, sq, k, sk, v, sv, dout, sdo, lse, delta, dq, sdq, dk, sdk, dv, sdv,
                      &p));
+  p.allow_side = allow_side;
   if (use_tc(pb.dtype) && have_bwd_tc(pb.D, pb.dtype)) return launch_bwd_tc(p, stream);
   return launch_bwd_ffma(p, stream);
 }
@@ -298,6 +299,64 @@ int device_sm_count() {
   return sms > 0 ? sms : 1;
 }
 
+// Side stream of each device, for a kernel that may overlap the caller's
+// stream (the backward's dQ kernel beside its dK/dV kernel).  One fork/join
+// at a time per device: the lock is held from side_begin to side_end, so two
+// host threads never interleave the records of the shared events.
+struct SideStream {
+  std::mutex mu;
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[kMaxDevices];
+
+fa_status side_begin(cudaStream_t caller, cudaStream_t* side) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
+  SideStream& ss = g_side[dev];
+  ss.mu.lock();
+  if (ss.s == nullptr) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+      if (j) cudaEventDestroy(j);
+      if (f) cudaEventDestroy(f);
+      if (st) cudaStreamDestroy(st);
+      ss.mu.unlock();
+      return FA_ERR_LAUNCH;
+    }
+    ss.s = st; ss.fork = f; ss.join = j;
+  }
+  if (cudaEventRecord(ss.fork, caller) != cudaSuccess ||
+      cudaStreamWaitEvent(ss.s, ss.fork, 0) != cudaSuccess) {
+    ss.mu.unlock();
+    return FA_ERR_LAUNCH;
+  }
+  *side = ss.s;
+  return FA_OK;
+}
+
+fa_status side_end(cudaStream_t caller) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  SideStream& ss = g_side[dev];
+  const bool ok = cudaEventRecord(ss.join, ss.s) == cudaSuccess &&
+                  cudaStreamWaitEvent(caller, ss.join, 0) == cudaSuccess;
+  ss.mu.unlock();
+  return ok ? FA_OK : FA_ERR_LAUNCH;
+}
+
+bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();          // clear the error; treat as capturing
+    return true;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
+
 int64_t head_group(int64_t BH, int64_t per_head_bytes) {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -314,6 +373,20 @@ int64_t head_group(int64_t BH, int64_t per_head_bytes) {
   if (per_head_bytes <= 0 || BH * per_head_bytes <= l2 * 3 / 4) return BH;
   const int64_t g = l2 * 3 / 8 / per_head_bytes;
   return g < 1 ? 1 : (g > BH ? BH : g);
+}
+
+fa_status bwd_square(const void* q, const void* k, const void* v, const void* dout,
+                     const float* lse, const float* delta, void* dq, void* dk, void* dv,
+                     int64_t B, int64_t H, int64_t N, int64_t D, const int64_t* sq,
+                     const int64_t* sk, const int64_t* sv, const int64_t* sdo,
+                     const int64_t* sdq, const int64_t* sdk, const int64_t* sdv, int causal,
+                     float scale, fa_dtype dtype, cudaStream_t stream, bool allow_side) {
+  FA_TRY(check_shape(B, H, N, D, dtype));
+  const fa_problem pr = square_problem(B, H, N, D, causal, scale, dtype);
+  Problem pb{};
+  FA_TRY(check_problem(&pr, &pb));
+  return run_bwd(pb, q, sq, k, sk, v, sv, dout, sdo, lse, delta, dq, sdq, dk, sdk, dv, sdv,
+                 stream, allow_side);
 }
 
 }  // namespace fa
@@ -358,6 +431,7 @@ fa_status fa_bwd_preprocess(const void* o, const void* dout, float* delta,
   return launch_preprocess(p, stream);
 }
 
+
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout,
                  const float* lse, const float* delta, void* dq, void* dk, void* dv,
                  int64_t B, int64_t H, int64_t N, int64_t D,
@@ -365,12 +439,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout,
                  const int64_t* sdo, const int64_t* sdq, const int64_t* sdk,
                  const int64_t* sdv, int causal, float scale, fa_dtype dtype,
                  cudaStream_t stream) {
-  FA_TRY(check_shape(B, H, N, D, dtype));
-  const fa_problem pr = square_problem(B, H, N, D, causal, scale, dtype);
-  Problem pb{};
-  FA_TRY(check_problem(&pr, &pb));
-  return run_bwd(pb, q, sq, k, sk, v, sv, dout, sdo, lse, delta, dq, sdq, dk, sdk, dv, sdv,
-                 stream);
+  return bwd_square(q, k, v, dout, lse, delta, dq, dk, dv, B, H, N, D, sq, sk, sv, sdo, sdq,
+                    sdk, sdv, causal, scale, dtype, stream, true);
 }
 
 fa_status fa_bwd_ex(const fa_problem* prob, const void* q, const int64_t* sq, const void* k,
@@ -427,7 +497,7 @@ fa_status fa_bwd_fused(const fa_problem* prob, const void* q, const int64_t* sq,
   if (reinterpret_cast<uintptr_t>(dq_accum) % 16 != 0) return FA_ERR_ALIGN;
   if (workspace_bytes < bwd_fused_workspace_floats(pb.g, pb.D) * sizeof(float))
     return FA_ERR_SCRATCH;
-  BwdParams p;
+  BwdParams p{};
   FA_TRY(prepare_bwd(pb, q, sq, k, sk, v, sv, dout, sdo, lse, delta, dq, sdq, dk, sdk, dv, sdv,
                      &p));
   p.withhold_arrival = g_withhold_next.exchange(0);

@@ -1558,6 +1558,22 @@ __global__ void __launch_bounds__(320, 1)
 // Longest sequence (query and key rows) for which the D <= 64 backward runs
 // the persistent dK/dV kernel.
 constexpr int64_t kPersistMaxN = 1024;
+// Sequences at most this long run the dQ kernel concurrently with the dK/dV
+// kernel (see run_bwd_tc).
+constexpr int64_t kConcurrentMaxN = 4096;
+
+// Joins the side stream back into the caller's stream on every return path.
+struct SideJoin {
+  cudaStream_t caller;
+  bool on = false;
+  ~SideJoin() {
+    if (on) side_end(caller);
+  }
+  fa_status end() {
+    on = false;
+    return side_end(caller);
+  }
+};
 
 template <typename T, int D, int DROP>
 fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
@@ -1597,6 +1613,22 @@ fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
   a.out0 = p.dv; a.out1 = p.dk;
   for (int i = 0; i < 4; ++i) { a.s0[i] = p.sdv[i]; a.s1[i] = p.sdk[i]; }
   // Short sequences (a few steps per key tile) at D <= 64 without dropout:
+  // Short sequences: the dQ kernel, which shares only inputs with the dK/dV
+  // kernel, runs on the device's side stream at the same time, so each fills
+  // SMs that the other's small grid and tail leave idle (N = 512: backward
+  // 169 -> 155 us).  Longer sequences keep them in sequence: their grids fill
+  // the GPU, and each kernel's launch duration stays its own.  Never while
+  // the caller's stream is being captured into a graph (the shared side
+  // stream would join that capture).
+  const bool concurrent = p.allow_side && g.Nq <= kConcurrentMaxN && g.Nk <= kConcurrentMaxN &&
+                          !stream_capturing(stream);
+  SideJoin join{stream};
+  cudaStream_t s2 = stream;
+  if (concurrent) {
+    const fa_status st = side_begin(stream, &s2);
+    if (st != FA_OK) return st;
+    join.on = true;
+  }
   // the persistent kernel, one CTA per SM walking the key tiles, hides each
   // tile's set-up, first loads and epilogue behind its neighbours'.
   bool persist = false;
@@ -1654,9 +1686,13 @@ fa_status run_bwd_tc(const BwdParams& p, cudaStream_t stream) {
   auto k2 = bwd_dq_tc_kernel<T, D, DROP>;
   if (cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM) != cudaSuccess)
     return FA_ERR_LAUNCH;
-  k2<<<dim3(static_cast<unsigned>(blocks2)), dim3(DqCfg<D>::THREADS), DqCfg<D>::SMEM, stream>>>(
+  k2<<<dim3(static_cast<unsigned>(blocks2)), dim3(DqCfg<D>::THREADS), DqCfg<D>::SMEM, s2>>>(
       mq, mk, mv, mdo, a);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  if (concurrent) {
+    const fa_status st = join.end();
+    if (st != FA_OK) return st;
+  }
   prof_record(p, 2, stream);
   return FA_OK;
 }

@@ -87,6 +87,7 @@ struct BwdParams {
   uint64_t timeout_ns;
   const cudaEvent_t* prof;   // 3 events to record around the two kernels, or null
   int withhold_arrival;      // test-only (single-pass backward): see fa.h
+  bool allow_side;           // the dQ kernel may run on the device's side stream
 };
 
 #ifdef __CUDACC__
@@ -231,6 +232,26 @@ bool encode_f32_rows_map(CUtensorMap* map, const float* base, int64_t cols, int6
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// fa_bwd with the choice of letting the tensor-core dQ kernel use the side
+// stream (fa_bwd: yes; fa_bwd_noalloc, which creates nothing: no).
+fa_status bwd_square(const void* q, const void* k, const void* v, const void* dout,
+                     const float* lse, const float* delta, void* dq, void* dk, void* dv,
+                     int64_t B, int64_t H, int64_t N, int64_t D, const int64_t* sq,
+                     const int64_t* sk, const int64_t* sv, const int64_t* sdo,
+                     const int64_t* sdq, const int64_t* sdk, const int64_t* sdv, int causal,
+                     float scale, fa_dtype dtype, cudaStream_t stream, bool allow_side);
+
+// The current device's side stream: side_begin makes it wait for the work
+// enqueued so far on `caller` and returns it (holding the device's fork/join
+// lock); side_end makes `caller` wait for everything enqueued on the side
+// stream since and releases the lock.  Every successful side_begin must be
+// followed by side_end on the same thread.
+fa_status side_begin(cudaStream_t caller, cudaStream_t* side);
+fa_status side_end(cudaStream_t caller);
+// True while `s` is being captured into a CUDA graph (or its status cannot
+// be read).
+bool stream_capturing(cudaStream_t s);
 
 // Heads per group of the grouped block order (grouped_tile), from
 // `per_head_bytes` (the operand that all CTAs of a head read) and the current

@@ -65,6 +65,8 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   // reads, so stale contents of the array are never used.
   const fa_status pre = fa_bwd_preprocess(o, dout, delta, B, H, N, D, so, sdo, dtype, stream);
   if (pre != FA_OK) return pre;
-  return fa_bwd(q, k, v, dout, lse, delta, dq, dk, dv, B, H, N, D, sq, sk, sv, sdo, sdq, sdk, sdv,
-                causal, scale, dtype, stream);
+  // In sequence on `stream`: this entry point creates nothing, not even the
+  // side stream fa_bwd may use.
+  return fa::bwd_square(q, k, v, dout, lse, delta, dq, dk, dv, B, H, N, D, sq, sk, sv, sdo, sdq, sdk,
+                    sdv, causal, scale, dtype, stream, false);
 }

@@ -47,6 +47,11 @@
  * -> fa_bwd must run in that order on one stream (or be ordered by the caller
  * with events).  The return code reports argument and launch errors only;
  * a device-side wait that runs out is reported by fa_get_device_status.
+ * The tensor-core backward may run part of its work on a stream of the
+ * library's own (one per device, created on first use and kept): that work
+ * starts after everything enqueued on `stream` before the call, and `stream`
+ * waits for it before anything enqueued after the call, so the call is
+ * ordered on `stream` like a single kernel.
  *
  * Precision.  fp16/bf16: products on tensor cores with fp32 accumulation; the
  * probabilities are rounded to the input type before P.V, dS and P^T before
@@ -113,8 +118,11 @@ FA_API fa_status fa_bwd_preprocess(const void* o, const void* dout, float* delta
 /*
  * Backward.  From Q, K, V, dO, the forward's lse and the preprocess's delta,
  * writes dQ, dK, dV (strides sdq, sdk, sdv).  P is rebuilt tile by tile as
- * exp(S - L); no N x N matrix is stored.  Runs a dK/dV kernel and then a dQ
- * kernel on `stream`; neither uses atomics.
+ * exp(S - L); no N x N matrix is stored.  Runs a dK/dV kernel and a dQ
+ * kernel; neither uses atomics.  With both sequence lengths at most 4096 (and
+ * `stream` not being captured into a CUDA graph) the tensor-core dQ kernel
+ * runs on the library's stream at the same time as the dK/dV kernel (see
+ * Ordering above); otherwise the two run one after the other on `stream`.
  */
 FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* dout,
                  const float* lse, const float* delta, void* dq, void* dk, void* dv,
@@ -358,8 +366,10 @@ FA_API void fa_set_wait_timeout_ns(uint64_t ns);
 /*
  * Profiling hook for benchmarks.  When `events` is non-NULL its three handles
  * are copied, and every later fa_bwd call records events[0] before its dK/dV
- * kernel, events[1] between the dK/dV and the dQ kernel, and events[2] after
- * the dQ kernel, on the call's stream.  NULL turns the hook off.  The caller
+ * kernel, events[1] after the dK/dV kernel, and events[2] after the dQ
+ * kernel, on the call's stream.  When the two kernels run at the same time
+ * (see fa_bwd), events[1] marks the dK/dV kernel's end and events[2] the end
+ * of both, so events[1] -> events[2] is not the dQ kernel's duration.  NULL turns the hook off.  The caller
  * creates and destroys the events and must not destroy them while the hook is
  * on.
  */
