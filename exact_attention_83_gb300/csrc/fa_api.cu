@@ -29,6 +29,7 @@ std::mutex g_mu;
 cudaEvent_t g_prof_events[3];
 std::atomic<bool> g_prof_on{false};
 std::atomic<int> g_withhold_next{0};   // one-shot test switch (fa_test_withhold_next_arrival)
+std::atomic<int64_t> g_l2_override{0};  // test switch (fa_test_set_l2_bytes)
 struct DeviceInfo {
   int state = 0;              // 0: not set up, 1: ready, -1: not sm_103
   int sm_count = 0;
@@ -368,6 +369,8 @@ int64_t head_group(int64_t BH, int64_t per_head_bytes) {
     cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev);
     l2 = v;
   }
+  const int64_t forced = g_l2_override.load();
+  if (forced > 0) l2 = forced;
   // All heads at once when their operands fit in L2 together (the order is
   // then the plain longest-first one); otherwise groups of 3/8 of L2.
   if (per_head_bytes <= 0 || BH * per_head_bytes <= l2 * 3 / 4) return BH;
@@ -559,6 +562,8 @@ void fa_set_profile_events(const cudaEvent_t* events) {
 }
 
 void fa_test_withhold_next_arrival(void) { g_withhold_next.store(1); }
+
+void fa_test_set_l2_bytes(int64_t bytes) { g_l2_override.store(bytes > 0 ? bytes : 0); }
 
 int fa_version(void) { return 0x000200; }
 

@@ -388,6 +388,18 @@ FA_API void fa_set_profile_events(const cudaEvent_t* events);
  */
 FA_API void fa_test_withhold_next_arrival(void);
 
+/*
+ * Test hook for the tiled kernels' block order.  The forward, dK/dV and dQ
+ * grids take heads in groups whose shared operand (K and V, or Q and dO) fits
+ * in part of the L2 cache, so that the CTAs in flight reuse it from L2; a
+ * group holds every head when all fit.  With `bytes` > 0 later calls size the
+ * groups as if L2 held that many bytes (small values force several groups,
+ * and a partial last one, on small problems); 0 restores the device's own
+ * size.  The order changes which CTAs run together, never what any CTA
+ * computes, so outputs are bitwise the same for every setting.
+ */
+FA_API void fa_test_set_l2_bytes(int64_t bytes);
+
 /* Library version, e.g. 0x000100 for 0.1.0. */
 FA_API int fa_version(void);
 
