@@ -565,6 +565,6 @@ void fa_test_withhold_next_arrival(void) { g_withhold_next.store(1); }
 
 void fa_test_set_l2_bytes(int64_t bytes) { g_l2_override.store(bytes > 0 ? bytes : 0); }
 
-int fa_version(void) { return 0x000200; }
+int fa_version(void) { return 0x000300; }
 
 }  // extern "C"
