@@ -262,7 +262,10 @@ FA_API fa_status fa_fwd_ex(const fa_problem* prob, const void* q, const int64_t*
  * Backward for a general problem: dQ, dK, dV from Q, K, V, dO, the forward's
  * lse and delta = rowsum(dO o O) (fa_bwd_preprocess over the Q-shaped rows:
  * B, Hq, Nq for fixed lengths; 1, Hq, total_q for packed ones).  Same problem
- * description (seed and offset included) as the forward call.
+ * description (seed and offset included) as the forward call.  Like fa_bwd,
+ * runs its dQ kernel on the library's own stream beside the dK/dV kernel when
+ * Nq and Nk are at most 4096 and `stream` is not being captured (see
+ * Ordering).
  */
 FA_API fa_status fa_bwd_ex(const fa_problem* prob, const void* q, const int64_t* sq,
                            const void* k, const int64_t* sk, const void* v,
