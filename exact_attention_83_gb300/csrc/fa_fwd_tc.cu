@@ -350,9 +350,6 @@ __global__ void __launch_bounds__(320, 1)
         if (mrow) mrow[j * a.g.rows_q] = make_uint4(kb[0], kb[1], kb[2], kb[3]);
       }
       if (!(ok = wait_warp(b_sfull0 + 8 * g, j & 1, ctl, a.status, a.timeout_ns))) break;
-      // S_j complete: every product reading ring unit j has completed (see the
-      // ring above); release it if the producer still has a unit for its slot
-
       tc_fence_after();
       float s[128];
       {
