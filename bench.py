@@ -57,11 +57,10 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 395.7 MB per launch measured on 16 heads,
-    # scaled by heads to the 32-head launch (captured on source a8f01e6e...;
-    # the file changed since only in the host launcher, not in any kernel)
-    ("dkdv", "1eff1ef5ffeb3978fc25486c466f58caa78b3f2537207e52b637d928579d209f",
-     "long-bf16-B1-H32-N16384-D128-causal"): 791.4e6,
+    # bwd_dkdv_tc_kernel<bf16,128>: 394.6 MB per launch measured on 16 heads,
+    # scaled by heads to the 32-head launch
+    ("dkdv", "28310b903eaa7175eb42420417c60a2eab20d688f112556c0fb20b671c964aab",
+     "long-bf16-B1-H32-N16384-D128-causal"): 789.2e6,
     # bwd_fused_tc_kernel<bf16,128>: 2929.2 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
     ("fused", "7a40ac2fd235fad28a6a7f44662e8e368ab7a4b4121be356c5b381d64da86cd1",
@@ -657,6 +656,9 @@ def run_sweep(fa, dev, stream, steps: int, warmup: int, peak: float):
             "clocks": clocks.summary()}
 
 
+E2E_REPS = 3     # repetitions of the end-to-end loop; the median one is reported
+
+
 def measure_e2e(args, w, dev, fa, fused=False):
     """Same metric through the public API with host buffers.  Every step copies
     Q, K, V, dO from pinned host memory to the device, runs the forward and
@@ -754,29 +756,46 @@ def measure_e2e(args, w, dev, fa, fused=False):
     cb.record(s_comp)
     torch.cuda.synchronize(dev)
     comp_ms = ca.elapsed_time(cb) / args.steps
-    comp_ev.update({i: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-                    for i in range(args.steps)})
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # No clock sampler here: nvidia-smi's queries stall this copy-heavy loop for
     # milliseconds at a time (measured: with 50 ms polling the compute spans
     # showed gaps of 0.8-4.6 ms and the first step started 1-6 ms late; without
     # it, no gap), so its clocks would cost the number they describe.  The
     # device-timed region, which has no copies, carries the clock record.
-    start.record(s_in)
-    h0 = time.perf_counter()
-    for i in range(args.steps):
-        step(i)
-    host_issue_ms = (time.perf_counter() - h0) * 1e3
-    # the end event follows the last copy of every stream
-    s_in.wait_stream(s_comp); s_in.wait_stream(s_out)
-    end.record(s_in)
-    torch.cuda.synchronize(dev)
-    ms = start.elapsed_time(end) / args.steps
-    # compute idle between consecutive steps (0 when the copies are hidden)
-    idle = [comp_ev[i][1].elapsed_time(comp_ev[i + 1][0]) for i in range(args.steps - 1)]
-    comp_overlap_ms = statistics.median(e[0].elapsed_time(e[1]) for e in comp_ev.values())
-    h2d_overlap_ms = statistics.median(e[2].elapsed_time(e[3]) for e in comp_ev.values())
-    d2h_overlap_ms = statistics.median(e[4].elapsed_time(e[5]) for e in comp_ev.values())
+    # The loop runs E2E_REPS times and the median repetition is reported, with
+    # every repetition's time and longest compute gap: on a machine shared with
+    # other jobs a single repetition has shown one gap of ~29 ms while the host
+    # had long since enqueued every step.
+    reps = []
+    for _ in range(E2E_REPS):
+        in_ready.clear(); comp_done.clear(); out_done.clear(); comp_ev.clear()
+        comp_ev.update({i: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+                        for i in range(args.steps)})
+        torch.cuda.synchronize(dev)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(s_in)
+        h0 = time.perf_counter()
+        for i in range(args.steps):
+            step(i)
+        host_issue_ms = (time.perf_counter() - h0) * 1e3
+        # the end event follows the last copy of every stream
+        s_in.wait_stream(s_comp); s_in.wait_stream(s_out)
+        end.record(s_in)
+        torch.cuda.synchronize(dev)
+        # compute idle between consecutive steps (0 when the copies are hidden)
+        idle = [comp_ev[i][1].elapsed_time(comp_ev[i + 1][0]) for i in range(args.steps - 1)]
+        reps.append({
+            "ms": start.elapsed_time(end) / args.steps,
+            "idle_med": statistics.median(idle) if idle else 0.0,
+            "idle_max": max(idle) if idle else 0.0,
+            "fill": start.elapsed_time(comp_ev[0][0]),
+            "drain": comp_ev[args.steps - 1][1].elapsed_time(end),
+            "host": host_issue_ms,
+            "comp": statistics.median(e[0].elapsed_time(e[1]) for e in comp_ev.values()),
+            "h2d": statistics.median(e[2].elapsed_time(e[3]) for e in comp_ev.values()),
+            "d2h": statistics.median(e[4].elapsed_time(e[5]) for e in comp_ev.values()),
+        })
+    rep = sorted(reps, key=lambda r: r["ms"])[len(reps) // 2]
+    ms = rep["ms"]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     nbytes = hq.numel() * hq.element_size()
     return {"value": world * w.fwd_bwd_flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -786,14 +805,16 @@ def measure_e2e(args, w, dev, fa, fused=False):
                      "h2d_gbs": 4 * nbytes / (h2d_ms * 1e-3) / 1e9,
                      "d2h_gbs": 4 * nbytes / (d2h_ms * 1e-3) / 1e9,
                      "compute_alone_ms": comp_ms,
-                     "compute_during_copies_ms": comp_overlap_ms,
-                     "h2d_during_compute_ms": h2d_overlap_ms,
-                     "d2h_during_compute_ms": d2h_overlap_ms,
-                     "compute_idle_between_steps_ms": statistics.median(idle) if idle else 0.0,
-                     "compute_idle_max_ms": max(idle) if idle else 0.0,
-                     "fill_ms": start.elapsed_time(comp_ev[0][0]),
-                     "drain_ms": comp_ev[args.steps - 1][1].elapsed_time(end),
-                     "host_issue_ms": host_issue_ms,
+                     "compute_during_copies_ms": rep["comp"],
+                     "h2d_during_compute_ms": rep["h2d"],
+                     "d2h_during_compute_ms": rep["d2h"],
+                     "compute_idle_between_steps_ms": rep["idle_med"],
+                     "compute_idle_max_ms": rep["idle_max"],
+                     "fill_ms": rep["fill"],
+                     "drain_ms": rep["drain"],
+                     "host_issue_ms": rep["host"],
+                     "repetitions_ms_per_step": [r["ms"] for r in reps],
+                     "repetitions_compute_idle_max_ms": [r["idle_max"] for r in reps],
                      "clocks": "not sampled in this region (nvidia-smi polling stalls its "
                                "copies); see the line's clocks",
                      "bound_ms": max(comp_ms, h2d_ms, d2h_ms),
@@ -801,7 +822,8 @@ def measure_e2e(args, w, dev, fa, fused=False):
                              "compute alone on the same device buffers; with full overlap "
                              "a step takes max of the three; the *_during_* times and the compute "
                              "idle between steps are medians over the timed end-to-end steps "
-                             "(compute_idle_max_ms the longest gap); fill_ms / drain_ms: start to "
+                             "(compute_idle_max_ms the longest gap) of the median repetition of "
+                             "E2E_REPS, whose times are listed; fill_ms / drain_ms: start to "
                              "the first step's compute, last step's compute to the end; "
                              "host_issue_ms is the host time to enqueue all timed steps"}}
 
