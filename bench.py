@@ -57,10 +57,10 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # on; a changed source gives null.  Figures come from the summaries under
 # profiles/.
 MEASURED_TRAFFIC = {
-    # bwd_dkdv_tc_kernel<bf16,128>: 394.6 MB per launch measured on 16 heads,
+    # bwd_dkdv_tc_kernel<bf16,128>: 393.8 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
-    ("dkdv", "28310b903eaa7175eb42420417c60a2eab20d688f112556c0fb20b671c964aab",
-     "long-bf16-B1-H32-N16384-D128-causal"): 789.2e6,
+    ("dkdv", "06b6ebce08f5a9277b0bc24bcf4ebda9a73b2c5d8e06476b28f3fd66af9aa34e",
+     "long-bf16-B1-H32-N16384-D128-causal"): 787.6e6,
     # bwd_fused_tc_kernel<bf16,128>: 2929.2 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch
     ("fused", "7a40ac2fd235fad28a6a7f44662e8e368ab7a4b4121be356c5b381d64da86cd1",

@@ -319,9 +319,11 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    // Issued from one lane: the whole-warp form of the other kernels ran this
-    // kernel about 3 % slower, its pace being set by the elementwise warps.
-    if (lane == 0) {
+    // The whole warp runs the issue loop and its waits (warp-uniform loop
+    // control and descriptor arithmetic); one elected lane issues the
+    // products and commits.
+    {
+      const bool leader = elect_one();
       const uint32_t idS = idesc_f16<T>(128, C::BT, false, false);
       const uint32_t idG = idesc_f16<T>(128, D, false, true);
       const uint64_t dK0 = sdesc_sw128(smem_u32(sK), 16, 1024);
@@ -335,22 +337,22 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_ST, dK0 + off, q + off, idS, kk > 0 ? 1u : 0u);
+          if (leader) mma_ss(tmem + C::COL_ST, dK0 + off, q + off, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(b_sfull);
+        if (leader) mma_commit(b_sfull);
       };
       auto issue_DPT = [&](int ds) {  // dP^T = V dO^T
         const uint64_t g = dDk + static_cast<uint64_t>((ds * C::DSLOT) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::CHUNK + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::COL_DPT, dV0 + off, g + off, idS, kk > 0 ? 1u : 0u);
+          if (leader) mma_ss(tmem + C::COL_DPT, dV0 + off, g + off, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(b_dpfull);
+        if (leader) mma_commit(b_dpfull);
       };
-      bool ok = wait_bounded(b_kv, 0, ctl, a.status, a.timeout_ns) &&
-                wait_bounded(b_qfull0, 0, ctl, a.status, a.timeout_ns) &&
-                wait_bounded(b_dfull0, 0, ctl, a.status, a.timeout_ns);
+      bool ok = wait_warp(b_kv, 0, ctl, a.status, a.timeout_ns) &&
+                wait_warp(b_qfull0, 0, ctl, a.status, a.timeout_ns) &&
+                wait_warp(b_dfull0, 0, ctl, a.status, a.timeout_ns);
       if (ok) {
         tc_fence_after();
         issue_ST(0);
@@ -363,17 +365,17 @@ __global__ void __launch_bounds__(320, 1)
         // dV += P^T dO (B: this tile's dO read MN-major, N = d)
         const uint64_t mdo = dDm + static_cast<uint64_t>((ds * C::DSLOT) >> 4);
         for (int h = 0; ok && h < 2; ++h) {
-          if (!(ok = h > 0 || wait_bounded(b_pready0, it & 1, ctl, a.status, a.timeout_ns))) break;
+          if (!(ok = h > 0 || wait_warp(b_pready0, it & 1, ctl, a.status, a.timeout_ns))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + C::COL_DV, tmem + C::COL_ST + 64 * h + 8 * kk,
+            if (leader) mma_ts(tmem + C::COL_DV, tmem + C::COL_ST + 64 * h + 8 * kk,
                    mdo + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
                    (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
         if (next) {
-          if (!(ok = wait_bounded(b_qfull0 + 8 * qs1, ((it + 1) / C::NQ) & 1, ctl, a.status,
+          if (!(ok = wait_warp(b_qfull0 + 8 * qs1, ((it + 1) / C::NQ) & 1, ctl, a.status,
                                   a.timeout_ns)))
             break;
           tc_fence_after();
@@ -382,27 +384,27 @@ __global__ void __launch_bounds__(320, 1)
         // dK += dS^T Q (B: this tile's Q read MN-major)
         const uint64_t mq = dQm + static_cast<uint64_t>((qs * C::TILE) >> 4);
         for (int h = 0; ok && h < 2; ++h) {
-          if (!(ok = h > 0 || wait_bounded(b_dsready0, it & 1, ctl, a.status, a.timeout_ns))) break;
+          if (!(ok = h > 0 || wait_warp(b_dsready0, it & 1, ctl, a.status, a.timeout_ns))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + C::COL_DK, tmem + C::COL_DPT + 64 * h + 8 * kk,
+            if (leader) mma_ts(tmem + C::COL_DK, tmem + C::COL_DPT + 64 * h + 8 * kk,
                    mq + static_cast<uint64_t>(((64 * h + 16 * kk) * 128) >> 4), idG,
                    (it > 0 || h > 0 || kk > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        mma_commit(b_qempty0 + 8 * qs);
-        mma_commit(b_dempty0 + 8 * ds);
+        if (leader) mma_commit(b_qempty0 + 8 * qs);
+        if (leader) mma_commit(b_dempty0 + 8 * ds);
         if (next) {
-          if (!(ok = wait_bounded(b_dfull0 + 8 * ds1, ((it + 1) / C::ND) & 1, ctl, a.status,
+          if (!(ok = wait_warp(b_dfull0 + 8 * ds1, ((it + 1) / C::ND) & 1, ctl, a.status,
                                   a.timeout_ns)))
             break;
           tc_fence_after();
           issue_DPT(ds1);
         }
       }
-      if (ok) mma_commit(b_accdone);
-      mma_commit(b_mmadone);
+      if (ok && leader) mma_commit(b_accdone);
+      if (leader) mma_commit(b_mmadone);
       wait_bounded(b_mmadone, 0, ctl, a.status, a.timeout_ns, false);
     }
     __syncwarp();
