@@ -58,8 +58,9 @@ METRIC = "attention TFLOP/s fwd & fwd+bwd, bf16 N=1k-16k, % of GB300 dense BF16 
 # profiles/.
 MEASURED_TRAFFIC = {
     # bwd_dkdv_tc_kernel<bf16,128>: 393.8 MB per launch measured on 16 heads,
-    # scaled by heads to the 32-head launch
-    ("dkdv", "06b6ebce08f5a9277b0bc24bcf4ebda9a73b2c5d8e06476b28f3fd66af9aa34e",
+    # scaled by heads to the 32-head launch (captured on source 06b6ebce...;
+    # the file has changed since only in a comment)
+    ("dkdv", "18895767631bca8a5cc47774cca7d10a7d5df65cee57a74897e0cc0d0d05f17c",
      "long-bf16-B1-H32-N16384-D128-causal"): 787.6e6,
     # bwd_fused_tc_kernel<bf16,128>: 2929.2 MB per launch measured on 16 heads,
     # scaled by heads to the 32-head launch

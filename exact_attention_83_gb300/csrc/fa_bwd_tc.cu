@@ -22,7 +22,8 @@
 // Warp roles (320 threads): warps 0-3 and 4-7 are two elementwise warpgroups
 // that split the 128 columns of each score tile (64 each; one TMEM lane = one
 // row per thread); warp 8 is the TMA producer and owns the TMEM allocation;
-// warp 9 issues the MMAs from one thread.  Each elementwise warpgroup writes
+// warp 9 issues the MMAs (the whole warp runs the issue loop, one elected
+// lane issues).  Each elementwise warpgroup writes
 // its rounded P^T / dS into the TMEM columns it alone reads, so the two never
 // race.  Both warpgroups release a product's operand on one barrier (256
 // arrivals), so the MMA thread waits once per product: the two halves are

@@ -29,7 +29,8 @@
 // K/V tile load.
 // Warps 0-3: softmax + epilogue of query tile 0 (one TMEM lane = one row per
 // thread); warps 4-7: the same for query tile 1; warp 8: TMA producer (lane 0)
-// and TMEM allocation; warp 9: MMA issuer (lane 0).  TMEM columns: S0 [0,128),
+// and TMEM allocation; warp 9: MMA issuer (the whole warp runs the issue loop,
+// one elected lane issues).  TMEM columns: S0 [0,128),
 // S1 [128,256), O0 [256,256+D), O1 [256+D,256+2D); P (input type, packed two
 // per column) overwrites the first 64 columns of its S after S is read.
 // The MMA issue order S0_0, S1_0, {PV0_j, S0_j+1, PV1_j, S1_j+1} lets one
